@@ -1,0 +1,396 @@
+/*
+ * spec_verify_ref.c -- CPU oracle (fp64) for batched speculative-sampling verification.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py, never by the CUDA library.  It
+ * shares no code with the CUDA path.  Plain, slow and written to be checked
+ * by eye against the pages:
+ *
+ *  [LEV]  "Fast Inference from Transformers via Speculative Decoding" (paper
+ *         review page), section "Speculative Sampling", Algorithm 1
+ *         SpeculativeDecodingStep, and section "Method: Speculative Decoding"
+ *         (temperature / top-k / nucleus / argmax all become standard sampling
+ *         from an adjusted distribution; argmax zeroes the non-max entries).
+ *  [SUR]  "投机解码（Speculative Decoding）" survey page, section 2 (lossless
+ *         acceptance rule, residual p' = norm(max(0, p - q))), section 4
+ *         (speculative_step pseudocode: left-to-right, stop at first rejection,
+ *         bonus from p_{gamma+1}).
+ *  [AGW]  "Speculative decoding: the art of guessing well", section 投机采样
+ *         (alpha = sum_x min(p, q); the `verify` listing: accept iff
+ *         uniform < min(1, p/q); first rejection = argmin(append(accepted, False));
+ *         q_{gamma+1} treated as zero so the residual becomes p_{gamma+1}).
+ *  [PHX]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+ *         1, 2, 3", SC'11 -- the Philox4x32-10 block function.
+ *
+ * Readings taken where the pages are silent (each one also listed in the design doc):
+ *  - normalisation order: temperature, softmax, top-k, renormalise, top-p,
+ *    renormalise; ties in top-k / top-p / argmax go to the lower token id;
+ *    the top-p set is the shortest descending prefix whose mass reaches top_p
+ *    (the crossing token is kept);
+ *  - acceptance is the strict test u * q(x) < p(x) (no division), so a draft
+ *    token with q(x) = 0 is accepted iff p(x) > 0;
+ *  - the residual / bonus draw is an inverse CDF in ascending token id with
+ *    v = u * Z, Z = sum_x max(0, p - q); if Z <= 0 the draw falls back to p;
+ *  - randomness: u = U(seed, b, pos, draw), draw 0 = acceptance at pos,
+ *    draw 1 = residual/bonus at pos, pos 1-based.
+ */
+#include "spec_verify_ref.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* Philox4x32-10 [PHX].  Parity: pinned only statistically (uniformity,       */
+/* independence and bijectivity tests) and by agreement with the separately   */
+/* written device copy; no published known-answer vector is stored here.      */
+/* ------------------------------------------------------------------------- */
+
+#define PHX_M0 0xD2511F53u /* round multipliers [PHX] */
+#define PHX_M1 0xCD9E8D57u
+#define PHX_W0 0x9E3779B9u /* Weyl key increments [PHX]: golden ratio, sqrt(3)-1 */
+#define PHX_W1 0xBB67AE85u
+
+void svr_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) { /* the key is bumped before every round but the first */
+            k0 += PHX_W0;
+            k1 += PHX_W1;
+        }
+        uint64_t prod0 = (uint64_t)PHX_M0 * (uint64_t)x0;
+        uint64_t prod1 = (uint64_t)PHX_M1 * (uint64_t)x2;
+        uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+        uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+        uint32_t y0 = hi1 ^ x1 ^ k0;
+        uint32_t y1 = lo1;
+        uint32_t y2 = hi0 ^ x3 ^ k1;
+        uint32_t y3 = lo0;
+        x0 = y0;
+        x1 = y1;
+        x2 = y2;
+        x3 = y3;
+    }
+    out[0] = x0;
+    out[1] = x1;
+    out[2] = x2;
+    out[3] = x3;
+}
+
+/* u = ((w0 >> 8) + 1/2) * 2^-24: strictly inside (0,1), exact in fp32 and fp64. */
+double svr_uniform(uint64_t seed, uint32_t b, uint32_t pos, uint32_t draw) {
+    uint32_t ctr[4] = {b, pos, draw, 0u};
+    uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    svr_philox4x32_10(ctr, key, out);
+    return ((double)(out[0] >> 8) + 0.5) / 16777216.0;
+}
+
+void svr_philox_uniforms(uint64_t seed, int B, int G, double* u_accept, double* u_resid) {
+    for (int b = 0; b < B; ++b) {
+        for (int i = 0; i < G; ++i) u_accept[(size_t)b * G + i] = svr_uniform(seed, (uint32_t)b, (uint32_t)(i + 1), 0u);
+        for (int j = 0; j <= G; ++j)
+            u_resid[(size_t)b * (G + 1) + j] = svr_uniform(seed, (uint32_t)b, (uint32_t)(j + 1), 1u);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Inputs                                                                     */
+/* ------------------------------------------------------------------------- */
+
+/* exact value of one stored logit, widened to double */
+static double logit_value(const void* base, int dtype, size_t idx) {
+    if (dtype == SVR_DTYPE_F32) return (double)((const float*)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16; /* bf16 = top half of an fp32 */
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Normalisation [LEV "Method": temperature / top-k / nucleus / argmax are all  */
+/* standard sampling from an adjusted distribution].                          */
+/* Parity: pinned by the softmax identity, argmax special case, brute force   */
+/* over all subsets for V <= 8, and the identity cases top_k = V, top_p = 1.  */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    double p;
+    int id;
+} ranked_t;
+
+/* descending probability, ascending token id on ties */
+static int ranked_cmp(const void* a, const void* b) {
+    const ranked_t* x = (const ranked_t*)a;
+    const ranked_t* y = (const ranked_t*)b;
+    if (x->p > y->p) return -1;
+    if (x->p < y->p) return 1;
+    return (x->id < y->id) ? -1 : (x->id > y->id);
+}
+
+int svr_normalise(const double* logits, int V, double T, int top_k, double top_p, double* probs,
+                  double* filter_margin) {
+    double margin = INFINITY;
+
+    /* the largest finite-or-minus-infinity logit; lowest id on ties */
+    int arg = -1;
+    for (int x = 0; x < V; ++x)
+        if (arg < 0 || logits[x] > logits[arg]) arg = x;
+    if (arg < 0 || !(logits[arg] > -INFINITY)) return -1;
+
+    if (T == 0.0) { /* argmax: zero the non-max entries and renormalise */
+        for (int x = 0; x < V; ++x) probs[x] = 0.0;
+        probs[arg] = 1.0;
+        if (filter_margin) *filter_margin = margin;
+        return 0;
+    }
+
+    /* temperature then softmax */
+    double m = logits[arg] / T;
+    double S = 0.0;
+    for (int x = 0; x < V; ++x) {
+        probs[x] = exp(logits[x] / T - m);
+        S += probs[x];
+    }
+    for (int x = 0; x < V; ++x) probs[x] /= S;
+
+    int use_k = (top_k > 0 && top_k < V);
+    int use_p = (top_p < 1.0);
+    if (use_k || use_p) {
+        ranked_t* order = (ranked_t*)malloc(sizeof(ranked_t) * (size_t)V);
+        for (int x = 0; x < V; ++x) {
+            order[x].p = probs[x];
+            order[x].id = x;
+        }
+        qsort(order, (size_t)V, sizeof(ranked_t), ranked_cmp);
+
+        if (use_k) { /* keep the k largest, renormalise */
+            double pk = order[top_k - 1].p, pn = order[top_k].p;
+            if (pn > 0.0 && pk > pn) margin = fmin(margin, (pk - pn) / pk);
+            double Sk = 0.0;
+            for (int r = 0; r < V; ++r) {
+                if (r < top_k)
+                    Sk += order[r].p;
+                else
+                    order[r].p = 0.0;
+            }
+            for (int r = 0; r < top_k; ++r) order[r].p /= Sk;
+        }
+        if (use_p) { /* shortest descending prefix with mass >= top_p, crossing token kept */
+            int keep = V;
+            double cum = 0.0, before = 0.0;
+            for (int r = 0; r < V; ++r) {
+                if (order[r].p <= 0.0) {
+                    keep = r; /* mass exhausted by rounding before reaching top_p */
+                    break;
+                }
+                before = cum;
+                cum += order[r].p;
+                if (cum >= top_p) {
+                    keep = r + 1;
+                    margin = fmin(margin, fmin(cum - top_p, top_p - before));
+                    if (r + 1 < V && order[r + 1].p > 0.0 && order[r].p > order[r + 1].p)
+                        margin = fmin(margin, (order[r].p - order[r + 1].p) / order[r].p);
+                    break;
+                }
+            }
+            double Sp = 0.0;
+            for (int r = 0; r < V; ++r) {
+                if (r < keep)
+                    Sp += order[r].p;
+                else
+                    order[r].p = 0.0;
+            }
+            for (int r = 0; r < keep; ++r) order[r].p /= Sp;
+        }
+        for (int r = 0; r < V; ++r) probs[order[r].id] = order[r].p;
+        free(order);
+    }
+    if (filter_margin) *filter_margin = margin;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Residual / bonus draw [LEV Algorithm 1 steps 4-5; AGW `verify`]:           */
+/* r = max(0, p - q) (q := 0 for the bonus), inverse CDF in ascending id.      */
+/* Parity: pinned by the worked example of the SpecTr page (residual          */
+/* (0, .5, .5)), exact enumeration and chi-square of the output marginal.     */
+/* ------------------------------------------------------------------------- */
+
+static int residual_draw(const double* p, const double* q, int V, double u, double* margin_out) {
+    double Z = 0.0;
+    for (int x = 0; x < V; ++x) {
+        double r = p[x] - (q ? q[x] : 0.0);
+        if (r > 0.0) Z += r;
+    }
+    int fallback = !(Z > 0.0); /* p <= q everywhere: cannot follow a rejection exactly; use p */
+    if (fallback) {
+        Z = 0.0;
+        for (int x = 0; x < V; ++x) Z += p[x];
+    }
+    double v = u * Z;
+    double cum = 0.0, before = 0.0;
+    int token = -1, last_pos = -1;
+    for (int x = 0; x < V; ++x) {
+        double r = fallback ? p[x] : p[x] - (q ? q[x] : 0.0);
+        if (!(r > 0.0)) continue;
+        last_pos = x;
+        before = cum;
+        cum += r;
+        if (cum > v) {
+            token = x;
+            break;
+        }
+    }
+    double margin;
+    if (token < 0) { /* v beyond the accumulated total by rounding: last token with mass */
+        token = last_pos;
+        margin = 0.0;
+    } else {
+        margin = fmin(v - before, cum - v) / Z;
+    }
+    if (Z < 1e-12) margin = 0.0; /* residual made of rounding noise: no stable answer */
+    if (margin_out) *margin_out = margin;
+    return token;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Batched verification [LEV Algorithm 1; SUR section 4; AGW `verify`].       */
+/* ------------------------------------------------------------------------- */
+
+int svr_verify(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+               const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+               const float* top_p, const double* u_accept, const double* u_resid, int B, int G, int V,
+               int32_t* accepted_len, int32_t* out_tokens, double* alpha, int32_t* pos_accept,
+               int32_t* pos_token, double* p_out, double* q_out, uint32_t* status,
+               double* accept_margin, double* resid_margin, double* filter_margin) {
+    if (B < 0 || G < 1 || V < 1) return -1;
+    if (dtype != SVR_DTYPE_F32 && dtype != SVR_DTYPE_BF16) return -1;
+    if (B > 0 && (!target || !draft || !draft_tokens || !temperature || !u_accept || !u_resid ||
+                  !accepted_len || !out_tokens || !alpha))
+        return -1;
+    int all_positions = (pos_accept || pos_token || accept_margin || resid_margin);
+
+    double* logits = (double*)malloc(sizeof(double) * (size_t)V);
+    double* P = (double*)malloc(sizeof(double) * (size_t)V * (size_t)(G + 1)); /* p_1..p_{G+1} */
+    double* Q = (double*)malloc(sizeof(double) * (size_t)V * (size_t)G);       /* q_1..q_G */
+
+    for (int b = 0; b < B; ++b) {
+        uint32_t st = 0;
+        int gamma = num_draft ? num_draft[b] : G;
+        double T = (double)temperature[b];
+        int k = top_k ? top_k[b] : 0;
+        double tp = top_p ? (double)top_p[b] : 1.0;
+        if (!(T >= 0.0) || isinf(T)) st |= SVR_ST_BAD_TEMPERATURE;
+        if (k < 0) st |= SVR_ST_BAD_TOP_K;
+        if (!(tp > 0.0 && tp <= 1.0)) st |= SVR_ST_BAD_TOP_P;
+        if (gamma < 1 || gamma > G) st |= SVR_ST_BAD_NUM_DRAFT;
+        if (!(st & SVR_ST_BAD_NUM_DRAFT))
+            for (int i = 0; i < gamma; ++i) {
+                int32_t x = draft_tokens[(size_t)b * G + i];
+                if (x < 0 || x >= V) st |= SVR_ST_BAD_DRAFT_TOKEN;
+            }
+
+        /* normalise the rows in use: target rows 0..gamma, draft rows 0..gamma-1 */
+        if (!st) {
+            for (int row = 0; row < 2 * gamma + 1 && !st; ++row) {
+                int is_target = row <= gamma;
+                int r = is_target ? row : row - gamma - 1;
+                const void* src = is_target ? target : draft;
+                size_t base = is_target ? ((size_t)b * (G + 1) + r) * (size_t)V : ((size_t)b * G + r) * (size_t)V;
+                for (int x = 0; x < V; ++x) {
+                    logits[x] = logit_value(src, dtype, base + x);
+                    if (isnan(logits[x]) || logits[x] == INFINITY) st |= SVR_ST_NONFINITE;
+                }
+                if (st) break;
+                double fm = INFINITY;
+                double* dst = is_target ? P + (size_t)r * V : Q + (size_t)r * V;
+                if (svr_normalise(logits, V, T, k, tp, dst, &fm) != 0) st |= SVR_ST_NONFINITE;
+                if (filter_margin) filter_margin[(size_t)b * (2 * G + 1) + (is_target ? r : G + 1 + r)] = fm;
+            }
+        }
+        if (status) status[b] = st;
+
+        /* defaults: nothing accepted, no token, zero alpha, undefined positions */
+        accepted_len[b] = 0;
+        for (int j = 0; j <= G; ++j) out_tokens[(size_t)b * (G + 1) + j] = -1;
+        for (int i = 0; i < G; ++i) alpha[(size_t)b * G + i] = 0.0;
+        if (pos_accept)
+            for (int i = 0; i < G; ++i) pos_accept[(size_t)b * G + i] = -1;
+        if (pos_token)
+            for (int j = 0; j <= G; ++j) pos_token[(size_t)b * (G + 1) + j] = -1;
+        if (accept_margin)
+            for (int i = 0; i < G; ++i) accept_margin[(size_t)b * G + i] = NAN;
+        if (resid_margin)
+            for (int j = 0; j <= G; ++j) resid_margin[(size_t)b * (G + 1) + j] = NAN;
+        if (filter_margin && st)
+            for (int r = 0; r < 2 * G + 1; ++r) filter_margin[(size_t)b * (2 * G + 1) + r] = NAN;
+        if (p_out) memset(p_out + (size_t)b * (G + 1) * V, 0, sizeof(double) * (size_t)(G + 1) * V);
+        if (q_out) memset(q_out + (size_t)b * G * V, 0, sizeof(double) * (size_t)G * V);
+        if (st) continue;
+
+        if (p_out) memcpy(p_out + (size_t)b * (G + 1) * V, P, sizeof(double) * (size_t)(gamma + 1) * V);
+        if (q_out) memcpy(q_out + (size_t)b * G * V, Q, sizeof(double) * (size_t)gamma * V);
+
+        /* per-position acceptance rate alpha_i = sum_x min(p_i(x), q_i(x)) [AGW 投机采样] */
+        for (int i = 0; i < gamma; ++i) {
+            double a = 0.0;
+            for (int x = 0; x < V; ++x) a += fmin(P[(size_t)i * V + x], Q[(size_t)i * V + x]);
+            alpha[(size_t)b * G + i] = a;
+        }
+
+        /* acceptance test left to right, stop at the first rejection [LEV Alg. 1 step 3] */
+        int n = gamma;
+        for (int i = 0; i < gamma; ++i) {
+            int x = draft_tokens[(size_t)b * G + i];
+            double px = P[(size_t)i * V + x], qx = Q[(size_t)i * V + x];
+            double u = u_accept[(size_t)b * G + i];
+            int accept = (u * qx < px);
+            if (accept_margin) accept_margin[(size_t)b * G + i] = (qx > 0.0) ? fabs(u - px / qx) : INFINITY;
+            if (pos_accept) pos_accept[(size_t)b * G + i] = accept;
+            if (!accept && n == gamma) {
+                n = i;
+                if (!all_positions) break;
+            }
+        }
+
+        /* residual at position n+1, or the bonus from p_{gamma+1} [LEV Alg. 1 steps 4-5] */
+        for (int j = 0; j <= gamma; ++j) {
+            if (!all_positions && j != n) continue;
+            const double* pj = P + (size_t)j * V;
+            const double* qj = (j < gamma) ? Q + (size_t)j * V : NULL; /* q_{gamma+1} := 0 */
+            double rm = 0.0;
+            int tok = residual_draw(pj, qj, V, u_resid[(size_t)b * (G + 1) + j], &rm);
+            if (pos_token) pos_token[(size_t)b * (G + 1) + j] = tok;
+            if (resid_margin) resid_margin[(size_t)b * (G + 1) + j] = rm;
+            if (j == n) {
+                for (int i = 0; i < n; ++i) out_tokens[(size_t)b * (G + 1) + i] = draft_tokens[(size_t)b * G + i];
+                out_tokens[(size_t)b * (G + 1) + n] = tok;
+                accepted_len[b] = n;
+            }
+        }
+    }
+    free(logits);
+    free(P);
+    free(Q);
+    return 0;
+}
+
+int svr_verify_seeded(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                      const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+                      const float* top_p, uint64_t seed, int B, int G, int V, int32_t* accepted_len,
+                      int32_t* out_tokens, double* alpha, int32_t* pos_accept, int32_t* pos_token,
+                      double* p_out, double* q_out, uint32_t* status, double* accept_margin,
+                      double* resid_margin, double* filter_margin) {
+    if (B < 0 || G < 1) return -1;
+    double* ua = (double*)malloc(sizeof(double) * (size_t)(B > 0 ? B : 1) * (size_t)G);
+    double* ur = (double*)malloc(sizeof(double) * (size_t)(B > 0 ? B : 1) * (size_t)(G + 1));
+    svr_philox_uniforms(seed, B, G, ua, ur);
+    int rc = svr_verify(target, draft, dtype, draft_tokens, num_draft, temperature, top_k, top_p, ua, ur, B, G,
+                        V, accepted_len, out_tokens, alpha, pos_accept, pos_token, p_out, q_out, status,
+                        accept_margin, resid_margin, filter_margin);
+    free(ua);
+    free(ur);
+    return rc;
+}

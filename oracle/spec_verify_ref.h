@@ -1,0 +1,97 @@
+/*
+ * spec_verify_ref.h -- CPU oracle for batched speculative-sampling verification.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py may load or call this code.  The
+ * product path (the CUDA library) never links, loads or calls it, and this
+ * oracle shares no code, header, constant table or helper with it.
+ *
+ * Everything here is plain, slow, fp64 C written from the pages:
+ *   - "Fast Inference from Transformers via Speculative Decoding" review pages
+ *     (Algorithm 1 "SpeculativeDecodingStep"; section "Speculative Sampling"),
+ *   - the speculative-decoding survey page, section 4 (speculative_step),
+ *   - "Speculative decoding: the art of guessing well", section 投机采样
+ *     (the `verify` listing: bonus token via q_{gamma+1} := 0).
+ * The Philox4x32-10 generator follows Salmon, Moraes, Dror and Shaw,
+ * "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11).
+ *
+ * Parity status of each function is given in its comment in the .c file.
+ */
+#ifndef SPEC_VERIFY_REF_H
+#define SPEC_VERIFY_REF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* logits storage types accepted by the oracle */
+#define SVR_DTYPE_F32 0
+#define SVR_DTYPE_BF16 1
+
+/* per-sequence status bits (same values as the library's contract) */
+#define SVR_ST_BAD_TEMPERATURE 0x01u
+#define SVR_ST_BAD_TOP_K 0x02u
+#define SVR_ST_BAD_TOP_P 0x04u
+#define SVR_ST_BAD_NUM_DRAFT 0x08u
+#define SVR_ST_BAD_DRAFT_TOKEN 0x10u
+#define SVR_ST_NONFINITE 0x20u
+
+/* Philox4x32-10 block function: ctr[4], key[2] -> out[4]. */
+void svr_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* Uniform in (0,1) on the 24-bit grid from counter (b, pos, draw, 0) and key = seed. */
+double svr_uniform(uint64_t seed, uint32_t b, uint32_t pos, uint32_t draw);
+
+/* Fill u_accept[B*G] (draw 0, pos = 1..G) and u_resid[B*(G+1)] (draw 1, pos = 1..G+1). */
+void svr_philox_uniforms(uint64_t seed, int B, int G, double* u_accept, double* u_resid);
+
+/* Normalise one row of logits into probabilities (temperature, then top-k, then top-p).
+ * T == 0 gives the one-hot argmax (lowest id on ties).  top_k <= 0 or >= V: off.
+ * top_p >= 1: off.  Returns 0, or -1 if the row has no finite maximum.
+ * filter_margin (may be NULL) receives the smallest margin of the filter decisions. */
+int svr_normalise(const double* logits, int V, double T, int top_k, double top_p, double* probs,
+                  double* filter_margin);
+
+/* The verification step for a batch, with the uniforms passed in.
+ *
+ * target: [B, G+1, V] logits, draft: [B, G, V] logits (dtype SVR_DTYPE_*)
+ * draft_tokens [B, G]; num_draft [B] (NULL = all G); temperature [B];
+ * top_k [B] (NULL = off); top_p [B] (NULL = off).
+ * u_accept [B, G]: uniform for the acceptance test at position i (1-based i = index+1)
+ * u_resid [B, G+1]: uniform for the residual / bonus draw at position j.
+ *
+ * Outputs: accepted_len [B], out_tokens [B, G+1], alpha [B, G].
+ * Optional outputs (NULL to skip):
+ *   pos_accept [B, G]   acceptance decision at every position 1..gamma_b (-1 beyond)
+ *   pos_token  [B, G+1] residual/bonus token that position j would emit (-1 beyond)
+ *   p_out [B, G+1, V], q_out [B, G, V]  normalised probabilities (0 beyond gamma_b)
+ *   status [B]          SVR_ST_* bits
+ *   accept_margin [B, G]  |u - p/q| of each acceptance decision (+inf if q(x) = 0)
+ *   resid_margin [B, G+1] distance of v/Z to the nearest CDF edge of the chosen token
+ *   filter_margin [B, 2G+1] smallest filter-boundary margin per row
+ *                           (target rows 0..G, then draft rows 0..G-1)
+ * When any of pos_accept / pos_token / accept_margin / resid_margin is given, every
+ * position is evaluated; the main outputs are unchanged by that.
+ * Returns 0, or a negative value on a bad argument. */
+int svr_verify(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+               const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+               const float* top_p, const double* u_accept, const double* u_resid, int B, int G, int V,
+               int32_t* accepted_len, int32_t* out_tokens, double* alpha, int32_t* pos_accept,
+               int32_t* pos_token, double* p_out, double* q_out, uint32_t* status,
+               double* accept_margin, double* resid_margin, double* filter_margin);
+
+/* Same, drawing the uniforms from the Philox stream keyed by (seed, b, pos, draw). */
+int svr_verify_seeded(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                      const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+                      const float* top_p, uint64_t seed, int B, int G, int V, int32_t* accepted_len,
+                      int32_t* out_tokens, double* alpha, int32_t* pos_accept, int32_t* pos_token,
+                      double* p_out, double* q_out, uint32_t* status, double* accept_margin,
+                      double* resid_margin, double* filter_margin);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
