@@ -1,0 +1,331 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched speculative-sampling verification step on GB300.
+
+One step = one spec_verify call over one batch of the workload (every row of
+the batch normalised, alpha for every position, acceptance, first rejection,
+residual/bonus draw).  Default workload: B=256, gamma=7, V=128256, bf16
+logits, T=1, top-k 50 then top-p 0.9 (the 128k-vocabulary configuration the
+throughput target is stated on).  Metric: verified draft positions per second
+(sum_b gamma_b per call / call time), with the achieved HBM GB/s of the
+dominant kernel against the measured copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU (under torchrun): every rank verifies its own batch (weak scaling;
+sequences are independent, so no collective touches the data path); the
+reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "positions/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("speculative_decoding_verification_20_gb300/csrc/sv_stream.cu",
+                  "speculative_decoding_verification_20_gb300/csrc/sv_internal.cuh",
+                  "speculative_decoding_verification_20_gb300/csrc/sv_finalize.cuh")
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    valid only while the kernel sources are unchanged since that capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("kernel_hash") != kernel_hash():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t_begin: float, t_end: float):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        loaded = [s for s, _, _ in rows if s > 0]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(m for _, m, _ in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(workload: str, budget_s: float = 12.0):
+    """The fp64 oracle, as it stands, single-threaded on this host, on a bounded
+    sample of the same workload (whole sequences, same recipe)."""
+    import oracle
+    from speculative_decoding_verification_20_gb300 import workloads
+
+    oracle.build()
+    n = 1
+    elapsed, positions = 0.0, 0
+    batches = 0
+    while elapsed < budget_s and batches < 64:
+        wl = workloads.make(workload, seed=10_000 + batches, B=n)
+        ni = wl.numpy_inputs()
+        t0 = time.perf_counter()
+        oracle.verify(ni["target"], ni["draft"], ni["draft_tokens"], ni["temperature"], ni["num_draft"], ni["top_k"],
+                      ni["top_p"], seed=wl.seed)
+        elapsed += time.perf_counter() - t0
+        positions += wl.positions()
+        batches += 1
+    return {"value": positions / elapsed, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{batches} whole sequences of the {workload} recipe ({positions} positions, "
+                      f"{elapsed:.1f} s of single-threaded fp64 oracle time)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from speculative_decoding_verification_20_gb300 import workloads
+
+    oracle.build()
+    per_step_seq = 1
+    times, positions = [], 0
+    for step in range(args.warmup + args.steps):
+        wl = workloads.make(args.workload, seed=20_000 + step, B=per_step_seq)
+        ni = wl.numpy_inputs()
+        t0 = time.perf_counter()
+        oracle.verify(ni["target"], ni["draft"], ni["draft_tokens"], ni["temperature"], ni["num_draft"], ni["top_k"],
+                      ni["top_p"], seed=wl.seed)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            positions += wl.positions()
+    total = sum(times)
+    value = positions / total
+    cfg = workload_config(args.workload)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(len(times), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step verifies {per_step_seq} whole sequence(s) of the {args.workload} "
+                                       f"recipe with the single-threaded fp64 oracle"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(name: str) -> dict:
+    from speculative_decoding_verification_20_gb300.workloads import CONFIGS
+
+    c = dict(CONFIGS[name])
+    filt = {"v128k": "T=1, top-k 50 then top-p 0.9", "v32k": "T=0.8, no filter", "b1024": "T=1, no filter",
+            "tiny": "T=1, no filter", "ragged": "T in {0,.3,.7,1,1.2}, top-p U[.8,1]"}[name]
+    return {"workload": f"{name}: B={c['B']}, gamma={c['G']}{' (ragged 1..8)' if name == 'ragged' else ''}, "
+                        f"V={c['V']}, {c['dtype']} logits, {filt}",
+            "B": c["B"], "gamma": c["G"], "V": c["V"], "logits": c["dtype"]}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="v128k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_verification_20_gb300 as sv
+    from speculative_decoding_verification_20_gb300 import _build, workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    sv.load_library()
+
+    wl = workloads.make(args.workload, seed=rank, device=dev)
+    B, G, V = wl.B, wl.G, wl.V
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.empty(sv.workspace_size(B, G, V, sv.SV_BF16 if wl.dtype == "bf16" else sv.SV_F32), dtype=torch.uint8,
+                     device=dev)
+
+    def step(seed, events=None):
+        return sv.spec_verify(wl.target, wl.draft, wl.draft_tokens, wl.temperature, wl.num_draft, wl.top_k, wl.top_p,
+                              seed=seed, workspace=ws, events=events)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    # per-step events around the dominant kernel, recorded by the library on the launching stream
+    main = "stream" if (wl.top_k is not None and int(wl.top_k.max()) <= sv.SV_STREAM_MAX_TOP_K) else "dense"
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    props = torch.cuda.get_device_properties(dev)
+    smi_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    with ClockSampler(smi_id) as clk:
+        wall0 = time.perf_counter()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(1_000_000 + i, events={main: kev[i]})
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall1 = time.perf_counter()
+    if world > 1:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+    t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    positions = wl.positions()
+    value = positions * world / (ms_step * 1e-3)
+    kernel_ms = [a.elapsed_time(b) for a, b in kev]
+    kernel_ms_avg = sum(kernel_ms) / len(kernel_ms)
+    bytes_per_launch = wl.logit_bytes()
+    achieved = bytes_per_launch / (kernel_ms_avg * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # end to end through the host-buffer entry point: pinned inputs in, results out, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        pin = lambda x: None if x is None else x.detach().cpu().contiguous().pin_memory()
+        h = [pin(x) for x in (wl.target, wl.draft, wl.draft_tokens, wl.temperature, wl.num_draft, wl.top_k,
+                               wl.top_p)]
+        staging = torch.empty(sv.host_staging_size(B, G, V, sv.SV_BF16 if wl.dtype == "bf16" else sv.SV_F32,
+                                                   h[4] is not None, h[5] is not None, h[6] is not None),
+                              dtype=torch.uint8, device=dev)
+        outs = None
+        for i in range(3):
+            outs = sv.spec_verify_host(*h, seed=i, staging=staging, outputs=outs)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        w0 = time.perf_counter()
+        for i in range(args.e2e_steps):
+            outs = sv.spec_verify_host(*h, seed=2_000_000 + i, staging=staging, outputs=outs)
+        w1 = time.perf_counter()
+        te = torch.tensor([w1 - w0], device=dev, dtype=torch.float64)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e_step = float(te.item()) / args.e2e_steps
+        h2d = sum(x.numel() * x.element_size() for x in h if x is not None)
+        d2h = sum(x.numel() * x.element_size() for x in outs.values())
+        e2e = {"value": positions * world / e_step, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e_step * 1e3}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    clocks = clk.summary(wall0, wall1)
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": dict(workload_config(args.workload),
+                       l2="inputs larger than L2: %.0f MB of logits per step vs 129 MB L2" % (bytes_per_launch / 1e6),
+                       parallelism=f"replicas x{world} (independent batches per GPU)"),
+        "hbm_gbs_step": bytes_per_launch / (ms_step * 1e-3) / 1e9,
+        "hbm_frac_step": bytes_per_launch / (ms_step * 1e-3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "kernel": "stream_kernel (streaming top-k path)" if main == "stream" else "dense_kernel (cluster path)",
+                     "kernel_ms": kernel_ms_avg, "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "traffic": traffic},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

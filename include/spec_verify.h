@@ -1,0 +1,177 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 batched speculative-sampling verification library.
+ *
+ * What one call computes (per sequence b of a batch, all on the GPU, no host sync):
+ *   1. normalise the target rows p_1..p_{gamma_b+1} and the draft rows q_1..q_{gamma_b}
+ *      the same way: temperature, softmax, top-k, renormalise, top-p, renormalise
+ *      ("Fast Inference from Transformers via Speculative Decoding" review page,
+ *      section "Method: Speculative Decoding": temperature / top-k / nucleus /
+ *      argmax are standard sampling from an adjusted distribution; argmax zeroes
+ *      the non-max entries);
+ *   2. alpha_i = sum_x min(p_i(x), q_i(x)) for i = 1..gamma_b
+ *      ("Speculative decoding: the art of guessing well", section 投机采样);
+ *   3. accept draft token x_i iff u_i * q_i(x_i) < p_i(x_i), u_i = U(seed, b, i, 0)
+ *      (same page, the `verify` listing: uniform < min(1, p/q));
+ *   4. n_b = number of draft tokens before the first rejection
+ *      (review page, Algorithm 1 SpeculativeDecodingStep, step 3);
+ *   5. one more token t drawn from norm(max(0, p_{n+1} - q_{n+1})) with
+ *      q_{gamma_b+1} := 0 (the bonus token when every draft was accepted) by an
+ *      inverse CDF in ascending token id with v = U(seed, b, n+1, 1) * Z
+ *      (Algorithm 1 steps 4-5; the `verify` listing's "treat it as zero").
+ * U(seed, b, pos, draw) = ((w >> 8) + 0.5) * 2^-24 with w = word 0 of
+ * Philox4x32-10(counter = (b, pos, draw, 0), key = (lo32(seed), hi32(seed))).
+ * Temperature 0 means greedy: p, q are one-hot at the argmax (lowest id on ties),
+ * so a draft token is accepted iff it is the target's argmax.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers unless the name says host.  The
+ *    caller owns every buffer; the library allocates nothing and keeps no
+ *    state between calls beyond the caller's workspace.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *    stream) and never synchronise with the host (spec_verify_host excepted).
+ *  - Argument errors return a negative SV_E* status before anything is
+ *    enqueued.  A failed launch returns SV_ECUDA.  Problems in the device-side
+ *    data of one sequence (bad per-row parameters, non-finite logits, draft
+ *    tokens out of range) never fail the call: that sequence gets
+ *    accepted_len = 0, out_tokens = -1, alpha = 0 and its SV_ROW_* bits in
+ *    row_status.
+ *  - Layouts are row-major, vocabulary innermost.  Logit arrays must start on
+ *    a 16-byte boundary.
+ *  - Results are deterministic for a given seed; callers advance the seed
+ *    every round.
+ *  - Calls on the same workspace must not overlap on the GPU.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+typedef enum {
+    SV_OK = 0,
+    SV_EINVAL = -1,       /* a bad argument (null pointer, bad size, misaligned logits) */
+    SV_EUNSUPPORTED = -2, /* unsupported combination (e.g. dtype) */
+    SV_ECUDA = -3,        /* a CUDA launch or runtime call failed */
+    SV_ETOO_LARGE = -4,   /* V, gamma_max or B beyond the supported maximum */
+    SV_EWORKSPACE = -5    /* workspace missing or smaller than spec_verify_workspace_size() */
+} sv_status;
+
+/* per-sequence bits written to row_status */
+#define SV_ROW_BAD_TEMPERATURE 0x01u /* temperature negative, NaN or infinite */
+#define SV_ROW_BAD_TOP_K 0x02u       /* top_k < 0 */
+#define SV_ROW_BAD_TOP_P 0x04u       /* top_p NaN, <= 0 or > 1 */
+#define SV_ROW_BAD_NUM_DRAFT 0x08u   /* num_draft outside [1, gamma_max] */
+#define SV_ROW_BAD_DRAFT_TOKEN 0x10u /* a draft token outside [0, V) */
+#define SV_ROW_NONFINITE 0x20u       /* NaN or +inf logit, or a row with no finite logit */
+
+/* supported maxima */
+#define SV_MAX_GAMMA 32
+#define SV_MAX_VOCAB 262144
+#define SV_MAX_BATCH 16777216
+
+/*
+ * Bytes of device workspace one call needs for this shape (a pure host
+ * function: no CUDA call).  The workspace may be reused by consecutive calls
+ * on one stream; it needs no initialisation.  Returns 0 for invalid shapes.
+ */
+size_t spec_verify_workspace_size(int B, int gamma_max, int V, int dtype);
+
+/*
+ * The batched verification step.
+ *
+ * target_logits [B, gamma_max+1, V]  dtype logits of the target model (row i = p_{i+1})
+ * draft_logits  [B, gamma_max, V]    dtype logits of the drafter (row i = q_{i+1})
+ * dtype                              SV_F32 or SV_BF16, both logit arrays
+ * draft_tokens  [B, gamma_max] int32 x_1..x_gamma; entries past gamma_b are ignored
+ * num_draft     [B] int32            gamma_b in [1, gamma_max], or NULL = all gamma_max
+ * temperature   [B] float            >= 0; 0 = greedy
+ * top_k         [B] int32            0 or >= V = off; NULL = off everywhere
+ * top_p         [B] float            in (0, 1], 1 = off; NULL = off everywhere
+ * seed                               Philox key for this call
+ * accepted_len  [B] int32 out        n_b in [0, gamma_b]; the round emits n_b + 1 tokens
+ * out_tokens    [B, gamma_max+1] int32 out  x_1..x_n, then the residual/bonus token, then -1
+ * alpha         [B, gamma_max] float out    alpha_i for i <= gamma_b, 0 beyond
+ * p_out         [B, gamma_max+1, V] float out or NULL: normalised target probabilities
+ * q_out         [B, gamma_max, V] float out or NULL: normalised draft probabilities
+ *               (debug outputs; rows past gamma_b are written as zeros)
+ * row_status    [B] uint32 out or NULL: SV_ROW_* bits, 0 = fine
+ * workspace, workspace_bytes         device scratch of spec_verify_workspace_size() bytes
+ * stream                             cudaStream_t
+ */
+int spec_verify(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                const int32_t* num_draft, const float* temperature, const int32_t* top_k, const float* top_p,
+                uint64_t seed, int B, int gamma_max, int V, int32_t* accepted_len, int32_t* out_tokens,
+                float* alpha, float* p_out, float* q_out, uint32_t* row_status, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* Path selection for spec_verify_ex (testing and measurement). */
+typedef enum {
+    SV_PATH_AUTO = 0,  /* greedy and top_k <= SV_STREAM_MAX_TOP_K rows: streaming top-k path; others: dense */
+    SV_PATH_DENSE = 1  /* every row through the dense (whole-row, cluster) path */
+} sv_path;
+
+#define SV_STREAM_MAX_TOP_K 256
+
+/*
+ * Extra, optional outputs and controls.  Zero-initialise, set struct_size =
+ * sizeof(sv_options), fill what you need.
+ *   pos_accept [B, gamma_max] int32: acceptance decision at every position
+ *              1..gamma_b, evaluated even after the first rejection (-1 beyond)
+ *   pos_token  [B, gamma_max+1] int32: the residual/bonus token each position
+ *              j would emit if the round stopped there (-1 beyond gamma_b+1)
+ *   path       sv_path
+ *   ev_stream  two cudaEvent_t (or NULL) recorded on `stream` immediately
+ *              before and after the streaming top-k kernel
+ *   ev_dense   the same around the dense cluster kernel
+ */
+typedef struct {
+    uint32_t struct_size;
+    int32_t* pos_accept;
+    int32_t* pos_token;
+    int32_t path;
+    void* ev_stream[2];
+    void* ev_dense[2];
+} sv_options;
+
+int spec_verify_ex(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                   const int32_t* num_draft, const float* temperature, const int32_t* top_k, const float* top_p,
+                   uint64_t seed, int B, int gamma_max, int V, int32_t* accepted_len, int32_t* out_tokens,
+                   float* alpha, float* p_out, float* q_out, uint32_t* row_status, void* workspace,
+                   size_t workspace_bytes, void* stream, const sv_options* options);
+
+/*
+ * Bytes of device staging that spec_verify_host needs (inputs and outputs
+ * copied through it) plus the workspace; a pure host function.
+ */
+size_t spec_verify_host_staging_size(int B, int gamma_max, int V, int dtype, int has_num_draft, int has_top_k,
+                                     int has_top_p);
+
+/*
+ * End-to-end form: the same computation on HOST buffers (pinned memory gives
+ * asynchronous copies).  Inputs are copied to `device_staging` with one
+ * cudaMemcpyAsync per array, spec_verify runs, the three outputs are copied
+ * back, and the call returns after cudaStreamSynchronize(stream).
+ * device_staging: device buffer of spec_verify_host_staging_size() bytes,
+ * 256-byte aligned.  Optional host arrays may be NULL as in spec_verify.
+ */
+int spec_verify_host(const void* host_target_logits, const void* host_draft_logits, int dtype,
+                     const int32_t* host_draft_tokens, const int32_t* host_num_draft,
+                     const float* host_temperature, const int32_t* host_top_k, const float* host_top_p,
+                     uint64_t seed, int B, int gamma_max, int V, int32_t* host_accepted_len,
+                     int32_t* host_out_tokens, float* host_alpha, void* device_staging, size_t staging_bytes,
+                     void* stream);
+
+/* A static English description of a status code. */
+const char* spec_verify_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,671 @@
+// sv_dense.cuh -- dense path: whole-row verification with a thread-block cluster per unit.
+//
+// A unit is (target row i, draft row i) for i <= gamma_b, or the bonus unit
+// (target row gamma_b+1 alone, q := 0).  The cluster's CTAs split the
+// vocabulary into contiguous column slices; every logit of the unit is read
+// from HBM once (16-byte loads) and stays in registers for all the passes:
+//   max            -> softmax with temperature via exp2 (one exponential per logit)
+//   radix select   -> top-k (count-weighted) then top-p (mass-weighted), ties by id
+//   alpha_i        =  sum_x min(p, q)
+//   acceptance     u * q(x) < p(x)
+//   residual/bonus inverse CDF in ascending token id (hierarchical search:
+//                  cluster prefix -> load group -> thread scan -> element).
+// Cross-CTA values move through distributed shared memory (DSMEM) with one
+// cluster barrier per exchange; partial sums are combined in fp64.
+// References: "Fast Inference from Transformers via Speculative Decoding"
+// review page (Algorithm 1; "Method" section on adjusted distributions) and
+// "Speculative decoding: the art of guessing well", section 投机采样.
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include "sv_finalize.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace sv {
+
+constexpr int kXch = 24;  // doubles per exchange slot
+
+struct DenseSmem {
+    float hist[16][kDenseThreads];  // per-thread histogram columns
+    double red[kDenseThreads / 32][kXch];
+    double xch[2][kXch];
+    double res[2 * kXch];
+};
+
+template <typename TIn, int R>
+struct DenseCfg {
+    static constexpr int NT = kDenseThreads;
+    static constexpr int VEC = 16 / (int)sizeof(TIn);
+    static constexpr int EPR = R * VEC;  // elements per row per thread
+    static constexpr int W = NT * EPR;   // columns per CTA
+};
+
+struct Ctx {
+    cg::cluster_group cl;
+    int cs, crank;
+    int xr;  // exchange counter (slot parity)
+};
+
+// Sum (or max) of n per-CTA values over the cluster.  `mine` lives in shared
+// memory.  Afterwards res[0..n) = total, res[n..2n) = exclusive prefix over
+// lower-ranked CTAs (sum only).  All threads of every CTA must call it.
+__device__ __forceinline__ void cluster_combine(Ctx& c, DenseSmem& sm, const double* mine, int n, bool is_max) {
+    double* slot = sm.xch[c.xr & 1];
+    if (threadIdx.x < n) slot[threadIdx.x] = mine[threadIdx.x];
+    c.cl.sync();
+    if (threadIdx.x < n) {
+        double tot = is_max ? -INFINITY : 0.0, pre = 0.0;
+        for (int r = 0; r < c.cs; ++r) {
+            const double v = *c.cl.map_shared_rank(&slot[threadIdx.x], r);
+            if (is_max) {
+                tot = fmax(tot, v);
+            } else {
+                if (r < c.crank) pre += v;
+                tot += v;
+            }
+        }
+        sm.res[threadIdx.x] = tot;
+        sm.res[n + threadIdx.x] = pre;
+    }
+    __syncthreads();
+    ++c.xr;
+}
+
+// Block sum of N doubles per thread; result in out[0..N) (shared), visible after return.
+template <int N>
+__device__ __forceinline__ void block_sum_vec(const double (&v)[N], DenseSmem& sm, double* out) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const double s = warp_sum(v[i]);
+        if (lane == 0) sm.red[wid][i] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < N) {
+        double s = 0.0;
+#pragma unroll
+        for (int w = 0; w < kDenseThreads / 32; ++w) s += sm.red[w][threadIdx.x];
+        out[threadIdx.x] = s;
+    }
+    __syncthreads();
+}
+
+template <int N>
+__device__ __forceinline__ void block_max_vec(const double (&v)[N], DenseSmem& sm, double* out) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        double s = v[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s = fmax(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
+        if (lane == 0) sm.red[wid][i] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < N) {
+        double s = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kDenseThreads / 32; ++w) s = fmax(s, sm.red[w][threadIdx.x]);
+        out[threadIdx.x] = s;
+    }
+    __syncthreads();
+}
+
+// exclusive scan (thread order) of a double; returns the prefix, *total = block total
+__device__ __forceinline__ double block_excl_scan_dbl(double v, DenseSmem& sm, double* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    double x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sm.red[wid][0] = x;
+    __syncthreads();
+    double before = 0.0, tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < kDenseThreads / 32; ++w) {
+        const double s = sm.red[w][0];
+        if (w < wid) before += s;
+        tot += s;
+    }
+    __syncthreads();
+    *total = tot;
+    return before + (x - v);
+}
+
+template <typename TIn, int R>
+__device__ __forceinline__ int col_of(const Ctx& c, int l, int j) {
+    using C = DenseCfg<TIn, R>;
+    return c.crank * C::W + (l * C::NT + (int)threadIdx.x) * C::VEC + j;
+}
+
+// First element, in ascending column order over the whole cluster, at which the
+// running sum of the weights wgt[] passes `target` (strictly if strict, else
+// reaches it); with scale_by_total the target is a fraction of the total weight.  Returns its column (the same value in every thread of every CTA),
+// or -1 if every weight is zero.  *cum_incl receives the running sum including it.
+template <typename TIn, int R, typename WF>
+__device__ int ordered_search(Ctx& c, DenseSmem& sm, WF wgt, double target, bool strict, bool scale_by_total,
+                              double* cum_incl) {
+    using C = DenseCfg<TIn, R>;
+    // per-thread sums of each load group (R groups of VEC consecutive columns)
+    double gs[R];
+#pragma unroll
+    for (int l = 0; l < R; ++l) {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < C::VEC; ++j) s += wgt(l, j);
+        gs[l] = (double)s;
+    }
+    double* G = sm.res + 2 * kXch - R;  // scratch tail of res, outside the exchange results
+    block_sum_vec<R>(gs, sm, G);
+    double gtot[R];
+    double cta_total = 0.0;
+#pragma unroll
+    for (int l = 0; l < R; ++l) {
+        gtot[l] = G[l];
+        cta_total += gtot[l];
+    }
+    __shared__ double s_one[2];
+    if (threadIdx.x == 0) s_one[0] = cta_total;
+    __syncthreads();
+    cluster_combine(c, sm, s_one, 1, false);
+    const double total = sm.res[0], pre = sm.res[1];
+    __syncthreads();
+    if (scale_by_total) target *= total;
+    // the CTA that holds the crossing, with a fallback to the last CTA with mass
+    bool here = strict ? (pre <= target && target < pre + cta_total) : (pre < target && target <= pre + cta_total);
+    here = here && cta_total > 0.0;
+    const bool beyond = strict ? !(target < total) : !(target <= total);
+    double found_col = 0.0, found_cum = 0.0;
+    if (here || beyond) {
+        // beyond: every CTA finds its own last positive element; the highest rank wins below
+        double tl = beyond ? INFINITY : target - pre;
+        int lsel = -1;
+        double acc = 0.0;
+#pragma unroll
+        for (int l = 0; l < R; ++l) {
+            if (lsel < 0 && gtot[l] > 0.0) {
+                const bool in = strict ? (tl < acc + gtot[l]) : (tl <= acc + gtot[l]);
+                if (in) lsel = l;
+            }
+            if (lsel < 0) acc += gtot[l];
+        }
+        if (lsel < 0) {  // rounding: last group with mass
+            acc = 0.0;
+#pragma unroll
+            for (int l = 0; l < R; ++l)
+                if (gtot[l] > 0.0) lsel = l;
+#pragma unroll
+            for (int l = 0; l < R; ++l)
+                if (l < lsel) acc += gtot[l];
+            tl = INFINITY;
+        }
+        const double tg = tl - acc;
+        double mine = 0.0;
+#pragma unroll
+        for (int l = 0; l < R; ++l)
+            if (l == lsel) mine = gs[l];
+        double tot_g;
+        const double before = block_excl_scan_dbl(mine, sm, &tot_g);
+        __shared__ int s_thr;
+        __shared__ unsigned s_lastpos;
+        if (threadIdx.x == 0) {
+            s_thr = 0x7FFFFFFF;
+            s_lastpos = 0u;
+        }
+        __syncthreads();
+        const bool in_t = mine > 0.0 && (strict ? (before <= tg && tg < before + mine) : (before < tg && tg <= before + mine));
+        if (in_t) atomicMin(&s_thr, (int)threadIdx.x);
+        if (mine > 0.0) atomicMax(&s_lastpos, threadIdx.x + 1u);
+        __syncthreads();
+        int thr = s_thr;
+        bool walk_all = false;
+        if (thr == 0x7FFFFFFF) {
+            thr = (int)s_lastpos - 1;
+            walk_all = true;
+        }
+        if ((int)threadIdx.x == thr) {
+            const double te = walk_all ? INFINITY : tg - before;
+            double run = 0.0;
+            int jsel = -1, jlast = -1;
+            double cum_sel = 0.0, cum_last = 0.0;
+#pragma unroll
+            for (int l = 0; l < R; ++l) {
+                if (l == lsel) {
+#pragma unroll
+                    for (int j = 0; j < C::VEC; ++j) {
+                        const double wv = (double)wgt(l, j);
+                        if (wv > 0.0) {
+                            run += wv;
+                            jlast = j;
+                            cum_last = run;
+                            if (jsel < 0 && (strict ? (te < run) : (te <= run))) {
+                                jsel = j;
+                                cum_sel = run;
+                            }
+                        }
+                    }
+                }
+            }
+            if (jsel < 0) {
+                jsel = jlast;
+                cum_sel = cum_last;
+            }
+            found_col = (double)(col_of<TIn, R>(c, lsel, jsel) + 1);
+            found_cum = pre + acc + before + cum_sel;
+            s_one[0] = found_col;
+            s_one[1] = found_cum;
+        }
+        __syncthreads();
+        found_col = s_one[0];
+        found_cum = s_one[1];
+        if (!(thr >= 0)) found_col = 0.0;
+    }
+    __syncthreads();
+    // share: column+1 (0 = none) and the running sum; with `beyond`, the highest-rank CTA wins
+    if (threadIdx.x == 0) {
+        s_one[0] = (here || beyond) ? found_col : 0.0;
+        s_one[1] = (here || beyond) ? found_cum : 0.0;
+    }
+    __syncthreads();
+    double vals[2] = {s_one[0], s_one[1]};
+    __syncthreads();
+    double* slot = sm.xch[c.xr & 1];
+    if (threadIdx.x < 2) slot[threadIdx.x] = vals[threadIdx.x];
+    c.cl.sync();
+    if (threadIdx.x == 0) {
+        double col = 0.0, cum = 0.0;
+        for (int r = 0; r < c.cs; ++r) {
+            const double cc = *c.cl.map_shared_rank(&slot[0], r);
+            if (cc > 0.0) {
+                if (col == 0.0 || beyond) {  // strict hit is unique; fallback takes the last
+                    col = cc;
+                    cum = *c.cl.map_shared_rank(&slot[1], r);
+                }
+            }
+        }
+        sm.res[0] = col;
+        sm.res[1] = cum;
+    }
+    __syncthreads();
+    ++c.xr;
+    const int col = (int)sm.res[0] - 1;
+    *cum_incl = sm.res[1];
+    __syncthreads();
+    return col;
+}
+
+// Keep the shortest prefix of the (e desc, column asc) order whose weight
+// (1 per element if !mass, else e) reaches `target`; zero e elsewhere.
+// Keys are the bit patterns of the non-negative floats e (monotone).
+template <typename TIn, int R>
+__device__ void select_keep(Ctx& c, DenseSmem& sm, float (&e)[DenseCfg<TIn, R>::EPR], int V, bool mass,
+                            double target) {
+    using C = DenseCfg<TIn, R>;
+    const int t = threadIdx.x;
+    uint32_t prefix = 0u;
+    double above = 0.0;
+    bool keep_all = false;
+    for (int d = 7; d >= 0; --d) {
+        const int sh = 4 * d;
+#pragma unroll
+        for (int bin = 0; bin < 16; ++bin) sm.hist[bin][t] = 0.0f;
+#pragma unroll
+        for (int l = 0; l < R; ++l) {
+#pragma unroll
+            for (int j = 0; j < C::VEC; ++j) {
+                const int i = l * C::VEC + j;
+                if (col_of<TIn, R>(c, l, j) < V) {
+                    const uint32_t key = __float_as_uint(e[i]);
+                    const bool match = (d == 7) || ((key >> (sh + 4)) == (prefix >> (sh + 4)));
+                    if (match) sm.hist[(key >> sh) & 15u][t] += mass ? e[i] : 1.0f;
+                }
+            }
+        }
+        __syncthreads();
+        // block-reduce the 16 bins: thread t sums 16 columns of bin (t & 15)
+        {
+            const int bin = t & 15, part = t >> 4;
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s += sm.hist[bin][part * 16 + i];
+            double ds = (double)s;
+            ds += __shfl_xor_sync(0xFFFFFFFFu, ds, 16);
+            const int wid = t >> 5, lane = t & 31;
+            if (lane < 16) sm.red[wid][lane] = ds;
+        }
+        __syncthreads();
+        __shared__ double s_bins[16];
+        if (t < 16) {
+            double s = 0.0;
+#pragma unroll
+            for (int w = 0; w < kDenseThreads / 32; ++w) s += sm.red[w][t];
+            s_bins[t] = s;
+        }
+        __syncthreads();
+        cluster_combine(c, sm, s_bins, 16, false);
+        double acc = above;
+        int dsel = -1, lowest = -1;
+        for (int bin = 15; bin >= 0; --bin) {
+            const double g = sm.res[bin];
+            if (g > 0.0) lowest = bin;
+            if (dsel < 0 && g > 0.0 && acc + g >= target) dsel = bin;
+            if (dsel < 0) acc += g;
+        }
+        if (dsel < 0) {  // the weight never reaches the target (rounding): keep everything
+            keep_all = true;
+            dsel = (lowest < 0) ? 0 : lowest;
+            acc = above;
+            for (int bin = 15; bin > dsel; --bin) acc += sm.res[bin];
+        }
+        __syncthreads();
+        above = acc;
+        prefix |= (uint32_t)dsel << sh;
+        if (keep_all) break;
+    }
+    if (keep_all) return;
+    // ties at the boundary key, in ascending column order
+    const uint32_t kappa = prefix;
+    auto wt = [&](int l, int j) -> float {
+        const int i = l * C::VEC + j;
+        const bool tie = col_of<TIn, R>(c, l, j) < V && __float_as_uint(e[i]) == kappa;
+        return tie ? (mass ? e[i] : 1.0f) : 0.0f;
+    };
+    double cum;
+    const int cstar = ordered_search<TIn, R>(c, sm, wt, target - above, false, false, &cum);
+#pragma unroll
+    for (int l = 0; l < R; ++l)
+#pragma unroll
+        for (int j = 0; j < C::VEC; ++j) {
+            const int i = l * C::VEC + j;
+            const int col = col_of<TIn, R>(c, l, j);
+            const uint32_t key = __float_as_uint(e[i]);
+            const bool keep = col < V && (key > kappa || (key == kappa && col <= cstar));
+            if (!keep) e[i] = 0.0f;
+        }
+}
+
+template <typename TIn, int R, bool VECTOR>
+__device__ __forceinline__ void load_row(const TIn* row, const Ctx& c, int V, float (&x)[DenseCfg<TIn, R>::EPR],
+                                         bool& bad) {
+    using C = DenseCfg<TIn, R>;
+#pragma unroll
+    for (int l = 0; l < R; ++l) {
+        const int col = col_of<TIn, R>(c, l, 0);
+        uint32_t wv[4] = {0u, 0u, 0u, 0u};
+        if (VECTOR) {
+            if (col < V) {
+                const uint4 v = ld_stream16(row + col);
+                wv[0] = v.x;
+                wv[1] = v.y;
+                wv[2] = v.z;
+                wv[3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < C::VEC; ++j)
+                if (col + j < V) {
+                    const uint32_t bits = (sizeof(TIn) == 4) ? __ldg((const unsigned int*)row + col + j)
+                                                             : (uint32_t)__ldg((const unsigned short*)row + col + j);
+                    wv[j / (4 / (int)sizeof(TIn))] |= bits << ((sizeof(TIn) == 2 && (j & 1)) ? 16 : 0);
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < C::VEC; ++j) {
+            uint32_t bits;
+            if (sizeof(TIn) == 4) {
+                bits = wv[j];
+            } else {
+                const uint32_t h = (j & 1) ? (wv[j >> 1] >> 16) : (wv[j >> 1] & 0xFFFFu);
+                bad |= (col + j < V) && bad16(h);
+                bits = h << 16;
+            }
+            if (sizeof(TIn) == 4) bad |= (col + j < V) && bad32(bits);
+            x[l * C::VEC + j] = (col + j < V) ? __uint_as_float(bits) : -INFINITY;
+        }
+    }
+}
+
+template <typename TIn, int R, bool VECTOR>
+__global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
+    using C = DenseCfg<TIn, R>;
+    __shared__ DenseSmem sm;
+    __shared__ double s_vals[kXch];
+    Ctx c{cg::this_cluster(), 0, 0, 0};
+    c.cs = (int)c.cl.num_blocks();
+    c.crank = (int)c.cl.block_rank();
+    const int t = threadIdx.x;
+    const int V = a.V, G = a.G;
+    const uint32_t n_units = a.counts[1];
+    const uint32_t cid = blockIdx.x / (uint32_t)c.cs, ncl = gridDim.x / (uint32_t)c.cs;
+
+    for (uint32_t w = cid; w < n_units; w += ncl) {
+        const uint32_t item = a.dense_units[w];
+        const int b = (int)(item >> 8), u = (int)(item & 0xFFu);
+        const SeqInfo si = a.seq[b];
+        const bool pair = u < si.gamma;
+        const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
+        const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
+
+        float xt[C::EPR], xd[C::EPR];
+        bool bad = false;
+        load_row<TIn, R, VECTOR>(trow, c, V, xt, bad);
+        if (pair) {
+            load_row<TIn, R, VECTOR>(drow, c, V, xd, bad);
+        } else {
+#pragma unroll
+            for (int i = 0; i < C::EPR; ++i) xd[i] = -INFINITY;
+        }
+
+        // ---- maxima (and the non-finite flag) over the cluster
+        {
+            float mt = -INFINITY, md = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < C::EPR; ++i) {
+                mt = fmaxf(mt, xt[i]);
+                md = fmaxf(md, xd[i]);
+            }
+            double v3[3] = {(double)mt, (double)md, bad ? 1.0 : 0.0};
+            block_max_vec<3>(v3, sm, s_vals);
+            cluster_combine(c, sm, s_vals, 3, true);
+        }
+        const float Mt = (float)sm.res[0], Md = (float)sm.res[1];
+        const bool nonfinite = sm.res[2] > 0.0 || !(Mt > -INFINITY) || (pair && !(Md > -INFINITY));
+        __syncthreads();
+        if (nonfinite) {
+            if (c.crank == 0) {
+                if (t == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+                unit_finished(a, b);
+            }
+            continue;
+        }
+
+        // ---- exponentials: e = 2^((x - M) log2(e) / T); greedy: indicator of the maximum
+        const bool greedy = (si.T == 0.0f);
+        const float cscale = greedy ? 0.0f : (float)(1.4426950408889634 / (double)si.T);
+#pragma unroll
+        for (int i = 0; i < C::EPR; ++i) {
+            if (greedy) {
+                xt[i] = (xt[i] == Mt) ? 1.0f : 0.0f;
+                xd[i] = (pair && xd[i] == Md) ? 1.0f : 0.0f;
+            } else {
+                xt[i] = exp2f(fmaf(xt[i], cscale, -Mt * cscale));
+                xd[i] = pair ? exp2f(fmaf(xd[i], cscale, -Md * cscale)) : 0.0f;
+            }
+        }
+
+        // ---- filters (greedy: keep the lowest-id maximum only)
+        const int kf = greedy ? 1 : si.k;
+        const float Pf = greedy ? 1.0f : si.P;
+        if (kf > 0) {
+            select_keep<TIn, R>(c, sm, xt, V, false, (double)kf);
+            if (pair) select_keep<TIn, R>(c, sm, xd, V, false, (double)kf);
+        }
+        if (Pf < 1.0f) {
+            double sums[2] = {0.0, 0.0};
+            float st = 0.0f, sd = 0.0f;
+#pragma unroll
+            for (int i = 0; i < C::EPR; ++i) {
+                st += xt[i];
+                sd += xd[i];
+            }
+            sums[0] = st;
+            sums[1] = sd;
+            block_sum_vec<2>(sums, sm, s_vals);
+            cluster_combine(c, sm, s_vals, 2, false);
+            const double St = sm.res[0], Sd = sm.res[1];
+            __syncthreads();
+            select_keep<TIn, R>(c, sm, xt, V, true, (double)Pf * St);
+            if (pair) select_keep<TIn, R>(c, sm, xd, V, true, (double)Pf * Sd);
+        }
+
+        // ---- normalisers of the kept mass
+        double St, Sd;
+        {
+            double sums[2];
+            float st = 0.0f, sd = 0.0f;
+#pragma unroll
+            for (int i = 0; i < C::EPR; ++i) {
+                st += xt[i];
+                sd += xd[i];
+            }
+            sums[0] = st;
+            sums[1] = sd;
+            block_sum_vec<2>(sums, sm, s_vals);
+            cluster_combine(c, sm, s_vals, 2, false);
+            St = sm.res[0];
+            Sd = sm.res[1];
+            __syncthreads();
+        }
+        const float inv_t = (float)(1.0 / St);
+        const float inv_d = pair ? (float)(1.0 / Sd) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < C::EPR; ++i) {
+            xt[i] *= inv_t;  // p
+            xd[i] *= inv_d;  // q
+        }
+
+        // ---- debug copies of the normalised rows
+        if (a.p_out || a.q_out) {
+#pragma unroll
+            for (int l = 0; l < R; ++l)
+#pragma unroll
+                for (int j = 0; j < C::VEC; ++j) {
+                    const int col = col_of<TIn, R>(c, l, j);
+                    if (col < V) {
+                        if (a.p_out) a.p_out[((size_t)b * (G + 1) + u) * V + col] = xt[l * C::VEC + j];
+                        if (a.q_out && pair) a.q_out[((size_t)b * G + u) * V + col] = xd[l * C::VEC + j];
+                    }
+                }
+        }
+
+        // ---- alpha, acceptance gather; the residual weights replace q in place
+        const int x_tok = pair ? a.draft_tokens[(size_t)b * G + u] : -1;
+        double part[4] = {0.0, 0.0, 0.0, 0.0};
+        {
+            float al = 0.0f, rs = 0.0f;
+#pragma unroll
+            for (int l = 0; l < R; ++l)
+#pragma unroll
+                for (int j = 0; j < C::VEC; ++j) {
+                    const int i = l * C::VEC + j;
+                    const float p = xt[i], q = xd[i];
+                    al += fminf(p, q);
+                    if (col_of<TIn, R>(c, l, j) == x_tok) {
+                        part[1] = (double)p;
+                        part[2] = (double)q;
+                    }
+                    xd[i] = pair ? fmaxf(p - q, 0.0f) : p;  // bonus: q_{gamma+1} := 0
+                    rs += xd[i];
+                }
+            part[0] = (double)al;
+            part[3] = (double)rs;
+        }
+        block_sum_vec<4>(part, sm, s_vals);
+        cluster_combine(c, sm, s_vals, 4, false);
+        const double alpha = sm.res[0], px = sm.res[1], qx = sm.res[2];
+        const double Z = sm.res[3];
+        __syncthreads();
+        if (!(Z > 0.0)) {  // p <= q everywhere: the draw falls back to p
+#pragma unroll
+            for (int i = 0; i < C::EPR; ++i) xd[i] = xt[i];
+        }
+        const double ua = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 0u);
+        const double ur = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 1u);
+        double cum;
+        // v = u * Z, with Z the search's own hierarchical total, so that v < Z exactly
+        const int token = ordered_search<TIn, R>(
+            c, sm, [&](int l, int j) -> float { return xd[l * C::VEC + j]; }, ur, true, true, &cum);
+        const int accept = pair ? ((ua * qx < px) ? 1 : 0) : 0;
+
+        if (c.crank == 0) {
+            if (t == 0) {
+                if (pair) {
+                    a.alpha[(size_t)b * G + u] = (float)alpha;
+                    a.unit_acc[(size_t)b * G + u] = accept;
+                    if (a.pos_accept) a.pos_accept[(size_t)b * G + u] = accept;
+                }
+                a.unit_tok[(size_t)b * (G + 1) + u] = token;
+                if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + u] = token;
+            }
+            unit_finished(a, b);
+        }
+    }
+    // no CTA may leave while a peer can still read its shared memory
+    c.cl.sync();
+}
+
+// vocabulary split: load groups per thread R and cluster size, smallest R first
+template <typename TIn>
+inline bool dense_shape(int V, int* R, int* cs) {
+    const int vec = 16 / (int)sizeof(TIn);
+    const int rmax = sizeof(TIn) == 2 ? 8 : 16;
+    for (int r = 1; r <= rmax; r <<= 1) {
+        const int w = kDenseThreads * r * vec;
+        const int c = (V + w - 1) / w;
+        if (c <= 8 || (r == rmax && c <= 16)) {
+            *R = r;
+            *cs = c;
+            return true;
+        }
+    }
+    return false;
+}
+
+// Persistent launch: as many clusters as fit on the GPU at once, each walking
+// the dense unit list.
+template <typename TIn, int R, bool VECTOR>
+cudaError_t launch_dense_cluster(const Args& a, int cs, int sms, cudaStream_t s) {
+    auto k = dense_kernel<TIn, R, VECTOR>;
+    static const bool attr_ok = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    (void)attr_ok;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kDenseThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)cs);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        clusters = sms / cs > 0 ? sms / cs : 1;
+    }
+    const long long upper = (long long)a.B * (a.G + 1);
+    long long n = clusters;
+    if (n > upper) n = upper;
+    if (n < 1) n = 1;
+    cfg.gridDim = dim3((unsigned)(n * cs));
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -1,0 +1,201 @@
+// sv_internal.cuh -- shared device/host internals of the GB300 verification library.
+//
+// Layout of one call on the GPU (all on the caller's stream, no host sync):
+//   plan kernel    (1 CTA)  validates the per-sequence parameters, picks a path
+//                           per sequence, zeroes the per-call counters and
+//                           writes the work lists;
+//   stream kernel           greedy and top-k <= 256 sequences: every row is cut
+//                           into 64 KB pieces; each piece streams its logits once
+//                           from HBM and keeps only top-k candidates; the last
+//                           piece of a (target row, draft row) unit merges them
+//                           and does the per-position arithmetic in fp64;
+//   dense kernel            every other sequence: one thread-block cluster holds
+//                           a whole (target row, draft row) unit in registers
+//                           (DSMEM reductions between the CTAs) and does softmax,
+//                           top-k/top-p, alpha, acceptance and the residual draw.
+// The last unit of a sequence to finish writes that sequence's outputs
+// (last-block-done counters; no thread ever waits on another block).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// configuration
+// ---------------------------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+constexpr int kStreamThreads = 256;
+constexpr int kStreamLoads = 16;  // 16-byte loads per thread per piece: a piece is 64 KB
+constexpr int kCandCap = 512;     // candidates a piece may hand to its unit
+constexpr int kStreamMaxK = SV_STREAM_MAX_TOP_K;
+constexpr int kSortCap = 2048;  // candidates per row sorted in shared memory by the merge step
+constexpr int kDenseThreads = 256;
+
+enum : uint32_t { kModeErr = 0, kModeStream = 1, kModeDense = 2 };
+
+// per-sequence plan (32 bytes)
+struct SeqInfo {
+    uint32_t mode;
+    uint32_t status;
+    int32_t gamma;
+    int32_t k;        // effective top-k (0 = off); 1 for greedy
+    float T;          // temperature (0 = greedy)
+    float P;          // effective top-p (1 = off)
+    uint32_t row_off; // index of this sequence's first row in the stream row list
+    uint32_t pad;
+};
+
+// Everything a kernel needs, passed by value.
+struct Args {
+    const void* target;
+    const void* draft;
+    const int32_t* draft_tokens;
+    const int32_t* num_draft;
+    const float* temperature;
+    const int32_t* top_k;
+    const float* top_p;
+    uint64_t seed;
+    int B, G, V;
+    int32_t* accepted_len;
+    int32_t* out_tokens;
+    float* alpha;
+    float* p_out;
+    float* q_out;
+    uint32_t* row_status;
+    int32_t* pos_accept;
+    int32_t* pos_token;
+    int force_dense;
+    int ppr;  // stream pieces per row
+    // workspace
+    SeqInfo* seq;
+    uint32_t* seq_done;
+    uint32_t* seq_status;
+    uint32_t* unit_done;
+    int32_t* unit_acc;
+    int32_t* unit_tok;
+    uint32_t* stream_rows;
+    uint32_t* dense_units;
+    uint32_t* counts;  // [0] stream rows, [1] dense units
+    uint2* cand;       // [stream rows * ppr * kCandCap] (key, id)
+    uint32_t* cand_cnt;
+};
+
+struct WsLayout {
+    size_t seq, seq_done, seq_status, unit_done, unit_acc, unit_tok, stream_rows, dense_units, counts, cand,
+        cand_cnt, total;
+    int ppr;
+};
+
+__host__ __device__ inline int stream_piece_elems(int dtype) {
+    return kStreamThreads * kStreamLoads * (dtype == SV_BF16 ? 8 : 4);
+}
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline WsLayout ws_layout(int B, int G, int V, int dtype) {
+    WsLayout L{};
+    size_t o = 0;
+    const size_t rows = (size_t)B * (2 * G + 1);
+    const size_t units = (size_t)B * (G + 1);
+    L.ppr = (V + stream_piece_elems(dtype) - 1) / stream_piece_elems(dtype);
+    L.seq = o;         o = align_up(o + sizeof(SeqInfo) * B, 256);
+    L.seq_done = o;    o = align_up(o + 4 * (size_t)B, 256);
+    L.seq_status = o;  o = align_up(o + 4 * (size_t)B, 256);
+    L.unit_done = o;   o = align_up(o + 4 * units, 256);
+    L.unit_acc = o;    o = align_up(o + 4 * (size_t)B * G, 256);
+    L.unit_tok = o;    o = align_up(o + 4 * units, 256);
+    L.stream_rows = o; o = align_up(o + 4 * rows, 256);
+    L.dense_units = o; o = align_up(o + 4 * units, 256);
+    L.counts = o;      o = align_up(o + 16, 256);
+    L.cand_cnt = o;    o = align_up(o + 4 * rows * L.ppr, 256);
+    L.cand = o;        o = align_up(o + 8 * rows * L.ppr * kCandCap, 256);
+    L.total = o;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of two 32x32->64
+// multiplies with the Weyl-bumped key; only output word 0 is used here.
+__device__ __forceinline__ uint32_t philox_w0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                              uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t a_lo = 0xD2511F53u * c0, a_hi = __umulhi(0xD2511F53u, c0);
+        const uint32_t b_lo = 0xCD9E8D57u * c2, b_hi = __umulhi(0xCD9E8D57u, c2);
+        c0 = b_hi ^ c1 ^ k0;
+        c1 = b_lo;
+        c2 = a_hi ^ c3 ^ k1;
+        c3 = a_lo;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c0;
+}
+
+// U(seed, b, pos, draw) = ((w >> 8) + 0.5) * 2^-24 (exact in double)
+__device__ __forceinline__ double uniform01(uint64_t seed, uint32_t b, uint32_t pos, uint32_t draw) {
+    const uint32_t w = philox_w0(b, pos, draw, 0u, (uint32_t)seed, (uint32_t)(seed >> 32));
+    return ((double)(w >> 8) + 0.5) * (1.0 / 16777216.0);
+}
+
+// Order-preserving unsigned keys of float bit patterns; -0 is folded onto +0
+// so equal values get equal keys.
+__device__ __forceinline__ uint32_t okey32(uint32_t bits) {
+    bits = (bits == 0x80000000u) ? 0u : bits;
+    return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t okey16(uint32_t h) {
+    h = (h == 0x8000u) ? 0u : h;
+    return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+}
+__device__ __forceinline__ float key_value32(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+__device__ __forceinline__ float key_value16(uint32_t k) {
+    const uint32_t h = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+    return __uint_as_float(h << 16);
+}
+// NaN or +inf (-inf is a legal, masked logit)
+__device__ __forceinline__ bool bad32(uint32_t bits) {
+    return ((bits & 0x7FFFFFFFu) > 0x7F800000u) || bits == 0x7F800000u;
+}
+__device__ __forceinline__ bool bad16(uint32_t h) { return ((h & 0x7FFFu) > 0x7F80u) || h == 0x7F80u; }
+
+// streaming 16-byte load: read once, do not keep in L1
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+#endif  // __CUDACC__
+
+// host launchers, one per kernel translation unit
+cudaError_t launch_stream_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s);
+cudaError_t launch_dense_f32(bool vector, const Args& a, int sms, cudaStream_t s);
+cudaError_t launch_dense_bf16(bool vector, const Args& a, int sms, cudaStream_t s);
+
+}  // namespace sv

@@ -1,0 +1,110 @@
+"""Parity checking between the CUDA path and the oracle (test infrastructure).
+
+Rules (from the verification contract):
+  * accepted_len / out_tokens and every per-position decision (acceptance at
+    each position, residual/bonus token of each position) must agree exactly,
+    except decisions whose oracle margin is below 1e-6 -- |u - p/q| for an
+    acceptance, the distance of v/Z to the nearest CDF edge for a draw, or a
+    filter (top-k / top-p) boundary margin of a row the decision reads.  Such
+    excused mismatches are counted and must stay under 1e-4 of all decisions.
+  * alpha within 1e-5 absolute; normalised probabilities within 1e-5 absolute.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+MARGIN = 1e-6
+EXCUSED_FRACTION = 1e-4
+ALPHA_TOL = 1e-5
+PROB_TOL = 1e-5
+
+
+@dataclass
+class ParityReport:
+    decisions: int = 0
+    low_margin: int = 0
+    excused: int = 0
+    hard: list = field(default_factory=list)
+    alpha_err: float = 0.0
+    prob_err: float = 0.0
+
+    def ok(self) -> bool:
+        return not self.hard and self.excused <= EXCUSED_FRACTION * max(self.decisions, 1) and \
+            self.alpha_err <= ALPHA_TOL and self.prob_err <= PROB_TOL
+
+    def __str__(self):
+        return (f"decisions={self.decisions} low_margin={self.low_margin} excused={self.excused} "
+                f"hard={self.hard[:5]} alpha_err={self.alpha_err:.3g} prob_err={self.prob_err:.3g}")
+
+
+def to_np(t):
+    return t.detach().cpu().numpy() if hasattr(t, "detach") else np.asarray(t)
+
+
+def compare(gpu: dict, ora, gammas, G: int, report: ParityReport | None = None) -> ParityReport:
+    """gpu: dict of tensors from spec_verify(..., positions=True); ora: OracleResult(all_positions=True)."""
+    rep = report or ParityReport()
+    acc, out = to_np(gpu["accepted_len"]), to_np(gpu["out_tokens"])
+    alpha = to_np(gpu["alpha"])
+    status = to_np(gpu["row_status"]).astype(np.uint32)
+    pa, pt = to_np(gpu["pos_accept"]), to_np(gpu["pos_token"])
+    B = acc.shape[0]
+    for b in range(B):
+        if status[b] != ora.status[b]:
+            rep.hard.append(("status", b, int(status[b]), int(ora.status[b])))
+            continue
+        if ora.status[b]:
+            if acc[b] != 0 or (out[b] != -1).any() or (alpha[b] != 0).any():
+                rep.hard.append(("invalid-row-outputs", b))
+            continue
+        g = int(gammas[b])
+        fm = ora.filter_margin[b]
+        row_excuse_t = [fm[j] < MARGIN for j in range(G + 1)]
+        row_excuse_d = [fm[G + 1 + j] < MARGIN for j in range(G)]
+        first_diff_excused = True
+        for i in range(g):
+            rep.decisions += 1
+            m = ora.accept_margin[b, i]
+            low = (m < MARGIN) or row_excuse_t[i] or row_excuse_d[i]
+            rep.low_margin += int(low)
+            if pa[b, i] != ora.pos_accept[b, i]:
+                if low:
+                    rep.excused += 1
+                else:
+                    rep.hard.append(("accept", b, i, int(pa[b, i]), int(ora.pos_accept[b, i]), float(m)))
+        for j in range(g + 1):
+            rep.decisions += 1
+            m = ora.resid_margin[b, j]
+            low = (m < MARGIN) or row_excuse_t[j] or (j < g and row_excuse_d[j])
+            rep.low_margin += int(low)
+            if pt[b, j] != ora.pos_token[b, j]:
+                if low:
+                    rep.excused += 1
+                else:
+                    rep.hard.append(("token", b, j, int(pt[b, j]), int(ora.pos_token[b, j]), float(m)))
+        # the emitted round follows from the per-position decisions
+        if acc[b] != ora.accepted_len[b] or (out[b] != ora.out_tokens[b]).any():
+            n = min(int(acc[b]), int(ora.accepted_len[b]))
+            explained = any(pa[b, i] != ora.pos_accept[b, i] for i in range(n + 1) if i < g) or \
+                any(pt[b, j] != ora.pos_token[b, j] for j in range(n + 2) if j <= g)
+            if not explained:
+                rep.hard.append(("round", b, int(acc[b]), int(ora.accepted_len[b])))
+        err = np.abs(alpha[b, :g] - ora.alpha[b, :g]).max() if g else 0.0
+        rep.alpha_err = max(rep.alpha_err, float(err))
+        if (alpha[b, g:] != 0).any():
+            rep.hard.append(("alpha-padding", b))
+    return rep
+
+
+def compare_probs(gpu: dict, ora, gammas, rep: ParityReport) -> ParityReport:
+    p, q = to_np(gpu["p_out"]), to_np(gpu["q_out"])
+    for b in range(p.shape[0]):
+        if ora.status[b]:
+            continue
+        g = int(gammas[b])
+        rep.prob_err = max(rep.prob_err, float(np.abs(p[b, : g + 1] - ora.p_out[b, : g + 1]).max()))
+        if g:
+            rep.prob_err = max(rep.prob_err, float(np.abs(q[b, :g] - ora.q_out[b, :g]).max()))
+    return rep
