@@ -78,7 +78,7 @@ void svr_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t ou
     out[3] = x3;
 }
 
-/* u = ((w0 >> 8) + 1/2) * 2^-24: strictly inside (0,1), exact in fp32 and fp64. */
+/* u = ((w0 >> 8) + 1/2) * 2^-24: strictly inside (0,1) and exact in fp64. */
 double svr_uniform(uint64_t seed, uint32_t b, uint32_t pos, uint32_t draw) {
     uint32_t ctr[4] = {b, pos, draw, 0u};
     uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
