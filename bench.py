@@ -175,10 +175,12 @@ def run_reference(args):
     return 0
 
 
-def workload_config(name: str) -> dict:
+def workload_config(name: str, B: int | None = None) -> dict:
     from speculative_decoding_verification_20_gb300.workloads import CONFIGS
 
     c = dict(CONFIGS[name])
+    if B is not None:
+        c["B"] = B
     filt = {"v128k": "T=1, top-k 50 then top-p 0.9", "v32k": "T=0.8, no filter", "b1024": "T=1, no filter",
             "tiny": "T=1, no filter", "ragged": "T in {0,.3,.7,1,1.2}, top-p U[.8,1]"}[name]
     return {"workload": f"{name}: B={c['B']}, gamma={c['G']}{' (ragged 1..8)' if name == 'ragged' else ''}, "
@@ -195,6 +197,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling of smaller cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -219,7 +222,7 @@ def main():
         dist.barrier()
     sv.load_library()
 
-    wl = workloads.make(args.workload, seed=rank, device=dev)
+    wl = workloads.make(args.workload, seed=rank, device=dev, B=args.batch)
     B, G, V = wl.B, wl.G, wl.V
     stream = torch.cuda.current_stream(dev)
     ws = torch.empty(sv.workspace_size(B, G, V, sv.SV_BF16 if wl.dtype == "bf16" else sv.SV_F32), dtype=torch.uint8,
@@ -236,6 +239,9 @@ def main():
     # per-step events around the dominant kernel, recorded by the library on the launching stream
     main = "stream" if (wl.top_k is not None and int(wl.top_k.max()) <= sv.SV_STREAM_MAX_TOP_K) else "dense"
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in kev:  # torch creates the underlying CUDA events on their first record
+        a_.record(stream)
+        b_.record(stream)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -304,7 +310,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic",
-        "config": dict(workload_config(args.workload),
+        "config": dict(workload_config(args.workload, B),
                        l2="inputs larger than L2: %.0f MB of logits per step vs 129 MB L2" % (bytes_per_launch / 1e6),
                        parallelism=f"replicas x{world} (independent batches per GPU)"),
         "hbm_gbs_step": bytes_per_launch / (ms_step * 1e-3) / 1e9,

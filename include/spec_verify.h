@@ -69,6 +69,7 @@ typedef enum {
 #define SV_ROW_BAD_NUM_DRAFT 0x08u   /* num_draft outside [1, gamma_max] */
 #define SV_ROW_BAD_DRAFT_TOKEN 0x10u /* a draft token outside [0, V) */
 #define SV_ROW_NONFINITE 0x20u       /* NaN or +inf logit, or a row with no finite logit */
+#define SV_ROW_INTERNAL 0x40u        /* a device-side wait gave up (internal error); outputs are defaults */
 
 /* supported maxima */
 #define SV_MAX_GAMMA 32

@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
     c.crank = (int)c.cl.block_rank();
     const int t = threadIdx.x;
     const int V = a.V, G = a.G;
-    const uint32_t n_units = a.counts[1];
+    const uint32_t n_units = a.counts[kCntDenseUnits];
     const uint32_t cid = blockIdx.x / (uint32_t)c.cs, ncl = gridDim.x / (uint32_t)c.cs;
 
     for (uint32_t w = cid; w < n_units; w += ncl) {

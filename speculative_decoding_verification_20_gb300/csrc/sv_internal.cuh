@@ -4,11 +4,15 @@
 //   plan kernel    (1 CTA)  validates the per-sequence parameters, picks a path
 //                           per sequence, zeroes the per-call counters and
 //                           writes the work lists;
-//   stream kernel           greedy and top-k <= 256 sequences: every row is cut
-//                           into 64 KB pieces; each piece streams its logits once
-//                           from HBM and keeps only top-k candidates; the last
-//                           piece of a (target row, draft row) unit merges them
-//                           and does the per-position arithmetic in fp64;
+//   select kernel           greedy and top-k <= 256 sequences: every row is cut
+//                           into pieces of up to 16 x 16 KB tiles, streamed once
+//                           from HBM by TMA bulk copies into a shared-memory
+//                           ring; each piece keeps only its exact top-k
+//                           (logit key, token id) candidates;
+//   combine kernel          one CTA per (target row, draft row) unit merges the
+//                           pieces' lists and does the per-position arithmetic
+//                           in fp64 (softmax over the kept logits, top-p,
+//                           alpha, acceptance, residual / bonus draw);
 //   dense kernel            every other sequence: one thread-block cluster holds
 //                           a whole (target row, draft row) unit in registers
 //                           (DSMEM reductions between the CTAs) and does softmax,
@@ -29,12 +33,15 @@ namespace sv {
 // configuration
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
-constexpr int kStreamThreads = 256;
-constexpr int kStreamLoads = 16;  // 16-byte loads per thread per piece: a piece is 64 KB
-constexpr int kCandCap = 512;     // candidates a piece may hand to its unit
+constexpr int kTileBytes = 16384;   // one TMA bulk copy
+constexpr int kTilesPerPiece = 16;  // a piece of a row: up to 256 KB of logits
 constexpr int kStreamMaxK = SV_STREAM_MAX_TOP_K;
-constexpr int kSortCap = 2048;  // candidates per row sorted in shared memory by the merge step
+constexpr int kListCap = 512;   // candidates one piece hands to the combine kernel
+constexpr int kSortCap = 2048;  // candidates per row sorted in shared memory by the combine kernel
 constexpr int kDenseThreads = 256;
+
+// counters at the head of the workspace list area
+enum : int { kCntStreamRows = 0, kCntDenseUnits = 1, kCntStreamUnits = 2, kCntPieceNext = 3, kCntError = 4 };
 
 enum : uint32_t { kModeErr = 0, kModeStream = 1, kModeDense = 2 };
 
@@ -80,20 +87,20 @@ struct Args {
     int32_t* unit_tok;
     uint32_t* stream_rows;
     uint32_t* dense_units;
-    uint32_t* counts;  // [0] stream rows, [1] dense units
-    uint2* cand;       // [stream rows * ppr * kCandCap] (key, id)
-    uint32_t* cand_cnt;
+    uint32_t* stream_units;
+    uint32_t* counts;         // kCnt* above
+    unsigned long long* cand; // [stream rows * ppr * kListCap] (key << 32 | ~id), unsorted
+    uint32_t* cand_cnt;       // [stream rows * ppr]
 };
 
 struct WsLayout {
-    size_t seq, seq_done, seq_status, unit_done, unit_acc, unit_tok, stream_rows, dense_units, counts, cand,
-        cand_cnt, total;
+    size_t seq, seq_done, seq_status, unit_done, unit_acc, unit_tok, stream_rows, dense_units, stream_units, counts,
+        cand, cand_cnt, total;
     int ppr;
 };
 
-__host__ __device__ inline int stream_piece_elems(int dtype) {
-    return kStreamThreads * kStreamLoads * (dtype == SV_BF16 ? 8 : 4);
-}
+__host__ __device__ inline int tile_elems(int dtype) { return kTileBytes / (dtype == SV_BF16 ? 2 : 4); }
+__host__ __device__ inline int stream_piece_elems(int dtype) { return kTilesPerPiece * tile_elems(dtype); }
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -111,9 +118,10 @@ __host__ __device__ inline WsLayout ws_layout(int B, int G, int V, int dtype) {
     L.unit_tok = o;    o = align_up(o + 4 * units, 256);
     L.stream_rows = o; o = align_up(o + 4 * rows, 256);
     L.dense_units = o; o = align_up(o + 4 * units, 256);
-    L.counts = o;      o = align_up(o + 16, 256);
+    L.stream_units = o; o = align_up(o + 4 * units, 256);
+    L.counts = o;      o = align_up(o + 64, 256);
     L.cand_cnt = o;    o = align_up(o + 4 * rows * L.ppr, 256);
-    L.cand = o;        o = align_up(o + 8 * rows * L.ppr * kCandCap, 256);
+    L.cand = o;        o = align_up(o + 8 * rows * L.ppr * kListCap, 256);
     L.total = o;
     return L;
 }
@@ -194,7 +202,7 @@ __device__ __forceinline__ float warp_max(float v) {
 #endif  // __CUDACC__
 
 // host launchers, one per kernel translation unit
-cudaError_t launch_stream_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s);
+cudaError_t launch_stream_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, void* const ev[2]);
 cudaError_t launch_dense_f32(bool vector, const Args& a, int sms, cudaStream_t s);
 cudaError_t launch_dense_bf16(bool vector, const Args& a, int sms, cudaStream_t s);
 
