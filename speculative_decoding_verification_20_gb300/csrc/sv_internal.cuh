@@ -5,7 +5,7 @@
 //                           per sequence, zeroes the per-call counters and
 //                           writes the work lists;
 //   select kernel           greedy and top-k <= 256 sequences: every row is cut
-//                           into pieces of up to 16 x 16 KB tiles, streamed once
+//                           into pieces of up to 8 x 32 KB tiles, streamed once
 //                           from HBM by TMA bulk copies into a shared-memory
 //                           ring; each piece keeps only its exact top-k
 //                           (logit key, token id) candidates;
@@ -33,8 +33,8 @@ namespace sv {
 // configuration
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
-constexpr int kTileBytes = 16384;   // one TMA bulk copy
-constexpr int kTilesPerPiece = 16;  // a piece of a row: up to 256 KB of logits
+constexpr int kTileBytes = 32768;   // one TMA bulk copy
+constexpr int kTilesPerPiece = 8;   // a piece of a row: up to 256 KB of logits
 constexpr int kStreamMaxK = SV_STREAM_MAX_TOP_K;
 constexpr int kListCap = 512;   // candidates one piece hands to the combine kernel
 constexpr int kSortCap = 2048;  // candidates per row sorted in shared memory by the combine kernel

@@ -9,8 +9,8 @@
 // the vocabulary.
 //
 // select_kernel (persistent, 2 CTAs per SM, 8 consumer warps + 1 producer warp)
-//   producer: pieces of rows are taken from a global counter; each 16 KB tile
-//     is brought into a 5-stage shared-memory ring by one cp.async.bulk
+//   producer: pieces of rows are taken from a global counter; each 32 KB tile
+//     is brought into a 3-stage shared-memory ring by one cp.async.bulk
 //     (TMA) whose completion is counted on the stage's mbarrier.
 //   consumers: per 16-byte vector, a packed max tree (NaN-propagating, so it
 //     also detects non-finite logits) is compared once with the running
@@ -18,7 +18,7 @@
 //     mask and append those (key, token id) candidates to a shared buffer.
 //     theta starts at a lower bound of the k-th largest key of the piece's
 //     first tile (per-warp ballots over the per-thread maxima); whenever the
-//     buffer exceeds 4k entries, a block-wide 4-bit radix select finds the
+//     buffer exceeds 2k entries, a block-wide 4-bit radix select finds the
 //     exact k-th key of the buffer, the buffer keeps only keys >= it, and the
 //     filter becomes strict (a later tie has a larger id, so it can never
 //     enter the top-k).
@@ -36,7 +36,7 @@
 
 namespace sv {
 
-constexpr int kStages = 5;
+constexpr int kStages = 3;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kSelThreads = kConsumers + 32;
@@ -205,6 +205,9 @@ struct RunOf<__nv_bfloat16> {
 // ---------------------------------------------------------------------------
 constexpr int kBufCap = 2048;   // candidate buffer
 constexpr int kPerThread = kBufCap / kConsumers;
+// a piece with at most this many candidates at its end hands them all over unselected
+constexpr int kFinalList = 512;
+static_assert(kFinalList <= kListCap && kFinalList >= kStreamMaxK, "final list bounds");
 
 struct SelSmem {
     alignas(128) uint8_t buf[kStages][kTileBytes];
@@ -212,6 +215,7 @@ struct SelSmem {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     int4 hdr[kStages];  // piece index (-1: no more work), tile index, elements, first column
+    int2 seqk[kStages]; // sequence b and its top-k for the piece
     int red[kConsumerWarps];
     int scan[kConsumerWarps];
     int hist[16];
@@ -258,6 +262,22 @@ __device__ __forceinline__ void append(SelSmem& sm, unsigned long long c) {
     if (slot < (unsigned)kBufCap) sm.cand[slot] = c;
 }
 
+// Reserve `mine` consecutive buffer slots for this lane with one shared atomic
+// per warp (all lanes of the warp call it); returns the lane's first slot.
+__device__ __forceinline__ unsigned warp_reserve(SelSmem& sm, unsigned mine) {
+    const int lane = threadIdx.x & 31;
+    unsigned x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    const unsigned total = __shfl_sync(0xFFFFFFFFu, x, 31);
+    unsigned base = 0u;
+    if (lane == 31 && total) base = atomicAdd(&sm.count, total);
+    return __shfl_sync(0xFFFFFFFFu, base, 31) + x - mine;
+}
+
 // Exact k-th largest key of the buffer (4-bit radix, shared histogram).
 // Every consumer holds up to kPerThread buffer entries in `mine`.  Returns the
 // key; *gt receives the number of entries strictly above it.
@@ -272,11 +292,16 @@ __device__ uint32_t buffer_kth_key(SelSmem& sm, const unsigned long long (&mine)
         cbar();
 #pragma unroll
         for (int i = 0; i < kPerThread; ++i) {
+            if (!__any_sync(0xFFFFFFFFu, i < nmine)) break;
+            int digit = -1;
             if (i < nmine) {
                 const uint32_t key = comp_key(mine[i]);
                 const bool match = (sh + 4 >= KB) || ((key >> (sh + 4)) == (prefix >> (sh + 4)));
-                if (match) atomicAdd(&sm.hist[(key >> sh) & 15u], 1);
+                if (match) digit = (int)((key >> sh) & 15u);
             }
+            // one shared atomic per distinct digit of the warp
+            const unsigned grp = __match_any_sync(0xFFFFFFFFu, digit);
+            if (digit >= 0 && (threadIdx.x & 31) == __ffs(grp) - 1) atomicAdd(&sm.hist[digit], __popc(grp));
         }
         cbar();
         int acc = above, dsel = 0;
@@ -301,9 +326,13 @@ __device__ __forceinline__ void buffer_keep_ge(SelSmem& sm, const unsigned long 
                                                uint32_t kth) {
     if (threadIdx.x == 0) sm.count = 0u;
     cbar();
+    unsigned keep = 0u;
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) keep += (i < nmine && comp_key(mine[i]) >= kth) ? 1u : 0u;
+    unsigned slot = warp_reserve(sm, keep);
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i)
-        if (i < nmine && comp_key(mine[i]) >= kth) append(sm, mine[i]);
+        if (i < nmine && comp_key(mine[i]) >= kth) sm.cand[slot++] = mine[i];
     cbar();
 }
 
@@ -458,16 +487,34 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
 #pragma unroll
             for (int s = 0; s < kStages; ++s) issued[s] = -1;  // full-barrier parity of the last copy per stage
             bool ok = true;
-            while (ok) {
-                uint32_t w = 0;
-                if (lane == 0) w = atomicAdd(&a.counts[kCntPieceNext], 1u);
-                if (!TMA) w = __shfl_sync(0xFFFFFFFFu, w, 0);
-                if (w >= n_pieces) break;
+            // the next piece is claimed (and its row looked up) one piece ahead
+            uint32_t w = 0;
+            if (lane == 0) w = atomicAdd(&a.counts[kCntPieceNext], 1u);
+            if (!TMA) w = __shfl_sync(0xFFFFFFFFu, w, 0);
+            int b = 0, r = 0, gamma = 0, k = 1;
+            if (w < n_pieces) {
+                const uint32_t item = a.stream_rows[w / (uint32_t)ppr];
+                b = (int)(item >> 8);
+                r = (int)(item & 0xFFu);
+                const SeqInfo si = a.seq[b];
+                gamma = si.gamma;
+                k = si.k;
+            }
+            while (ok && w < n_pieces) {
+                uint32_t w_next = 0;
+                if (lane == 0) w_next = atomicAdd(&a.counts[kCntPieceNext], 1u);
+                if (!TMA) w_next = __shfl_sync(0xFFFFFFFFu, w_next, 0);
+                int b_next = 0, r_next = 0, gamma_next = 0, k_next = 1;
+                if (w_next < n_pieces) {
+                    const uint32_t item = a.stream_rows[w_next / (uint32_t)ppr];
+                    b_next = (int)(item >> 8);
+                    r_next = (int)(item & 0xFFu);
+                    const SeqInfo si = a.seq[b_next];
+                    gamma_next = si.gamma;
+                    k_next = si.k;
+                }
                 const uint32_t row_slot = w / (uint32_t)ppr;
                 const int piece = (int)(w - row_slot * (uint32_t)ppr);
-                const uint32_t item = a.stream_rows[row_slot];
-                const int b = (int)(item >> 8), r = (int)(item & 0xFFu);
-                const int gamma = a.seq[b].gamma;
                 const TIn* row = (r <= gamma) ? (const TIn*)a.target + ((size_t)b * (G + 1) + r) * (size_t)V
                                               : (const TIn*)a.draft + ((size_t)b * G + (r - gamma - 1)) * (size_t)V;
                 const int c0 = piece * PE, c1 = min(V, c0 + PE);
@@ -477,7 +524,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
                         ok = false;
                         break;
                     }
-                    if (lane == 0) sm.hdr[stage] = make_int4((int)w, tile, n, col);
+                    if (lane == 0) {
+                        sm.hdr[stage] = make_int4((int)w, tile, n, col);
+                        sm.seqk[stage] = make_int2(b, k);
+                    }
                     if (TMA) {
                         mbar_arrive_expect_tx(&sm.full[stage], (uint32_t)(n * sizeof(TIn)));
                         tma_load_1d(sm.buf[stage], row + col, (uint32_t)(n * sizeof(TIn)), &sm.full[stage]);
@@ -493,6 +543,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
                         ph ^= 1u;
                     }
                 }
+                w = w_next;
+                b = b_next;
+                r = r_next;
+                gamma = gamma_next;
+                k = k_next;
             }
             if (ok && mbar_wait(&sm.empty[stage], ph)) {
                 if (lane == 0) {
@@ -531,9 +586,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
         const int nvec = (n + E::VEC - 1) / E::VEC;
 
         if (first) {
-            const uint32_t item = a.stream_rows[row_slot];
-            b = (int)(item >> 8);
-            k = a.seq[b].k;
+            const int2 bk = sm.seqk[stage];
+            b = bk.x;
+            k = bk.y;
             run_max = -INFINITY;
             // theta_0: each warp takes the ceil(k/8)-th largest of its lanes' maxima
             // (ballot/popc, no block barrier); the minimum over the 8 warps leaves at
@@ -602,17 +657,27 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
                 any |= pass[q];
             }
             run_max = fmax_nan(run_max, run_value(rs));
-            if (any) {
+            if (__any_sync(0xFFFFFFFFu, any)) {
+                // per-element masks, then one slot reservation per warp
+                unsigned msk[Q];
+                unsigned mine = 0u;
 #pragma unroll
                 for (int q = 0; q < Q; ++q) {
-                    if (!pass[q]) continue;
+                    msk[q] = pass[q] ? pass_mask(v[q], thv, strict, (TIn*)nullptr) : 0u;
+                    mine += __popc(msk[q]);
+                }
+                unsigned slot = warp_reserve(sm, mine);
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
                     const int e0 = (q * kConsumers + t) * E::VEC;
-                    unsigned msk = pass_mask(v[q], thv, strict, (TIn*)nullptr);
-                    while (msk) {
-                        const int j = __ffs(msk) - 1;
-                        msk &= msk - 1u;
+                    unsigned mm = msk[q];
+                    while (mm) {
+                        const int j = __ffs(mm) - 1;
+                        mm &= mm - 1u;
+                        // a non-finite logit may be kept here; the piece is flagged by its maximum
                         const uint32_t bb = E::bits(v[q], j);
-                        if (!E::bad(bb)) append(sm, composite(E::key(bb), (uint32_t)(col0 + e0 + j)));
+                        if (slot < (unsigned)kBufCap) sm.cand[slot] = composite(E::key(bb), (uint32_t)(col0 + e0 + j));
+                        ++slot;
                     }
                 }
             }
@@ -651,24 +716,31 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
         }
 
         const int cnt = (int)sm.count;
-        if (last || cnt > max(4 * k, 256)) {
-            // raise theta to the exact k-th key of the buffer and drop what is below it;
-            // from then on the filter is strict: a later tie has a larger id
-            const int nmine = load_mine(sm, mine);
-            int gt = 0;
-            const uint32_t kth = cnt >= k ? buffer_kth_key<E::KB>(sm, mine, nmine, k, &gt) : 0u;
-            if (!last) {
-                if (cnt >= k) {
-                    buffer_keep_ge(sm, mine, nmine, kth);
-                    if (t == 0) {
-                        sm.theta_key = kth;
-                        sm.strict = 1;
-                    }
-                }
-            } else {
-                // hand every candidate >= the k-th key (ties included) to the combine kernel
+        if (!last) {
+            if (cnt > max(4 * k, 256)) {
+                // raise theta to the exact k-th key of the buffer and drop what is below it;
+                // from then on the filter is strict: a later tie has a larger id
+                const int nmine = load_mine(sm, mine);
+                int gt = 0;
+                const uint32_t kth = buffer_kth_key<E::KB>(sm, mine, nmine, k, &gt);
                 buffer_keep_ge(sm, mine, nmine, kth);
-                int total = (int)sm.count;
+                if (t == 0) {
+                    sm.theta_key = kth;
+                    sm.strict = 1;
+                }
+                cbar();
+            }
+        } else {
+            // hand the candidates to the combine kernel: all of them when few (a superset of
+            // the piece's top-k, which the combine kernel's exact sort resolves), else every
+            // candidate >= the k-th key (ties included)
+            int total = cnt;
+            if (cnt > kFinalList) {
+                const int nmine = load_mine(sm, mine);
+                int gt = 0;
+                const uint32_t kth = buffer_kth_key<E::KB>(sm, mine, nmine, k, &gt);
+                buffer_keep_ge(sm, mine, nmine, kth);
+                total = (int)sm.count;
                 if (total > kListCap) {  // very many ties: resolve them exactly here
                     const int n2 = next_pow2(total);
                     for (int i = total + t; i < n2; i += kConsumers) sm.cand[i] = 0ull;
@@ -676,15 +748,15 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
                     csort_desc(sm.cand, n2);
                     total = k;
                 }
-                unsigned long long* out = a.cand + (size_t)w * kListCap;
-                for (int i = t; i < total; i += kConsumers) out[i] = sm.cand[i];
-                // non-finite logits in this piece (NaN or +inf dominate the NaN-propagating max)
-                const bool nf = isnan(run_max) || run_max == INFINITY;
-                const int any_nf = cbar_count(nf);
-                if (t == 0) {
-                    a.cand_cnt[w] = (uint32_t)total;
-                    if (any_nf) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
-                }
+            }
+            unsigned long long* out = a.cand + (size_t)w * kListCap;
+            for (int i = t; i < total; i += kConsumers) out[i] = sm.cand[i];
+            // non-finite logits in this piece (NaN or +inf dominate the NaN-propagating max)
+            const bool nf = isnan(run_max) || run_max == INFINITY;
+            const int any_nf = cbar_count(nf);
+            if (t == 0) {
+                a.cand_cnt[w] = (uint32_t)total;
+                if (any_nf) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
             }
             cbar();
         }
