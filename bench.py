@@ -32,6 +32,9 @@ sys.path.insert(0, ROOT)
 METRIC = "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
+# kernels one spec_verify call launches: plan, select (streaming top-k), combine, dense
+# (the dense launch exits at once when no unit takes that path)
+LAUNCHES_PER_STEP = 4
 KERNEL_SOURCES = ("speculative_decoding_verification_20_gb300/csrc/sv_stream.cu",
                   "speculative_decoding_verification_20_gb300/csrc/sv_internal.cuh",
                   "speculative_decoding_verification_20_gb300/csrc/sv_finalize.cuh")
@@ -175,6 +178,28 @@ def run_reference(args):
     return 0
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of one float over all ranks (the slowest rank's time); x itself at world size 1."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, seconds_per_step: float) -> float:
+    """Units of all ranks per second: every rank processes its own batch (weak scaling)."""
+    return units_per_rank * world / seconds_per_step
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank verifies its own synthetic batch: the workload seed is the rank."""
+    return rank
+
+
 def workload_config(name: str, B: int | None = None) -> dict:
     from speculative_decoding_verification_20_gb300.workloads import CONFIGS
 
@@ -222,7 +247,7 @@ def main():
         dist.barrier()
     sv.load_library()
 
-    wl = workloads.make(args.workload, seed=rank, device=dev, B=args.batch)
+    wl = workloads.make(args.workload, seed=rank_seed(rank), device=dev, B=args.batch)
     B, G, V = wl.B, wl.G, wl.V
     stream = torch.cuda.current_stream(dev)
     ws = torch.empty(sv.workspace_size(B, G, V, sv.SV_BF16 if wl.dtype == "bf16" else sv.SV_F32), dtype=torch.uint8,
@@ -258,14 +283,10 @@ def main():
         wall1 = time.perf_counter()
     if world > 1:
         dist.barrier()
-    ms_total = t0.elapsed_time(t1)
-    t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total = float(t.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dev)
     ms_step = ms_total / args.steps
     positions = wl.positions()
-    value = positions * world / (ms_step * 1e-3)
+    value = whole_job_rate(positions, world, ms_step * 1e-3)
     kernel_ms = [a.elapsed_time(b) for a, b in kev]
     kernel_ms_avg = sum(kernel_ms) / len(kernel_ms)
     bytes_per_launch = wl.logit_bytes()
@@ -291,13 +312,10 @@ def main():
         for i in range(args.e2e_steps):
             outs = sv.spec_verify_host(*h, seed=2_000_000 + i, staging=staging, outputs=outs)
         w1 = time.perf_counter()
-        te = torch.tensor([w1 - w0], device=dev, dtype=torch.float64)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e_step = float(te.item()) / args.e2e_steps
+        e_step = max_over_ranks(w1 - w0, dev) / args.e2e_steps
         h2d = sum(x.numel() * x.element_size() for x in h if x is not None)
         d2h = sum(x.numel() * x.element_size() for x in outs.values())
-        e2e = {"value": positions * world / e_step, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": whole_job_rate(positions, world, e_step), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e_step * 1e3}
 
     if rank != 0:
@@ -318,11 +336,11 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
-                     "kernel": "stream_kernel (streaming top-k path)" if main == "stream" else "dense_kernel (cluster path)",
+                     "kernel": "select_kernel (streaming top-k path)" if main == "stream" else "dense kernel (cluster path)",
                      "kernel_ms": kernel_ms_avg, "algorithmic_bytes_per_launch": bytes_per_launch,
                      "traffic": traffic},
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
