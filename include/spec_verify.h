@@ -26,7 +26,8 @@
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers unless the name says host.  The
  *    caller owns every buffer; the library allocates nothing and keeps no
- *    state between calls beyond the caller's workspace.
+ *    state between calls beyond the caller's workspace (spec_verify_static
+ *    excepted: it uses a fixed buffer of the library's own).
  *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
  *    stream) and never synchronise with the host (spec_verify_host excepted).
  *  - Argument errors return a negative SV_E* status before anything is
@@ -59,7 +60,8 @@ typedef enum {
     SV_EUNSUPPORTED = -2, /* unsupported combination (e.g. dtype) */
     SV_ECUDA = -3,        /* a CUDA launch or runtime call failed */
     SV_ETOO_LARGE = -4,   /* V, gamma_max or B beyond the supported maximum */
-    SV_EWORKSPACE = -5    /* workspace missing or smaller than spec_verify_workspace_size() */
+    SV_EWORKSPACE = -5,   /* workspace missing or smaller than spec_verify_workspace_size() */
+    SV_ESCRATCH = -6      /* spec_verify_static: the shape needs more than SV_STATIC_SCRATCH_BYTES */
 } sv_status;
 
 /* per-sequence bits written to row_status */
@@ -167,6 +169,36 @@ int spec_verify_host(const void* host_target_logits, const void* host_draft_logi
                      uint64_t seed, int B, int gamma_max, int V, int32_t* host_accepted_len,
                      int32_t* host_out_tokens, float* host_alpha, void* device_staging, size_t staging_bytes,
                      void* stream);
+
+/*
+ * The same step as spec_verify with no workspace argument and no allocation:
+ * the scratch is a fixed device buffer of SV_STATIC_SCRATCH_BYTES owned by the
+ * library (the pages have no counterpart; this is a deployment form).
+ *
+ * For callers that cannot allocate device memory between decode steps: a
+ * plain C/C++ host with no caching allocator to own a workspace, or a loop
+ * that must not call cudaMalloc / cudaFree (cudaFree waits for the whole
+ * device, stalling every other stream).
+ *
+ * Arguments, outputs and errors are those of spec_verify, plus:
+ *  - SV_ESCRATCH, before anything is enqueued, when
+ *    spec_verify_workspace_size(B, gamma_max, V, dtype) > SV_STATIC_SCRATCH_BYTES
+ *    (8 MiB; that query tells a caller beforehand whether a shape fits -- decode
+ *    batches of a few dozen sequences at 128k-152k vocabularies do); beyond it,
+ *    use spec_verify with a workspace;
+ *  - SV_ECUDA if the buffer's address cannot be looked up.
+ * The first call on each device looks the buffer's address up (once); make
+ * that call outside any stream capture.  All calls on a device share the one
+ * buffer: calls that may overlap on the GPU race and must be ordered (one
+ * stream, or events).  Nothing has to be cleared between calls.
+ */
+#define SV_STATIC_SCRATCH_BYTES (8u << 20)
+
+int spec_verify_static(const void* target_logits, const void* draft_logits, int dtype,
+                       const int32_t* draft_tokens, const int32_t* num_draft, const float* temperature,
+                       const int32_t* top_k, const float* top_p, uint64_t seed, int B, int gamma_max, int V,
+                       int32_t* accepted_len, int32_t* out_tokens, float* alpha, float* p_out, float* q_out,
+                       uint32_t* row_status, void* stream);
 
 /* A static English description of a status code. */
 const char* spec_verify_strerror(int status);

@@ -31,7 +31,10 @@ ROW_NONFINITE = 0x20
 
 # every symbol include/spec_verify.h declares
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_verify_host",
-            "spec_verify_host_staging_size", "spec_verify_strerror")
+            "spec_verify_host_staging_size", "spec_verify_strerror", "spec_verify_static")
+
+SV_ESCRATCH = -6
+STATIC_SCRATCH_BYTES = 8 << 20  # SV_STATIC_SCRATCH_BYTES
 
 
 class SpecVerifyError(RuntimeError):
@@ -73,6 +76,8 @@ def load_library():
     lib.spec_verify_host_staging_size.restype = SZ
     lib.spec_verify_host.argtypes = [P, P, I, P, P, P, P, P, U64, I, I, I, P, P, P, P, SZ, P]
     lib.spec_verify_host.restype = I
+    lib.spec_verify_static.argtypes = [P, P, I, P, P, P, P, P, U64, I, I, I, P, P, P, P, P, P, P]
+    lib.spec_verify_static.restype = I
     lib.spec_verify_strerror.argtypes = [I]
     lib.spec_verify_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -222,5 +227,51 @@ def spec_verify_host(target, draft, draft_tokens, temperature, num_draft=None, t
                                   ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF), B, G, V,
                                   _ptr(outputs["accepted_len"]), _ptr(outputs["out_tokens"]), _ptr(outputs["alpha"]),
                                   _ptr(staging), staging.numel(), ctypes.c_void_p(s.cuda_stream))
+    _check(rc)
+    return outputs
+
+
+def spec_verify_static(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor, temperature,
+                       num_draft=None, top_k=None, top_p=None, *, seed: int, stream=None,
+                       outputs: Optional[dict] = None) -> dict:
+    """The no-allocation form: the library's fixed device scratch instead of a workspace.
+
+    For callers that must not allocate device memory between decode steps.  Pass
+    ``outputs`` (accepted_len [B] int32, out_tokens [B, G+1] int32, alpha [B, G]
+    float32, row_status [B] int32, all CUDA) to make the call allocate nothing
+    here either; parameter vectors given as CUDA int32/float32 tensors of B
+    entries are passed through as they are.  Raises SpecVerifyError with status
+    SV_ESCRATCH when the shape needs more than STATIC_SCRATCH_BYTES of scratch.
+    Calls that can overlap on the GPU share the scratch and race: keep them on
+    one stream.
+    """
+    lib = load_library()
+    if not (target.is_cuda and draft.is_cuda):
+        raise ValueError("target and draft must be CUDA tensors")
+    dt = _dtype_code(target)
+    if _dtype_code(draft) != dt:
+        raise TypeError("target and draft dtypes differ")
+    B, G1, V = target.shape
+    G = G1 - 1
+    if tuple(draft.shape) != (B, G, V) or not (target.is_contiguous() and draft.is_contiguous()):
+        raise ValueError("target [B, G+1, V] and draft [B, G, V] must be contiguous and match")
+    dev = target.device
+    toks = draft_tokens.to(device=dev, dtype=torch.int32).contiguous()
+    T = _dev_vec(temperature, B, torch.float32, dev, "temperature")
+    nd = _dev_vec(num_draft, B, torch.int32, dev, "num_draft")
+    tk = _dev_vec(top_k, B, torch.int32, dev, "top_k")
+    tp = _dev_vec(top_p, B, torch.float32, dev, "top_p")
+    if outputs is None:
+        outputs = dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+                       out_tokens=torch.empty(B, G + 1, dtype=torch.int32, device=dev),
+                       alpha=torch.empty(B, G, dtype=torch.float32, device=dev),
+                       row_status=torch.empty(B, dtype=torch.int32, device=dev))
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.spec_verify_static(_ptr(target), _ptr(draft), dt, _ptr(toks), _ptr(nd), _ptr(T), _ptr(tk), _ptr(tp),
+                                    ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF), B, G, V,
+                                    _ptr(outputs["accepted_len"]), _ptr(outputs["out_tokens"]),
+                                    _ptr(outputs["alpha"]), None, None, _ptr(outputs.get("row_status")),
+                                    ctypes.c_void_p(s.cuda_stream))
     _check(rc)
     return outputs

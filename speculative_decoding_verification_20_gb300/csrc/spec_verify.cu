@@ -186,6 +186,9 @@ extern "C" const char* spec_verify_strerror(int status) {
         case SV_ECUDA: return "a CUDA launch or runtime call failed";
         case SV_ETOO_LARGE: return "shape beyond the supported maximum (B, gamma_max or V)";
         case SV_EWORKSPACE: return "workspace missing or smaller than spec_verify_workspace_size()";
+        case SV_ESCRATCH:
+            return "shape needs more scratch than spec_verify_static's fixed buffer (SV_STATIC_SCRATCH_BYTES); "
+                   "use spec_verify with a workspace";
         default: return "unknown status";
     }
 }
