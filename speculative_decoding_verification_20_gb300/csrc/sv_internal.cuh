@@ -33,8 +33,8 @@ namespace sv {
 // configuration
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
-constexpr int kTileBytes = 32768;   // one TMA bulk copy
-constexpr int kTilesPerPiece = 8;   // a piece of a row: up to 256 KB of logits
+constexpr int kTileBytes = 28672;   // one TMA bulk copy: 7 16-byte vectors per consumer thread
+constexpr int kTilesPerPiece = 10;  // a piece of a row: up to 280 KB of logits (a whole 128k bf16 row)
 constexpr int kStreamMaxK = SV_STREAM_MAX_TOP_K;
 constexpr int kListCap = 512;   // candidates one piece hands to the combine kernel
 constexpr int kSortCap = 2048;  // candidates per row sorted in shared memory by the combine kernel
@@ -101,6 +101,11 @@ struct WsLayout {
 
 __host__ __device__ inline int tile_elems(int dtype) { return kTileBytes / (dtype == SV_BF16 ? 2 : 4); }
 __host__ __device__ inline int stream_piece_elems(int dtype) { return kTilesPerPiece * tile_elems(dtype); }
+// the combine kernel sorts all pieces' lists of a row at once
+static_assert(((SV_MAX_VOCAB + kTilesPerPiece * (kTileBytes / 4) - 1) / (kTilesPerPiece * (kTileBytes / 4))) *
+                      kListCap <=
+                  kSortCap,
+              "pieces per row times the list cap must fit the combine sort");
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

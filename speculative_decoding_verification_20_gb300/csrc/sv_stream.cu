@@ -8,23 +8,33 @@
 // read from HBM exactly once and no exponential is evaluated on the bulk of
 // the vocabulary.
 //
-// select_kernel (persistent, 2 CTAs per SM, 8 consumer warps + 1 producer warp)
-//   producer: pieces of rows are taken from a global counter; each 32 KB tile
-//     is brought into a 3-stage shared-memory ring by one cp.async.bulk
-//     (TMA) whose completion is counted on the stage's mbarrier.
-//   consumers: per 16-byte vector, a packed max tree (NaN-propagating, so it
-//     also detects non-finite logits) is compared once with the running
-//     threshold theta; only vectors that beat theta build a per-element pass
-//     mask and append those (key, token id) candidates to a shared buffer.
-//     theta starts at a lower bound of the k-th largest key of the piece's
-//     first tile (per-warp ballots over the per-thread maxima); whenever the
-//     buffer exceeds 2k entries, a block-wide 4-bit radix select finds the
-//     exact k-th key of the buffer, the buffer keeps only keys >= it, and the
-//     filter becomes strict (a later tie has a larger id, so it can never
-//     enter the top-k).
-//   At the end of a piece every candidate >= its exact k-th key (ties
-//   included, at most 512) is written to the workspace.
-// combine_kernel (one CTA per unit)
+// select_kernel (persistent, 2 CTAs per SM, 7 consumer warps + 1 producer warp)
+//   producer: pieces of rows are taken from a global counter (one piece ahead);
+//     each 28 KB tile is brought into a 3-stage shared-memory ring by one
+//     cp.async.bulk (TMA) whose completion is counted on the stage's mbarrier.
+//   consumers: every warp takes its own 16-byte vectors of each tile into
+//     registers.  A packed max tree per vector (NaN-propagating, so it also
+//     detects non-finite logits) is compared with the threshold; the thread's
+//     passing elements make one 64-bit mask, and only those few are read back
+//     from the tile and appended, as (key, token id), to the warp's own list in
+//     shared memory (then the stage goes back to the producer).
+//   threshold, speculative: a piece spanning several tiles starts from the
+//     (3k / tiles)-th largest of the warps' top lane maxima in its first tile,
+//     which aims at about the piece's 3k-th largest logit.  At the end of the
+//     piece it is checked: at least k logits reached it, so the piece's k-th
+//     largest logit is at or above it and the whole top-k was appended.  If
+//     not, the consumers redo the piece conservatively from global memory.
+//   threshold, conservative (single-tile pieces, large k, redo): the larger of
+//     the warp's own k-th largest key so far and the block floor min_w pub[w],
+//     where warp w publishes its ceil(k/W)-th largest key; the W warps then
+//     hold at least k keys >= the floor, so it never exceeds the piece's k-th
+//     largest key.  The list is re-selected after every tile it grew in.
+//   A list about to overflow is cut to its exact top-k (ties to the lower id).
+//   Warps meet only on a piece's first tile and at its end, on a bounded
+//   mbarrier.  At the end of a piece the warps' lists (a superset of the
+//   piece's top-k, at most 512 entries; else cut to exactly k) are written to
+//   the workspace.
+// combine_kernel (one warp per unit)
 //   merges the pieces of the unit's target and draft rows and does, in fp64,
 //   softmax over the kept logits, top-p, alpha, the acceptance test and the
 //   residual / bonus draw (inverse CDF in ascending token id).
@@ -37,11 +47,11 @@
 namespace sv {
 
 constexpr int kStages = 3;
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 7;  // with the producer, 8 warps: 2 CTAs per SM at up to 128 registers
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kSelThreads = kConsumers + 32;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-constexpr int kCombineThreads = 128;
+constexpr int kCombineThreads = 128;  // 4 warps
 
 // ---------------------------------------------------------------------------
 // PTX helpers: mbarriers, TMA bulk copies, the consumer-only named barrier
@@ -87,15 +97,6 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
-__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
-__device__ __forceinline__ int cbar_count(bool p) {
-    int r;
-    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %1, 0;\n bar.red.popc.u32 %0, 1, %2, q;\n}"
-                 : "=r"(r)
-                 : "r"((uint32_t)p), "n"(kConsumers)
-                 : "memory");
-    return r;
-}
 
 // ---------------------------------------------------------------------------
 // keys and composites
@@ -113,6 +114,11 @@ struct Elem<__nv_bfloat16> {
     __device__ static float value(uint32_t b) { return __uint_as_float(b << 16); }
     __device__ static double key_value(uint32_t k) { return (double)key_value16(k); }
     __device__ static bool bad(uint32_t b) { return bad16(b); }
+    // bit pattern of a float that holds a bf16 value exactly
+    __device__ static uint32_t bits_of(float f) { return __float_as_uint(f) >> 16; }
+    __device__ static uint32_t load_bits(const __nv_bfloat16* p, int i) {
+        return reinterpret_cast<const unsigned short*>(p)[i];
+    }
     static constexpr uint32_t kNegInfBits = 0xFF80u;
 };
 template <>
@@ -123,6 +129,8 @@ struct Elem<float> {
     __device__ static float value(uint32_t b) { return __uint_as_float(b); }
     __device__ static double key_value(uint32_t k) { return (double)key_value32(k); }
     __device__ static bool bad(uint32_t b) { return bad32(b); }
+    __device__ static uint32_t bits_of(float f) { return __float_as_uint(f); }
+    __device__ static uint32_t load_bits(const float* p, int i) { return reinterpret_cast<const uint32_t*>(p)[i]; }
     static constexpr uint32_t kNegInfBits = 0xFF800000u;
 };
 
@@ -203,40 +211,64 @@ struct RunOf<__nv_bfloat16> {
 // ---------------------------------------------------------------------------
 // select kernel
 // ---------------------------------------------------------------------------
-constexpr int kBufCap = 2048;   // candidate buffer
+constexpr int kWarpCap = kStreamMaxK + 32;          // a warp's list: its exact top-k plus one step of appends
+constexpr int kWarpSlots = kWarpCap / 32;           // list entries per lane
+constexpr int kBufCap = kConsumerWarps * kWarpCap;  // the warps' lists side by side
 constexpr int kPerThread = kBufCap / kConsumers;
-// a piece with at most this many candidates at its end hands them all over unselected
-constexpr int kFinalList = 512;
-static_assert(kFinalList <= kListCap && kFinalList >= kStreamMaxK, "final list bounds");
+static_assert(kWarpCap % 32 == 0 && kBufCap % kConsumers == 0, "list geometry");
+static_assert(kListCap <= kBufCap, "a piece's list fits the buffer");
+
 
 struct SelSmem {
     alignas(128) uint8_t buf[kStages][kTileBytes];
-    unsigned long long cand[kBufCap];  // (key << 32 | ~id), unsorted
+    unsigned long long cand[kBufCap];  // warp w's list at [w * kWarpCap, ...): (key << 32 | ~id), unsorted
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    int4 hdr[kStages];  // piece index (-1: no more work), tile index, elements, first column
-    int2 seqk[kStages]; // sequence b and its top-k for the piece
+    uint64_t gsync;                    // consumer-warp barrier (one arrival per warp, bounded waits)
+    int4 hdr[kStages];                 // piece index (-1: no more work), tile index, elements, first column
+    int2 seqk[kStages];                // sequence b and its top-k for the piece
+    uint32_t pub[kConsumerWarps];      // per warp: its ceil(k/W)-th largest key of the piece so far (0: none)
+    uint32_t spec[32];                 // warp w's largest lane maxima of a piece's first tile at [4w, 4w + 4)
     int red[kConsumerWarps];
     int scan[kConsumerWarps];
     int hist[16];
-    unsigned int count;
-    uint32_t theta_key;
-    int strict;
 };
 
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Barrier of the consumer warps on an mbarrier (8 arrivals per phase): bounded
+// like every other wait, so a lost copy cannot leave warps parked for good.
+// Once a wait has failed the warp stops taking part and reports false.
+struct GSync {
+    uint32_t ph;
+    bool ok;
+};
+__device__ __forceinline__ bool gbar(SelSmem& sm, GSync& g) {
+    __syncwarp();
+    if (!g.ok) return false;
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.gsync);
+    g.ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sm.gsync, g.ph));
+    g.ph ^= 1u;
+    return g.ok;
+}
+
 // block sum over the consumers
-__device__ __forceinline__ int csum(int v, SelSmem& sm) {
+__device__ __forceinline__ int gsum(int v, SelSmem& sm, GSync& g) {
     v = __reduce_add_sync(0xFFFFFFFFu, v);
     if ((threadIdx.x & 31) == 0) sm.red[threadIdx.x >> 5] = v;
-    cbar();
+    gbar(sm, g);
     int tot = 0;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) tot += sm.red[w];
-    cbar();
+    gbar(sm, g);
     return tot;
 }
 // exclusive scan over the consumers in thread order
-__device__ __forceinline__ int cscan(int v, SelSmem& sm, int* total) {
+__device__ __forceinline__ int gscan(int v, SelSmem& sm, GSync& g, int* total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int x = v;
 #pragma unroll
@@ -245,65 +277,238 @@ __device__ __forceinline__ int cscan(int v, SelSmem& sm, int* total) {
         if (lane >= o) x += y;
     }
     if (lane == 31) sm.scan[wid] = x;
-    cbar();
+    gbar(sm, g);
     int before = 0, tot = 0;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
         before += (w < wid) ? sm.scan[w] : 0;
         tot += sm.scan[w];
     }
-    cbar();
+    gbar(sm, g);
     *total = tot;
     return before + x - v;
 }
 
-__device__ __forceinline__ void append(SelSmem& sm, unsigned long long c) {
-    const unsigned slot = atomicAdd(&sm.count, 1u);
-    if (slot < (unsigned)kBufCap) sm.cand[slot] = c;
-}
-
-// Reserve `mine` consecutive buffer slots for this lane with one shared atomic
-// per warp (all lanes of the warp call it); returns the lane's first slot.
-__device__ __forceinline__ unsigned warp_reserve(SelSmem& sm, unsigned mine) {
-    const int lane = threadIdx.x & 31;
-    unsigned x = mine;
+// Exclusive prefix over the warp of a per-lane count c < 2^NB, and the warp total.
+template <int NB>
+__device__ __forceinline__ int warp_prefix(unsigned c, int* total) {
+    const unsigned lt = lanemask_lt();
+    int pre = 0, tot = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
+    for (int bit = 0; bit < NB; ++bit) {
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1u);
+        pre += __popc(bal & lt) << bit;
+        tot += __popc(bal) << bit;
     }
-    const unsigned total = __shfl_sync(0xFFFFFFFFu, x, 31);
-    unsigned base = 0u;
-    if (lane == 31 && total) base = atomicAdd(&sm.count, total);
-    return __shfl_sync(0xFFFFFFFFu, base, 31) + x - mine;
+    *total = tot;
+    return pre;
 }
 
-// Exact k-th largest key of the buffer (4-bit radix, shared histogram).
-// Every consumer holds up to kPerThread buffer entries in `mine`.  Returns the
-// key; *gt receives the number of entries strictly above it.
+// The ka-th and kb-th largest of the warp's keys (N per lane, the first `used`
+// slots in use, 0 = no entry): the largest c with at least ka (kb) keys >= c,
+// found bit by bit below the common prefix of the smallest and largest key;
+// 0 when the warp holds fewer keys.
+template <int KB, int N>
+__device__ __forceinline__ void warp_two_kth(const uint32_t (&key)[N], int used, int ka, int kb, uint32_t* xa,
+                                             uint32_t* xb) {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    unsigned cnt = 0u;
+#pragma unroll
+    for (int m = 0; m < N; ++m)
+        if (m < used && key[m] != 0u) {
+            lo = min(lo, key[m]);
+            hi = max(hi, key[m]);
+            ++cnt;
+        }
+    lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+    hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+    if (cnt < (unsigned)ka && cnt < (unsigned)kb) {
+        *xa = *xb = 0u;
+        return;
+    }
+    const uint32_t diff = lo ^ hi;
+    const int nb = diff ? 32 - __clz(diff) : 0;  // bits below the common prefix
+    const uint32_t base = nb >= 32 ? 0u : (lo & ~((1u << nb) - 1u));
+    uint32_t pa = base, pb = base;
+#pragma unroll 1
+    for (int bit = nb - 1; bit >= 0; --bit) {
+        const uint32_t ca = pa | (1u << bit), cb = pb | (1u << bit);
+        unsigned na = 0u, nbb = 0u;
+#pragma unroll
+        for (int m = 0; m < N; ++m)
+            if (m < used) {
+                na += key[m] >= ca;
+                nbb += key[m] >= cb;
+            }
+        na = __reduce_add_sync(0xFFFFFFFFu, na);
+        nbb = __reduce_add_sync(0xFFFFFFFFu, nbb);
+        if (na >= (unsigned)ka) pa = ca;
+        if (nbb >= (unsigned)kb) pb = cb;
+    }
+    *xa = cnt >= (unsigned)ka ? pa : 0u;
+    *xb = cnt >= (unsigned)kb ? pb : 0u;
+    (void)KB;
+}
+
+// lower bound of the piece's k-th key from every warp's published estimate (a
+// stale value is lower, so still a lower bound)
+__device__ __forceinline__ uint32_t block_floor(const SelSmem& sm, int lane) {
+    const uint32_t pv = lane < kConsumerWarps ? ((const volatile uint32_t*)sm.pub)[lane] : 0xFFFFFFFFu;
+    return __reduce_min_sync(0xFFFFFFFFu, pv);
+}
+
+struct WarpList {
+    int cnt;          // entries in the warp's list
+    uint32_t th_own;  // the warp's own threshold key (its k-th largest so far; 0: none)
+};
+
+// Refresh a warp's list (N slots per lane cover it): publish its ceil(k/8)-th
+// largest key, raise its own threshold to its k-th largest key and keep only
+// the keys >= max(that, the block floor).  With `exact`, ties at the k-th key
+// beyond k entries are cut too (lowest ids kept), so at most k entries remain.
+template <int KB, int N>
+__device__ __forceinline__ WarpList warp_refresh_n(SelSmem& sm, int warp, int lane, WarpList st, int k, int kw,
+                                                   bool exact) {
+    unsigned long long* L = sm.cand + warp * kWarpCap;
+    const int used = (st.cnt + 31) >> 5;
+    unsigned long long e[N];
+    uint32_t key[N];
+#pragma unroll
+    for (int m = 0; m < N; ++m) {
+        const int i = lane + 32 * m;
+        e[m] = (m < used && i < st.cnt) ? L[i] : 0ull;
+        key[m] = comp_key(e[m]);
+    }
+    uint32_t xw, xk;
+    warp_two_kth<KB, N>(key, used, kw, k, &xw, &xk);
+    if (lane == 0 && xw > ((volatile uint32_t*)sm.pub)[warp]) ((volatile uint32_t*)sm.pub)[warp] = xw;
+    if (xk > st.th_own) st.th_own = xk;
+    const uint32_t floor = block_floor(sm, lane);
+    const uint32_t cut = max(st.th_own, floor);
+    uint32_t id_cut = 0xFFFFFFFFu;
+    if (exact && xk > 0u && xk >= floor) {  // ties at the k-th key beyond k entries: lowest ids (< 2^18)
+        unsigned gt = 0u, eq = 0u;
+#pragma unroll
+        for (int m = 0; m < N; ++m) {
+            gt += key[m] > xk;
+            eq += key[m] == xk;
+        }
+        gt = __reduce_add_sync(0xFFFFFFFFu, gt);
+        eq = __reduce_add_sync(0xFFFFFFFFu, eq);
+        const unsigned need = (unsigned)k - gt;
+        if (eq > need) {
+            uint32_t lo = 0u;
+#pragma unroll 1
+            for (int bit = 17; bit >= 0; --bit) {
+                const uint32_t c = lo | (1u << bit);
+                unsigned nlt = 0u;
+#pragma unroll
+                for (int m = 0; m < N; ++m) nlt += key[m] == xk && (uint32_t)comp_id(e[m]) < c;
+                nlt = __reduce_add_sync(0xFFFFFFFFu, nlt);
+                if (nlt < need) lo = c;
+            }
+            id_cut = lo;
+        }
+    }
+    // compact in place: every entry is already in registers
+    __syncwarp();
+    const unsigned lt = lanemask_lt();
+    int base = 0;
+#pragma unroll
+    for (int m = 0; m < N; ++m) {
+        if (m < used) {
+            const bool keep = key[m] != 0u && key[m] >= cut && !(key[m] == xk && (uint32_t)comp_id(e[m]) > id_cut);
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+            if (keep) L[base + __popc(bal & lt)] = e[m];
+            base += __popc(bal);
+        }
+    }
+    __syncwarp();
+    st.cnt = base;
+    return st;
+}
 template <int KB>
-__device__ uint32_t buffer_kth_key(SelSmem& sm, const unsigned long long (&mine)[kPerThread], int nmine, int k,
-                                   int* gt) {
+__device__ __noinline__ WarpList warp_refresh(SelSmem& sm, int warp, int lane, WarpList st, int k, int kw,
+                                              bool exact) {
+    if (st.cnt <= 64) return warp_refresh_n<KB, 2>(sm, warp, lane, st, k, kw, exact);
+    if (st.cnt <= 128) return warp_refresh_n<KB, 4>(sm, warp, lane, st, k, kw, exact);
+    return warp_refresh_n<KB, kWarpSlots>(sm, warp, lane, st, k, kw, exact);
+}
+// out-of-line exact refresh for the rare overflow path inside the tile loop
+template <int KB>
+__device__ __noinline__ WarpList warp_refresh_out(SelSmem& sm, int warp, int lane, WarpList st, int k, int kw) {
+    return warp_refresh_n<KB, kWarpSlots>(sm, warp, lane, st, k, kw, true);
+}
+
+// per-element pass mask of one 16-byte vector: value >= the threshold value
+__device__ __forceinline__ unsigned pass_mask(const uint4& v, float thv, __nv_bfloat16*) {
+    const __nv_bfloat162 th2 = __float2bfloat162_rn(thv);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    unsigned msk = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+        const unsigned m = __hge2_mask(x, th2);
+        msk |= ((m & 1u) | ((m >> 15) & 2u)) << (2 * i);
+    }
+    return msk;
+}
+__device__ __forceinline__ unsigned pass_mask(const uint4& v, float thv, float*) {
+    const float x[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w)};
+    unsigned msk = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) msk |= (x[i] >= thv) ? (1u << i) : 0u;
+    return msk;
+}
+
+// Rare fallback at the end of a piece whose warps' lists together exceed
+// kListCap: gather them, find the exact k-th key of the union (4-bit radix),
+// resolve ties at it by id, and write exactly k entries.  Returns the count.
+template <int KB>
+__device__ __noinline__ int piece_cut(SelSmem& sm, GSync& g, int warp, int lane, int cnt, int off, int total, int k,
+                         unsigned long long* out) {
+    const int t = threadIdx.x;
+    // gather into one contiguous array (through registers: the lists overlap it)
+    unsigned long long e[kWarpSlots];
+    const unsigned long long* L = sm.cand + warp * kWarpCap;
+#pragma unroll
+    for (int m = 0; m < kWarpSlots; ++m) {
+        const int i = lane + 32 * m;
+        e[m] = i < cnt ? L[i] : 0ull;
+    }
+    gbar(sm, g);
+#pragma unroll
+    for (int m = 0; m < kWarpSlots; ++m) {
+        const int i = lane + 32 * m;
+        if (i < cnt) sm.cand[off + i] = e[m];
+    }
+    gbar(sm, g);
+    total = min(total, kBufCap);
+    unsigned long long mine[kPerThread];
+    int nmine = 0;
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int idx = t + i * kConsumers;
+        mine[i] = idx < total ? sm.cand[idx] : 0ull;
+        nmine += idx < total;
+    }
+    // k-th largest key of the union: 4-bit digits from the top, shared histogram
     uint32_t prefix = 0u;
     int above = 0;
 #pragma unroll 1
     for (int sh = KB - 4; sh >= 0; sh -= 4) {
-        if (threadIdx.x < 16) sm.hist[threadIdx.x] = 0;
-        cbar();
+        if (t < 16) sm.hist[t] = 0;
+        gbar(sm, g);
 #pragma unroll
         for (int i = 0; i < kPerThread; ++i) {
-            if (!__any_sync(0xFFFFFFFFu, i < nmine)) break;
-            int digit = -1;
             if (i < nmine) {
                 const uint32_t key = comp_key(mine[i]);
                 const bool match = (sh + 4 >= KB) || ((key >> (sh + 4)) == (prefix >> (sh + 4)));
-                if (match) digit = (int)((key >> sh) & 15u);
+                if (match) atomicAdd(&sm.hist[(key >> sh) & 15u], 1);
             }
-            // one shared atomic per distinct digit of the warp
-            const unsigned grp = __match_any_sync(0xFFFFFFFFu, digit);
-            if (digit >= 0 && (threadIdx.x & 31) == __ffs(grp) - 1) atomicAdd(&sm.hist[digit], __popc(grp));
         }
-        cbar();
+        gbar(sm, g);
         int acc = above, dsel = 0;
         for (int d = 15; d >= 0; --d) {
             const int h = sm.hist[d];
@@ -315,146 +520,347 @@ __device__ uint32_t buffer_kth_key(SelSmem& sm, const unsigned long long (&mine)
         }
         above = acc;
         prefix |= (uint32_t)dsel << sh;
-        cbar();
+        gbar(sm, g);
     }
-    *gt = above;
-    return prefix;
-}
-
-// Keep the buffer entries with key >= kth (every consumer re-appends its own).
-__device__ __forceinline__ void buffer_keep_ge(SelSmem& sm, const unsigned long long (&mine)[kPerThread], int nmine,
-                                               uint32_t kth) {
-    if (threadIdx.x == 0) sm.count = 0u;
-    cbar();
-    unsigned keep = 0u;
+    const uint32_t kth = prefix;
+    const int need = k - above;  // ties at kth to keep, lowest ids first
+    int eq = 0;
 #pragma unroll
-    for (int i = 0; i < kPerThread; ++i) keep += (i < nmine && comp_key(mine[i]) >= kth) ? 1u : 0u;
-    unsigned slot = warp_reserve(sm, keep);
+    for (int i = 0; i < kPerThread; ++i) eq += i < nmine && comp_key(mine[i]) == kth;
+    uint32_t id_cut = 0xFFFFFFFFu;
+    if (gsum(eq, sm, g) > need) {
+        uint32_t lo = 0u;
+#pragma unroll 1
+        for (int bit = 17; bit >= 0; --bit) {
+            const uint32_t c = lo | (1u << bit);
+            int nlt = 0;
 #pragma unroll
-    for (int i = 0; i < kPerThread; ++i)
-        if (i < nmine && comp_key(mine[i]) >= kth) sm.cand[slot++] = mine[i];
-    cbar();
-}
-
-__device__ __forceinline__ int load_mine(SelSmem& sm, unsigned long long (&mine)[kPerThread]) {
-    const int cnt = min((int)sm.count, kBufCap);
-    int n = 0;
+            for (int i = 0; i < kPerThread; ++i)
+                nlt += i < nmine && comp_key(mine[i]) == kth && (uint32_t)comp_id(mine[i]) < c;
+            if (gsum(nlt, sm, g) < need) lo = c;
+        }
+        id_cut = lo;
+    }
+    int keep = 0;
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
-        const int idx = threadIdx.x + i * kConsumers;
-        mine[i] = idx < cnt ? sm.cand[idx] : 0ull;
-        n += idx < cnt;
+        const uint32_t key = comp_key(mine[i]);
+        keep += i < nmine && (key > kth || (key == kth && (uint32_t)comp_id(mine[i]) <= id_cut));
     }
-    return n;
+    int written;
+    int slot = gscan(keep, sm, g, &written);
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const uint32_t key = comp_key(mine[i]);
+        if (i < nmine && (key > kth || (key == kth && (uint32_t)comp_id(mine[i]) <= id_cut)) && slot < kListCap)
+            out[slot++] = mine[i];
+    }
+    return min(written, kListCap);
 }
 
-// per-element pass mask of one 16-byte vector against the threshold value
-__device__ __forceinline__ unsigned pass_mask(const uint4& v, float thv, bool strict, __nv_bfloat16*) {
-    const __nv_bfloat162 th2 = __float2bfloat162_rn(thv);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    unsigned msk = 0;
+// ---------------------------------------------------------------------------
+// consumer steps
+// ---------------------------------------------------------------------------
+constexpr int kSpecFactor = 3;  // the speculative threshold aims at the piece's (3k)-th largest logit
+constexpr int kSpecPub = 4;     // lane maxima each warp publishes for it
+constexpr int kSpecMaxRank = kSpecPub * kConsumerWarps;
+static_assert(kSpecMaxRank <= 32, "the published maxima fit one per lane");
+
+// Bitonic sort of one value per lane across the warp, descending: lane i ends
+// with the i-th largest.
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t x, int lane) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-        const unsigned m = strict ? __hgt2_mask(x, th2) : __hge2_mask(x, th2);
-        msk |= ((m & 1u) | ((m >> 15) & 2u)) << (2 * i);
-    }
-    return msk;
-}
-__device__ __forceinline__ unsigned pass_mask(const uint4& v, float thv, bool strict, float*) {
-    const float x[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w)};
-    unsigned msk = 0;
+    for (int k2 = 2; k2 <= 32; k2 <<= 1)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) msk |= (strict ? (x[i] > thv) : (x[i] >= thv)) ? (1u << i) : 0u;
-    return msk;
+        for (int j = k2 >> 1; j > 0; j >>= 1) {
+            const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
+            const bool lower = (lane & j) == 0;
+            const bool desc = (lane & k2) == 0;  // this block's direction (all descending at the end)
+            x = (lower == desc) ? max(x, y) : min(x, y);
+        }
+    return x;
 }
 
-// Exact top-k of one tile appended to the buffer (used when a tile would
-// overflow it): k-th largest key by a bitwise search, then the keys above it
-// and the lowest-id ties at it.
+// Rank (in the piece's first tile) whose value is the speculative threshold of
+// a piece of `tiles` tiles, or 0 when the piece is handled conservatively from
+// the start (a single tile, where it would gain nothing, or a large k).
+__device__ __forceinline__ int spec_rank(int k, int tiles) {
+    if (tiles < 2) return 0;
+    const int j = min(k, max(1, (kSpecFactor * k + tiles - 1) / tiles));
+    return j <= kSpecMaxRank ? j : 0;
+}
+
+struct CState {
+    WarpList st;
+    int since;        // appends since the last refresh
+    int appended;     // appends in this piece
+    bool overflow;    // the list had to be cut inside the piece
+    bool spec;        // the piece runs on a speculative threshold
+    float run_max;    // NaN-propagating maximum of the piece's logits seen by this warp
+    uint32_t th_spec; // speculative threshold key
+};
+
+// The vectors of one tile held by a warp (v; the tile's elements at elem, n of
+// them from column col0): filter against the warp's threshold, append what
+// passes to its list.
+//   first tile of a piece: reset, then the starting thresholds from the
+//     per-vector maxima (one barrier): speculative -- the spec_rank-th largest
+//     of the warps' top maxima together; conservative -- every warp publishes
+//     its ceil(k/8)-th largest maximum and starts at its own k-th.
+//   conservative pieces refresh the list after every tile that appended.
+// Returns false if a barrier wait gave up.
 template <typename TIn>
-__device__ void tile_exact_append(SelSmem& sm, const uint4* tile, int nvec, int n, int col0, int k) {
+__device__ __forceinline__ bool consume_tile(SelSmem& sm, GSync& g, const uint4 (&v)[kTileBytes / 16 / kConsumers],
+                                             const TIn* elem, int n, int col0, bool first, bool last, int tiles,
+                                             int k, CState& cs, int warp, int lane) {
     using E = Elem<TIn>;
     constexpr int Q = kTileBytes / 16 / kConsumers;
     const int t = threadIdx.x;
-    uint32_t kth = 0u;
-    for (int bit = E::KB - 1; bit >= 0; --bit) {
-        const uint32_t c = kth | (1u << bit);
-        int mine = 0;
+    const int kw = (k + kConsumerWarps - 1) / kConsumerWarps;
+    unsigned long long* L = sm.cand + warp * kWarpCap;
+    if (first) {
+        cs.st = WarpList{0, 0u};
+        cs.since = cs.appended = 0;
+        cs.overflow = false;
+        cs.run_max = -INFINITY;
+        cs.th_spec = 0u;
+        // per-vector maxima (a NaN or +inf maximum is left out)
+        uint32_t vk[Q];
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-            const int vi = q * kConsumers + t;
-            if (vi < nvec) {
-                const uint4 v = tile[vi];
+            const int e0 = (q * kConsumers + t) * E::VEC;
+            float mv = -INFINITY;
+            if (e0 + E::VEC <= n) {
+                mv = vmax_nan(v[q], (TIn*)nullptr);
+            } else {
 #pragma unroll
                 for (int j = 0; j < E::VEC; ++j)
-                    mine += (vi * E::VEC + j < n) && !E::bad(E::bits(v, j)) && E::key(E::bits(v, j)) >= c;
+                    if (e0 + j < n) mv = fmax_nan(mv, E::value(E::bits(v[q], j)));
             }
+            vk[q] = (isnan(mv) || mv == INFINITY || e0 >= n) ? 0u : E::key(E::bits_of(mv));
         }
-        if (csum(mine, sm) >= k) kth = c;
+        if (cs.spec) {
+            // every warp publishes its kSpecPub largest lane maxima; the threshold is
+            // the j-th largest of them all
+            const int j = spec_rank(k, tiles);
+            uint32_t lm = 0u;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) lm = max(lm, vk[q]);
+            lm = warp_sort_desc(lm, lane);
+            if (lane < kSpecPub) sm.spec[warp * kSpecPub + lane] = lm;
+            if (!gbar(sm, g)) return false;
+            uint32_t u = lane < kSpecMaxRank ? sm.spec[lane] : 0u;
+            u = warp_sort_desc(u, lane);
+            cs.th_spec = __shfl_sync(0xFFFFFFFFu, u, j - 1);
+        } else {
+            uint32_t xw, xk;
+            warp_two_kth<E::KB, Q>(vk, Q, kw, k, &xw, &xk);
+            if (lane == 0) sm.pub[warp] = xw;
+            cs.st.th_own = xk;
+            if (!gbar(sm, g)) return false;
+        }
     }
-    int gt = 0;
+
+    const uint32_t th = cs.spec ? max(cs.th_spec, cs.st.th_own) : max(cs.st.th_own, block_floor(sm, lane));
+    const float thv = th == 0u ? -INFINITY : (float)E::key_value(th);
+    // filter: one pass bit per element of this thread's vectors (bit q * VEC + j)
+    static_assert(Q * E::VEC <= 64, "a thread's elements of a tile fit one mask");
+    typename RunOf<TIn>::type rs;
+    run_init(rs, thv);
+    unsigned long long pm = 0ull;
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
-        const int vi = q * kConsumers + t;
-        if (vi < nvec) {
-            const uint4 v = tile[vi];
+        const int e0 = (q * kConsumers + t) * E::VEC;
+        unsigned msk = 0u;
+        if (e0 + E::VEC <= n) {
+            if (vec_test(v[q], rs, false)) msk = pass_mask(v[q], thv, (TIn*)nullptr);
+        } else if (e0 < n) {  // the tile's ragged end
 #pragma unroll
             for (int j = 0; j < E::VEC; ++j) {
-                const uint32_t b = E::bits(v, j);
-                if (vi * E::VEC + j < n && !E::bad(b) && E::key(b) > kth) {
-                    append(sm, composite(E::key(b), (uint32_t)(col0 + vi * E::VEC + j)));
-                    ++gt;
+                const uint32_t bb = E::bits(v[q], j);
+                if (e0 + j < n) {
+                    cs.run_max = fmax_nan(cs.run_max, E::value(bb));
+                    if (!E::bad(bb) && E::key(bb) >= th) msk |= 1u << j;
                 }
             }
         }
+        pm |= (unsigned long long)msk << (q * E::VEC);
     }
-    const int need = k - csum(gt, sm);
-    int base = 0;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        const int vi = q * kConsumers + t;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        int mine = 0;
-        if (vi < nvec) {
-            v = tile[vi];
-#pragma unroll
-            for (int j = 0; j < E::VEC; ++j)
-                mine += (vi * E::VEC + j < n) && !E::bad(E::bits(v, j)) && E::key(E::bits(v, j)) == kth;
-        }
+    cs.run_max = fmax_nan(cs.run_max, run_value(rs));
+
+    // append: what passed is read back from the tile (elem) by index
+    if (__any_sync(0xFFFFFFFFu, pm != 0ull)) {
         int tot;
-        int rank = base + cscan(mine, sm, &tot);
-        if (mine) {
-#pragma unroll
-            for (int j = 0; j < E::VEC; ++j) {
-                const uint32_t b = E::bits(v, j);
-                if (vi * E::VEC + j < n && !E::bad(b) && E::key(b) == kth) {
-                    if (rank < need) append(sm, composite(kth, (uint32_t)(col0 + vi * E::VEC + j)));
-                    ++rank;
+        const int pre = warp_prefix<7>((unsigned)__popcll(pm), &tot);
+        if (cs.st.cnt + tot <= kWarpCap) {
+            int slot = cs.st.cnt + pre;
+            while (pm) {
+                const int i = __ffsll((long long)pm) - 1;
+                pm &= pm - 1ull;
+                const int e = ((i / E::VEC) * kConsumers + t) * E::VEC + (i % E::VEC);
+                L[slot++] = composite(E::key(E::load_bits(elem, e)), (uint32_t)(col0 + e));
+            }
+            cs.st.cnt += tot;
+            cs.since += tot;
+            cs.appended += tot;
+        } else {
+            // the list would overflow: append one element position at a time (at most
+            // 32 entries) and cut the list to its exact top-k when it is full (a cut
+            // leaves at most k <= kWarpCap - 32 entries)
+#pragma unroll 1
+            for (int i = 0; i < Q * E::VEC; ++i) {
+                bool p = (pm >> i) & 1ull;
+                unsigned bal = __ballot_sync(0xFFFFFFFFu, p);
+                if (!bal) continue;
+                const int e = ((i / E::VEC) * kConsumers + t) * E::VEC + (i % E::VEC);
+                const uint32_t key = p ? E::key(E::load_bits(elem, e)) : 0u;
+                if (cs.st.cnt + __popc(bal) > kWarpCap) {
+                    cs.st = warp_refresh_out<E::KB>(sm, warp, lane, cs.st, k, kw);
+                    cs.overflow = true;
+                    cs.since = 0;
+                    const uint32_t th2 = cs.spec ? max(cs.th_spec, cs.st.th_own)
+                                                 : max(cs.st.th_own, block_floor(sm, lane));
+                    p = p && key >= th2;
+                    bal = __ballot_sync(0xFFFFFFFFu, p);
                 }
+                if (p) L[cs.st.cnt + __popc(bal & lanemask_lt())] = composite(key, (uint32_t)(col0 + e));
+                cs.st.cnt += __popc(bal);
+                cs.since += __popc(bal);
+                cs.appended += __popc(bal);
             }
         }
-        base += tot;
     }
-    cbar();
+
+    if (!cs.spec && (cs.since > 0 || last)) {
+        __syncwarp();
+        cs.st = warp_refresh<E::KB>(sm, warp, lane, cs.st, k, kw, false);
+        cs.since = 0;
+    }
+    return true;
 }
 
-// bitonic sort (descending) of n = 2^m buffer entries by the consumers
-__device__ __forceinline__ void csort_desc(unsigned long long* s, int n) {
-    for (int k2 = 2; k2 <= n; k2 <<= 1)
-        for (int j = k2 >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < n; i += kConsumers) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const unsigned long long x = s[i], y = s[ixj];
-                    if (((i & k2) == 0) ? (x < y) : (x > y)) {
-                        s[i] = y;
-                        s[ixj] = x;
-                    }
+// End of a piece: every warp's list goes to the workspace (at most kListCap
+// entries together; else cut to exactly k).  A speculative piece is only
+// accepted if at least k of its logits reached the threshold (or a list had to
+// be cut, which needs more than k): then the piece's k-th largest logit is at
+// or above it and every logit of the top-k was appended.
+// Returns 1 when written, 0 when the speculation failed (nothing written, the
+// piece must be redone conservatively), -1 when a barrier wait gave up.
+template <int KB>
+__device__ __forceinline__ int finish_piece(SelSmem& sm, GSync& g, const Args& a, int w, int b, int k, CState& cs, int warp,
+                           int lane) {
+    unsigned long long* L = sm.cand + warp * kWarpCap;
+    if (!gbar(sm, g)) return -1;  // every warp's final estimate is published
+    if (!cs.spec) {
+        const uint32_t floor = block_floor(sm, lane);
+        const int used = (cs.st.cnt + 31) >> 5;
+        const unsigned lt = lanemask_lt();
+        int base = 0;
+        for (int m = 0; m < used; ++m) {  // drop what is below the final floor
+            const int i = lane + 32 * m;
+            const unsigned long long e = i < cs.st.cnt ? L[i] : 0ull;
+            const bool keep = i < cs.st.cnt && comp_key(e) >= floor;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+            __syncwarp();
+            if (keep) L[base + __popc(bal & lt)] = e;
+            base += __popc(bal);
+        }
+        cs.st.cnt = base;
+    }
+    const bool nf = __any_sync(0xFFFFFFFFu, isnan(cs.run_max) || cs.run_max == INFINITY);
+    if (lane == 0) {
+        sm.scan[warp] = cs.st.cnt | (nf ? 0x10000 : 0) | (cs.overflow ? 0x20000 : 0);
+        sm.red[warp] = cs.appended;
+    }
+    if (!gbar(sm, g)) return -1;
+    int off = 0, total = 0, appended = 0;
+    bool any_nf = false, any_overflow = false;
+#pragma unroll
+    for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+        const int sv = sm.scan[w2];
+        off += w2 < warp ? (sv & 0xFFFF) : 0;
+        total += sv & 0xFFFF;
+        any_nf |= (sv & 0x10000) != 0;
+        any_overflow |= (sv & 0x20000) != 0;
+        appended += sm.red[w2];
+    }
+    if (lane == 0) sm.pub[warp] = 0u;  // every warp has read the floor: reset for the next piece
+    if (cs.spec && !any_overflow && appended < k) return 0;
+    unsigned long long* out = a.cand + (size_t)w * kListCap;
+    int written = total;
+    if (total <= kListCap) {
+        for (int i = lane; i < cs.st.cnt; i += 32) out[off + i] = L[i];
+    } else {
+        GSync g2 = g;  // the out-of-line call gets a copy, so g stays in registers
+        written = piece_cut<KB>(sm, g2, warp, lane, cs.st.cnt, off, total, k, out);
+        g = g2;
+        if (!g.ok) return -1;
+    }
+    if (threadIdx.x == 0) {
+        a.cand_cnt[w] = (uint32_t)written;
+        if (any_nf) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+    }
+    return 1;
+}
+
+// A tile's vectors for this consumer straight from global memory (the redo of
+// a piece): 16-byte loads when rows are 16-byte aligned, else element loads.
+template <typename TIn, bool VEC16>
+__device__ __forceinline__ void load_global_tile(const TIn* row, int col0, int n, int t,
+                                                 uint4 (&v)[kTileBytes / 16 / kConsumers]) {
+    using E = Elem<TIn>;
+    constexpr int Q = kTileBytes / 16 / kConsumers;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int e0 = (q * kConsumers + t) * E::VEC;
+        if (VEC16) {
+            v[q] = e0 < n ? __ldg(reinterpret_cast<const uint4*>(row + col0) + (q * kConsumers + t))
+                          : make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            uint32_t wd[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int j = 0; j < E::VEC; ++j) {
+                if (e0 + j < n) {
+                    uint32_t bits;
+                    if (sizeof(TIn) == 2)
+                        bits = __ldg(reinterpret_cast<const unsigned short*>(row + col0) + e0 + j);
+                    else
+                        bits = __ldg(reinterpret_cast<const unsigned int*>(row + col0) + e0 + j);
+                    if (sizeof(TIn) == 2)
+                        wd[j >> 1] |= bits << (16 * (j & 1));
+                    else
+                        wd[j] = bits;
                 }
             }
-            cbar();
+            v[q] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
+    }
+}
+
+// The speculative threshold was too high for piece w (fewer than k logits
+// reached it): do the piece again, conservatively, reading it straight from
+// global memory.  Out of line, so that the main loop keeps its registers.
+template <typename TIn, bool TMA>
+__device__ __noinline__ bool redo_piece(SelSmem& sm, GSync& g, const Args& a, int w, int b, int k, int c0, int c1,
+                                        int warp, int lane) {
+    constexpr int TE = kTileBytes / (int)sizeof(TIn);
+    const int V = a.V, G = a.G;
+    const uint32_t item = a.stream_rows[(uint32_t)w / (uint32_t)a.ppr];
+    const int r = (int)(item & 0xFFu);
+    const int gamma = a.seq[b].gamma;
+    const TIn* row = (r <= gamma) ? (const TIn*)a.target + ((size_t)b * (G + 1) + r) * (size_t)V
+                                  : (const TIn*)a.draft + ((size_t)b * G + (r - gamma - 1)) * (size_t)V;
+    CState cs;
+    cs.spec = false;
+    uint4 v[kTileBytes / 16 / kConsumers];
+    for (int col = c0; col < c1; col += TE) {
+        const int n = min(TE, c1 - col);
+        load_global_tile<TIn, TMA>(row, col, n, threadIdx.x, v);
+        if (!consume_tile<TIn>(sm, g, v, row + col, n, col, col == c0, col + n >= c1, (c1 - c0 + TE - 1) / TE, k, cs,
+                               warp, lane))
+            return false;
+    }
+    return finish_piece<Elem<TIn>::KB>(sm, g, a, w, b, k, cs, warp, lane) >= 0;
 }
 
 template <typename TIn, bool TMA>
@@ -473,8 +879,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kConsumerWarps);
         }
+        mbar_init(&sm.gsync, kConsumerWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (t < kConsumerWarps) sm.pub[t] = 0u;
     __syncthreads();
     const uint32_t n_pieces = a.counts[kCntStreamRows] * (uint32_t)ppr;
 
@@ -567,251 +975,181 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
     // ------------------------------ consumers ------------------------------
     int stage = 0;
     uint32_t ph = 0;
+    GSync g{0u, true};
     int k = 1, b = 0;
-    float run_max = -INFINITY;
-    unsigned long long mine[kPerThread];
+    CState cs;
+    cs.st = WarpList{0, 0u};
     while (true) {
-        if (!mbar_wait(&sm.full[stage], ph)) {
-            if (t == 0) atomicOr(&a.counts[kCntError], 1u);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sm.full[stage], ph))) {
+            g.ok = false;
             break;
         }
         const int4 h = sm.hdr[stage];
         if (h.x < 0) break;
+        const int2 bk = sm.seqk[stage];
         const int w = h.x, tile_idx = h.y, n = h.z, col0 = h.w;
         const uint32_t row_slot = (uint32_t)w / (uint32_t)ppr;
         const int piece = w - (int)row_slot * ppr;
-        const bool first = tile_idx == 0;
-        const bool last = col0 + n >= min(V, piece * PE + PE);
+        const int c0 = piece * PE, c1 = min(V, c0 + PE);
+        const bool last = col0 + n >= c1;
+        // this warp's vectors of the tile into registers; the stage goes straight back
+        // this warp's vectors of the tile into registers; the stage goes back once the
+        // few elements that pass have been read again
         const uint4* tile = reinterpret_cast<const uint4*>(sm.buf[stage]);
-        const int nvec = (n + E::VEC - 1) / E::VEC;
-
-        if (first) {
-            const int2 bk = sm.seqk[stage];
+        uint4 v[Q];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) v[q] = tile[q * kConsumers + t];
+        if (tile_idx == 0) {
             b = bk.x;
             k = bk.y;
-            run_max = -INFINITY;
-            // theta_0: each warp takes the ceil(k/8)-th largest of its lanes' maxima
-            // (ballot/popc, no block barrier); the minimum over the 8 warps leaves at
-            // least 8 * ceil(k/8) >= k elements of the tile >= theta_0, so every
-            // element of the piece's top-k passes the filter
-            uint32_t tmax = 0u;
-            if (n == TE) {  // full tile: max tree per vector (a NaN/+inf maximum is left out)
-#pragma unroll
-                for (int q = 0; q < Q; ++q) {
-                    typename RunOf<TIn>::type rs;
-                    run_init(rs, 0.0f);
-                    (void)vec_test(tile[q * kConsumers + t], rs, false);
-                    const float mv = run_value(rs);
-                    if (!(isnan(mv) || mv == INFINITY)) tmax = max(tmax, okey32(__float_as_uint(mv)) >> (32 - E::KB));
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < Q; ++q) {
-                    const int vi = q * kConsumers + t;
-                    if (vi < nvec) {
-                        const uint4 v = tile[vi];
-#pragma unroll
-                        for (int j = 0; j < E::VEC; ++j) {
-                            const uint32_t bb = E::bits(v, j);
-                            if (vi * E::VEC + j < n && !E::bad(bb)) tmax = max(tmax, E::key(bb));
-                        }
-                    }
-                }
-            }
-            const int kw = (k + kConsumerWarps - 1) / kConsumerWarps;
-            uint32_t thw = 0u;
-            for (int bit = E::KB - 1; bit >= 0; --bit) {
-                const uint32_t c = thw | (1u << bit);
-                if (__popc(__ballot_sync(0xFFFFFFFFu, tmax >= c)) >= kw) thw = c;
-            }
-            if (lane == 0) sm.red[warp] = (int)thw;
-            cbar();
-            uint32_t th = 0xFFFFFFFFu;
-#pragma unroll
-            for (int w2 = 0; w2 < kConsumerWarps; ++w2) th = min(th, (uint32_t)sm.red[w2]);
-            if (t == 0) {
-                sm.count = 0u;
-                sm.theta_key = th;
-                sm.strict = 0;
-            }
+            cs.spec = spec_rank(k, (c1 - c0 + TE - 1) / TE) > 0;
         }
-        cbar();
-        const unsigned count_before = sm.count;
-        const uint32_t th_key = sm.theta_key;
-        const bool strict = sm.strict != 0;
-        const float thv = th_key == 0u ? -INFINITY : (float)E::key_value(th_key);
-
-        if (n == TE && th_key != 0u) {
-            // fast path for a full tile: all loads first, then one max tree and one
-            // packed comparison per vector
-            uint4 v[Q];
-#pragma unroll
-            for (int q = 0; q < Q; ++q) v[q] = tile[q * kConsumers + t];
-            typename RunOf<TIn>::type rs;
-            run_init(rs, thv);
-            bool pass[Q];
-            bool any = false;
-#pragma unroll
-            for (int q = 0; q < Q; ++q) {
-                pass[q] = vec_test(v[q], rs, strict);
-                any |= pass[q];
-            }
-            run_max = fmax_nan(run_max, run_value(rs));
-            if (__any_sync(0xFFFFFFFFu, any)) {
-                // per-element masks, then one slot reservation per warp
-                unsigned msk[Q];
-                unsigned mine = 0u;
-#pragma unroll
-                for (int q = 0; q < Q; ++q) {
-                    msk[q] = pass[q] ? pass_mask(v[q], thv, strict, (TIn*)nullptr) : 0u;
-                    mine += __popc(msk[q]);
-                }
-                unsigned slot = warp_reserve(sm, mine);
-#pragma unroll
-                for (int q = 0; q < Q; ++q) {
-                    const int e0 = (q * kConsumers + t) * E::VEC;
-                    unsigned mm = msk[q];
-                    while (mm) {
-                        const int j = __ffs(mm) - 1;
-                        mm &= mm - 1u;
-                        // a non-finite logit may be kept here; the piece is flagged by its maximum
-                        const uint32_t bb = E::bits(v[q], j);
-                        if (slot < (unsigned)kBufCap) sm.cand[slot] = composite(E::key(bb), (uint32_t)(col0 + e0 + j));
-                        ++slot;
-                    }
-                }
-            }
-        } else {
-            // partial tile, or no threshold yet: element by element
-#pragma unroll
-            for (int q = 0; q < Q; ++q) {
-                const int vi = q * kConsumers + t;
-                if (vi >= nvec) continue;
-                const uint4 v = tile[vi];
-                const int e0 = vi * E::VEC;
-#pragma unroll
-                for (int j = 0; j < E::VEC; ++j) {
-                    if (e0 + j >= n) continue;
-                    const uint32_t bb = E::bits(v, j);
-                    run_max = fmax_nan(run_max, E::value(bb));
-                    if (E::bad(bb)) continue;
-                    const uint32_t key = E::key(bb);
-                    if (strict ? (key > th_key) : (key >= th_key)) append(sm, composite(key, (uint32_t)(col0 + e0 + j)));
-                }
-            }
-        }
-        cbar();
-        if (sm.count > (unsigned)kBufCap) {  // this tile overflowed the buffer: append its exact top-k instead
-            cbar();
-            if (t == 0) sm.count = count_before;
-            cbar();
-            tile_exact_append<TIn>(sm, tile, nvec, n, col0, k);
-        }
-        // the stage can be refilled
+        const bool ok = consume_tile<TIn>(sm, g, v, reinterpret_cast<const TIn*>(sm.buf[stage]), n, col0,
+                                          tile_idx == 0, last, (c1 - c0 + TE - 1) / TE, k, cs, warp, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
         if (++stage == kStages) {
             stage = 0;
             ph ^= 1u;
         }
+        if (!ok) break;
+        if (!last) continue;
 
-        const int cnt = (int)sm.count;
-        if (!last) {
-            if (cnt > max(4 * k, 256)) {
-                // raise theta to the exact k-th key of the buffer and drop what is below it;
-                // from then on the filter is strict: a later tie has a larger id
-                const int nmine = load_mine(sm, mine);
-                int gt = 0;
-                const uint32_t kth = buffer_kth_key<E::KB>(sm, mine, nmine, k, &gt);
-                buffer_keep_ge(sm, mine, nmine, kth);
-                if (t == 0) {
-                    sm.theta_key = kth;
-                    sm.strict = 1;
-                }
-                cbar();
-            }
-        } else {
-            // hand the candidates to the combine kernel: all of them when few (a superset of
-            // the piece's top-k, which the combine kernel's exact sort resolves), else every
-            // candidate >= the k-th key (ties included)
-            int total = cnt;
-            if (cnt > kFinalList) {
-                const int nmine = load_mine(sm, mine);
-                int gt = 0;
-                const uint32_t kth = buffer_kth_key<E::KB>(sm, mine, nmine, k, &gt);
-                buffer_keep_ge(sm, mine, nmine, kth);
-                total = (int)sm.count;
-                if (total > kListCap) {  // very many ties: resolve them exactly here
-                    const int n2 = next_pow2(total);
-                    for (int i = total + t; i < n2; i += kConsumers) sm.cand[i] = 0ull;
-                    cbar();
-                    csort_desc(sm.cand, n2);
-                    total = k;
-                }
-            }
-            unsigned long long* out = a.cand + (size_t)w * kListCap;
-            for (int i = t; i < total; i += kConsumers) out[i] = sm.cand[i];
-            // non-finite logits in this piece (NaN or +inf dominate the NaN-propagating max)
-            const bool nf = isnan(run_max) || run_max == INFINITY;
-            const int any_nf = cbar_count(nf);
-            if (t == 0) {
-                a.cand_cnt[w] = (uint32_t)total;
-                if (any_nf) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
-            }
-            cbar();
+        int r = finish_piece<E::KB>(sm, g, a, w, b, k, cs, warp, lane);
+        if (r < 0) break;
+        if (r == 0) {
+            GSync g2 = g;  // the out-of-line call gets a copy, so g stays in registers
+            const bool ok = redo_piece<TIn, TMA>(sm, g2, a, w, b, k, c0, c1, warp, lane);
+            g = g2;
+            if (!ok) break;
         }
     }
+    if (!g.ok && lane == 0) atomicOr(&a.counts[kCntError], 1u);
 }
+
 
 // ---------------------------------------------------------------------------
 // combine kernel
 // ---------------------------------------------------------------------------
-struct CombSmem {
-    unsigned long long sort[kSortCap];
-    unsigned long long top[2][kStreamMaxK];
+constexpr int kCombineWarps = 4;  // one unit per warp
+constexpr int kSelBuf = 512;      // a warp's scratch for a row's candidates
+static_assert(kSelBuf >= kStreamMaxK + 32, "the scratch holds a top-k plus one load step");
+
+struct CombWarp {
+    unsigned long long buf[kSelBuf];        // candidates of the row being selected
+    unsigned long long top[2][kStreamMaxK]; // kept entries of the target / draft row, (key desc, id asc)
     double prob[2][kStreamMaxK];
     double resid[kStreamMaxK];
     int rid[kStreamMaxK];
-    int kept[2];
 };
+
+// Keep the exact top-k (key descending, then id ascending) of buf[0..m) in
+// buf[0..k), unordered; returns the count.  The k-th key is found bit by bit
+// below the common prefix of the smallest and largest key (warp reductions),
+// ties at it by id (ids < 2^18).
+template <int KB>
+__device__ int warp_keep_topk(unsigned long long* buf, int m, int k, int lane) {
+    __syncwarp();
+    if (m <= k) return m;
+    constexpr int M = kSelBuf / 32;
+    const int used = (m + 31) >> 5;
+    unsigned long long e[M];
+    uint32_t key[M];
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const int idx = lane + 32 * i;
+        e[i] = (i < used && idx < m) ? buf[idx] : 0ull;
+        key[i] = comp_key(e[i]);
+        if (key[i] != 0u) {
+            lo = min(lo, key[i]);
+            hi = max(hi, key[i]);
+        }
+    }
+    lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+    hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const uint32_t diff = lo ^ hi;
+    const int nb = diff ? 32 - __clz(diff) : 0;
+    uint32_t kth = nb >= 32 ? 0u : (lo & ~((1u << nb) - 1u));
+#pragma unroll 1
+    for (int bit = nb - 1; bit >= 0; --bit) {
+        const uint32_t c = kth | (1u << bit);
+        unsigned n = 0u;
+#pragma unroll
+        for (int i = 0; i < M; ++i)
+            if (i < used) n += key[i] >= c;
+        if (__reduce_add_sync(0xFFFFFFFFu, n) >= (unsigned)k) kth = c;
+    }
+    unsigned gt = 0u, eq = 0u;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        gt += key[i] > kth;
+        eq += key[i] == kth;
+    }
+    gt = __reduce_add_sync(0xFFFFFFFFu, gt);
+    eq = __reduce_add_sync(0xFFFFFFFFu, eq);
+    const unsigned need = (unsigned)k - gt;
+    uint32_t id_cut = 0xFFFFFFFFu;
+    if (eq > need) {
+        uint32_t idl = 0u;
+#pragma unroll 1
+        for (int bit = 17; bit >= 0; --bit) {
+            const uint32_t c = idl | (1u << bit);
+            unsigned nlt = 0u;
+#pragma unroll
+            for (int i = 0; i < M; ++i) nlt += key[i] == kth && (uint32_t)comp_id(e[i]) < c;
+            if (__reduce_add_sync(0xFFFFFFFFu, nlt) < need) idl = c;
+        }
+        id_cut = idl;
+    }
+    __syncwarp();
+    const unsigned lt = lanemask_lt();
+    int base = 0;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        if (i < used) {
+            const bool keep = key[i] > kth || (key[i] == kth && (uint32_t)comp_id(e[i]) <= id_cut);
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+            if (keep) buf[base + __popc(bal & lt)] = e[i];
+            base += __popc(bal);
+        }
+    }
+    __syncwarp();
+    return base;
+}
 
 // Exact top-k of a row, sorted by (logit desc, id asc), from its pieces' candidate
 // lists (each a superset of that piece's top-k); returns how many were found (k normally).
-__device__ int merge_row(const Args& a, uint32_t row_slot, int k, unsigned long long* out, CombSmem& sm) {
+template <int KB>
+__device__ int row_topk(const Args& a, uint32_t row_slot, int k, CombWarp& sw, unsigned long long* top, int lane) {
     const int ppr = a.ppr;
-    int total = 0;
-    for (int j = 0; j < ppr; ++j) total += (int)__ldcg(&a.cand_cnt[(size_t)row_slot * ppr + j]);
-    const int n2 = next_pow2(total < 2 ? 2 : total);
-    int off = 0;
+    int kept = 0;
     for (int j = 0; j < ppr; ++j) {
         const size_t piece = (size_t)row_slot * ppr + j;
         const int c = (int)__ldcg(&a.cand_cnt[piece]);
-        for (int i = threadIdx.x; i < c; i += blockDim.x) sm.sort[off + i] = __ldcg(&a.cand[piece * kListCap + i]);
-        off += c;
-    }
-    for (int i = total + threadIdx.x; i < n2; i += blockDim.x) sm.sort[i] = 0ull;
-    __syncthreads();
-    for (int k2 = 2; k2 <= n2; k2 <<= 1)
-        for (int j = k2 >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const unsigned long long x = sm.sort[i], y = sm.sort[ixj];
-                    if (((i & k2) == 0) ? (x < y) : (x > y)) {
-                        sm.sort[i] = y;
-                        sm.sort[ixj] = x;
-                    }
-                }
-            }
-            __syncthreads();
+        const unsigned long long* src = a.cand + piece * kListCap;
+        for (int i0 = 0; i0 < c;) {
+            if (kept + 32 > kSelBuf) kept = warp_keep_topk<KB>(sw.buf, kept, k, lane);
+            const int take = min(c - i0, kSelBuf - kept);
+#pragma unroll 4
+            for (int i = lane; i < take; i += 32) sw.buf[kept + i] = __ldcg(&src[i0 + i]);
+            kept += take;
+            i0 += take;
         }
-    const int kk = total < k ? total : k;
-    for (int i = threadIdx.x; i < kk; i += blockDim.x) out[i] = sm.sort[i];
-    __syncthreads();
-    return kk;
+    }
+    kept = warp_keep_topk<KB>(sw.buf, kept, k, lane);
+    // order by composite, descending: an entry's rank is the number of larger ones
+    for (int i = lane; i < kept; i += 32) {
+        const unsigned long long e = sw.buf[i];
+        int r = 0;
+        for (int j = 0; j < kept; ++j) r += sw.buf[j] > e;
+        top[r] = e;
+    }
+    __syncwarp();
+    return kept;
 }
 
-// fp64 normalisation of one sorted kept list by warp 0: softmax over the kept
+// fp64 normalisation of one sorted kept list by one warp: softmax over the kept
 // logits at temperature T (one-hot if T == 0), then top-p.  prob[j] for j < k.
 template <typename TIn>
 __device__ void normalise_kept(const unsigned long long* top, int k, float Tf, float Pf, double* prob) {
@@ -864,16 +1202,15 @@ __device__ void normalise_kept(const unsigned long long* top, int k, float Tf, f
 }
 
 template <typename TIn>
-__device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, CombSmem& sm) {
+__device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, CombWarp& sm, int lane) {
     const int G = a.G;
     const bool pair = unit < si.gamma;
     const uint32_t slot_t = si.row_off + (uint32_t)unit;
     const uint32_t slot_d = si.row_off + (uint32_t)si.gamma + 1u + (uint32_t)unit;
-    const int kt = merge_row(a, slot_t, si.k, sm.top[0], sm);  // exact top-k, ties to the lower id
-    const int kd = pair ? merge_row(a, slot_d, si.k, sm.top[1], sm) : 0;
+    const int kt = row_topk<Elem<TIn>::KB>(a, slot_t, si.k, sm, sm.top[0], lane);  // exact top-k, ties to the lower id
+    const int kd = pair ? row_topk<Elem<TIn>::KB>(a, slot_d, si.k, sm, sm.top[1], lane) : 0;
 
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
+    {
         // a row without a finite logit (or with non-finite ones, already flagged)
         const uint32_t ninf_key = Elem<TIn>::key(Elem<TIn>::kNegInfBits);
         const bool dead = kt < 1 || comp_key(sm.top[0][0]) <= ninf_key ||
@@ -989,24 +1326,27 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
                     a.q_out[((size_t)b * G + unit) * a.V + comp_id(sm.top[1][j])] = (float)sm.prob[1][j];
         }
     }
-    unit_finished(a, b);
+    unit_finished_warp(a, b, lane);
 }
 
+// one warp per unit (target row i with draft row i, or the bonus row alone)
 template <typename TIn>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Args a) {
-    __shared__ CombSmem sm;
+    extern __shared__ __align__(16) uint8_t comb_raw[];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    CombWarp& sw = reinterpret_cast<CombWarp*>(comb_raw)[wid];
     const uint32_t n_units = a.counts[kCntStreamUnits];
     const bool failed = a.counts[kCntError] != 0u;
-    for (uint32_t w = blockIdx.x; w < n_units; w += gridDim.x) {
+    for (uint32_t w = blockIdx.x * kCombineWarps + wid; w < n_units; w += gridDim.x * kCombineWarps) {
         const uint32_t item = a.stream_units[w];
         const int b = (int)(item >> 8), unit = (int)(item & 0xFFu);
         const SeqInfo si = a.seq[b];
         if (failed) {  // a select CTA gave up waiting: no result of this call can be trusted
-            if (threadIdx.x == 0) atomicOr(&a.seq_status[b], SV_ROW_INTERNAL);
-            unit_finished(a, b);
+            if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_INTERNAL);
+            unit_finished_warp(a, b, lane);
             continue;
         }
-        combine_unit<TIn>(a, b, unit, si, sm);
+        combine_unit<TIn>(a, b, unit, si, sw, lane);
     }
 }
 
@@ -1036,10 +1376,19 @@ cudaError_t launch_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev && ev[1]) cudaEventRecord((cudaEvent_t)ev[1], s);
-    long long cgrid = (long long)a.B * (a.G + 1);
-    if (cgrid > (long long)sms * 16) cgrid = (long long)sms * 16;
+    const int csmem = (int)(kCombineWarps * sizeof(CombWarp));
+    static const bool cattr_ok = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem) ==
+                                 cudaSuccess;
+    if (!cattr_ok) return cudaErrorInvalidValue;
+    static const int cocc = [&] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, comb, kCombineThreads, csmem) != cudaSuccess) n = 1;
+        return n > 0 ? n : 1;
+    }();
+    long long cgrid = ((long long)a.B * (a.G + 1) + kCombineWarps - 1) / kCombineWarps;
+    if (cgrid > (long long)sms * cocc) cgrid = (long long)sms * cocc;
     if (cgrid < 1) cgrid = 1;
-    comb<<<(unsigned)cgrid, kCombineThreads, 0, s>>>(a);
+    comb<<<(unsigned)cgrid, kCombineThreads, csmem, s>>>(a);
     return cudaGetLastError();
 }
 }  // namespace
