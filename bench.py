@@ -32,9 +32,10 @@ sys.path.insert(0, ROOT)
 METRIC = "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
-# kernels one spec_verify call launches: plan, select (streaming top-k), combine, dense
-# (the dense launch exits at once when no unit takes that path)
-LAUNCHES_PER_STEP = 4
+# kernels one spec_verify call launches: plan, select (streaming top-k), combine,
+# the unfiltered whole-row kernel and the dense cluster kernel (a kernel whose
+# path no row takes exits at once)
+LAUNCHES_PER_STEP = 5
 KERNEL_SOURCES = ("speculative_decoding_verification_20_gb300/csrc/sv_stream.cu",
                   "speculative_decoding_verification_20_gb300/csrc/sv_internal.cuh",
                   "speculative_decoding_verification_20_gb300/csrc/sv_finalize.cuh")
@@ -262,7 +263,12 @@ def main():
     torch.cuda.synchronize(dev)
 
     # per-step events around the dominant kernel, recorded by the library on the launching stream
-    main = "stream" if (wl.top_k is not None and int(wl.top_k.max()) <= sv.SV_STREAM_MAX_TOP_K) else "dense"
+    if wl.top_k is not None and int(wl.top_k.max()) <= sv.SV_STREAM_MAX_TOP_K:
+        main = "stream"
+    elif wl.top_k is None and wl.top_p is None and float(wl.temperature.min()) > 0.0:
+        main = "free"
+    else:
+        main = "dense"
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a_, b_ in kev:  # torch creates the underlying CUDA events on their first record
         a_.record(stream)
@@ -336,7 +342,9 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
-                     "kernel": "select_kernel (streaming top-k path)" if main == "stream" else "dense kernel (cluster path)",
+                     "kernel": {"stream": "select_kernel (streaming top-k path)",
+                                "free": "free_kernel (whole-row path of unfiltered rows)",
+                                "dense": "dense_kernel (cluster path)"}[main],
                      "kernel_ms": kernel_ms_avg, "algorithmic_bytes_per_launch": bytes_per_launch,
                      "traffic": traffic},
         "e2e": e2e,

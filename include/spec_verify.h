@@ -115,7 +115,8 @@ int spec_verify(const void* target_logits, const void* draft_logits, int dtype, 
 
 /* Path selection for spec_verify_ex (testing and measurement). */
 typedef enum {
-    SV_PATH_AUTO = 0,  /* greedy and top_k <= SV_STREAM_MAX_TOP_K rows: streaming top-k path; others: dense */
+    SV_PATH_AUTO = 0,  /* greedy and top_k <= SV_STREAM_MAX_TOP_K rows: streaming top-k path; rows with no
+                          top-k and no top-p: whole-row path; others: dense cluster path */
     SV_PATH_DENSE = 1  /* every row through the dense (whole-row, cluster) path */
 } sv_path;
 
@@ -131,7 +132,9 @@ typedef enum {
  *   path       sv_path
  *   ev_stream  two cudaEvent_t (or NULL) recorded on `stream` immediately
  *              before and after the streaming top-k kernel
- *   ev_dense   the same around the dense cluster kernel
+ *   ev_dense   the same around the dense cluster kernel (top-p, top-k > 256)
+ *   ev_free    the same around the whole-row kernel of unfiltered rows
+ *              (no top-k, no top-p)
  */
 typedef struct {
     uint32_t struct_size;
@@ -140,6 +143,7 @@ typedef struct {
     int32_t path;
     void* ev_stream[2];
     void* ev_dense[2];
+    void* ev_free[2];
 } sv_options;
 
 int spec_verify_ex(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,

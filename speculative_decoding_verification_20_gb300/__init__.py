@@ -45,7 +45,8 @@ class SpecVerifyError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32), ("pos_accept", ctypes.c_void_p), ("pos_token", ctypes.c_void_p),
-                ("path", ctypes.c_int32), ("ev_stream", ctypes.c_void_p * 2), ("ev_dense", ctypes.c_void_p * 2)]
+                ("path", ctypes.c_int32), ("ev_stream", ctypes.c_void_p * 2), ("ev_dense", ctypes.c_void_p * 2),
+                ("ev_free", ctypes.c_void_p * 2)]
 
 
 _lib = None
@@ -150,8 +151,9 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.T
     tensors, sequences or scalars (None = off / all G).  Returns a dict with
     accepted_len [B], out_tokens [B, G+1], alpha [B, G], row_status [B] and, on
     request, p_out / q_out (probs=True) and pos_accept / pos_token (positions=True).
-    events: {"stream": (begin, end), "dense": (begin, end)} torch.cuda.Event pairs that the
-    library records on the launching stream around its streaming and dense kernels.
+    events: {"stream": (begin, end), "dense": (begin, end), "free": (begin, end)} torch.cuda.Event
+    pairs that the library records on the launching stream around its streaming top-k, dense
+    cluster and unfiltered whole-row kernels.
     """
     lib = load_library()
     if not (target.is_cuda and draft.is_cuda):
@@ -189,7 +191,7 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.T
     ws = workspace if workspace is not None else _workspace(need, dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     opts = _Options(ctypes.sizeof(_Options), _ptr(pa), _ptr(pt), SV_PATH_DENSE if path == "dense" else SV_PATH_AUTO)
-    for key in ("stream", "dense"):  # optional (begin, end) torch.cuda.Event pairs around each kernel
+    for key in ("stream", "dense", "free"):  # optional (begin, end) torch.cuda.Event pairs around each kernel
         if events and events.get(key):
             getattr(opts, "ev_" + key)[0] = events[key][0].cuda_event
             getattr(opts, "ev_" + key)[1] = events[key][1].cuda_event

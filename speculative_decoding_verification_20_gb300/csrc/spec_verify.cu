@@ -45,7 +45,7 @@ __device__ __forceinline__ uint32_t block_excl_scan_1024(uint32_t v, uint32_t* s
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
     __shared__ uint32_t s_warp[32];
-    uint32_t base_rows = 0, base_units = 0, base_sunits = 0;
+    uint32_t base_rows = 0, base_units = 0, base_sunits = 0, base_funits = 0;
     const int G = a.G, V = a.V;
     for (int b0 = 0; b0 < a.B; b0 += blockDim.x) {
         const int b = b0 + threadIdx.x;
@@ -76,18 +76,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
                     P = 1.0f;
                 }
                 const bool stream = (k >= 1 && k <= kStreamMaxK);
-                mode = (stream && !a.force_dense) ? kModeStream : kModeDense;
+                const bool unfiltered = k == 0 && P >= 1.0f;
+                mode = a.force_dense ? kModeDense : stream ? kModeStream : unfiltered ? kModeFree : kModeDense;
                 if (mode == kModeStream)
                     nrows = 2 * gamma + 1;
-                else
+                else if (mode == kModeDense)
                     nunits = gamma + 1;
             }
         }
         const uint32_t nsunits = (mode == kModeStream) ? (uint32_t)(gamma + 1) : 0u;
-        uint32_t tot_r, tot_u, tot_s;
+        const uint32_t nfunits = (mode == kModeFree) ? (uint32_t)(gamma + 1) : 0u;
+        uint32_t tot_r, tot_u, tot_s, tot_f;
         const uint32_t off_r = block_excl_scan_1024(nrows, s_warp, &tot_r);
         const uint32_t off_u = block_excl_scan_1024(nunits, s_warp, &tot_u);
         const uint32_t off_s = block_excl_scan_1024(nsunits, s_warp, &tot_s);
+        const uint32_t off_f = block_excl_scan_1024(nfunits, s_warp, &tot_f);
         if (b < a.B) {
             SeqInfo si;
             si.mode = mode;
@@ -105,6 +108,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
             for (uint32_t r = 0; r < nrows; ++r) a.stream_rows[base_rows + off_r + r] = ((uint32_t)b << 8) | r;
             for (uint32_t u = 0; u < nunits; ++u) a.dense_units[base_units + off_u + u] = ((uint32_t)b << 8) | u;
             for (uint32_t u = 0; u < nsunits; ++u) a.stream_units[base_sunits + off_s + u] = ((uint32_t)b << 8) | u;
+            for (uint32_t u = 0; u < nfunits; ++u) a.free_units[base_funits + off_f + u] = ((uint32_t)b << 8) | u;
             const int first_pad = st ? 0 : gamma;
             for (int i = first_pad; i < G; ++i) {
                 a.alpha[(size_t)b * G + i] = 0.0f;
@@ -121,11 +125,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
         base_rows += tot_r;
         base_units += tot_u;
         base_sunits += tot_s;
+        base_funits += tot_f;
     }
     if (threadIdx.x == 0) {
         a.counts[kCntStreamRows] = base_rows;
         a.counts[kCntDenseUnits] = base_units;
         a.counts[kCntStreamUnits] = base_sunits;
+        a.counts[kCntFreeUnits] = base_funits;
+        a.counts[kCntFreeNext] = 0u;
         a.counts[kCntPieceNext] = 0u;
         a.counts[kCntError] = 0u;
     }
@@ -154,6 +161,7 @@ DeviceInfo& device_info(int dev) {
 cudaError_t launch_all(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, const sv_options& o) {
     cudaError_t e;
     if ((e = launch_stream_kernel(dtype, vector, a, sms, s, o.ev_stream)) != cudaSuccess) return e;
+    if ((e = launch_free_kernel(dtype, vector, a, sms, s, o.ev_free)) != cudaSuccess) return e;
     if (o.ev_dense[0]) cudaEventRecord((cudaEvent_t)o.ev_dense[0], s);
     e = (dtype == SV_BF16) ? launch_dense_bf16(vector, a, sms, s) : launch_dense_f32(vector, a, sms, s);
     if (e != cudaSuccess) return e;
@@ -253,6 +261,7 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
     a.stream_rows = (uint32_t*)(ws + L.stream_rows);
     a.dense_units = (uint32_t*)(ws + L.dense_units);
     a.stream_units = (uint32_t*)(ws + L.stream_units);
+    a.free_units = (uint32_t*)(ws + L.free_units);
     a.counts = (uint32_t*)(ws + L.counts);
     a.cand = (unsigned long long*)(ws + L.cand);
     a.cand_cnt = (uint32_t*)(ws + L.cand_cnt);

@@ -1,0 +1,770 @@
+// sv_free.cu -- whole-row path of unfiltered sequences (no top-k, no top-p,
+// temperature > 0).
+//
+// A unit is (target row i, draft row i) for i <= gamma_b, or the bonus unit
+// (target row gamma_b+1 alone, q := 0).  With no filter, p and q are plain
+// softmaxes of the whole vocabulary at temperature T ("Fast Inference from
+// Transformers via Speculative Decoding" review page, section "Method:
+// Speculative Decoding"), and each unit needs:
+//   - the normaliser of each row (pass 1: online maximum and sum of exp),
+//   - alpha = sum_x min(p, q) and the residual weights r = max(0, p - q)
+//     (p for the bonus row), summed per tile (pass 2),
+//   - the acceptance test u * q(x) < p(x) of the draft token
+//     ("Speculative decoding: the art of guessing well", section 投机采样),
+//   - the residual / bonus draw: v = u * sum r, the tile where the running sum
+//     of r passes v, then the token inside it (a re-read of that one tile).
+//
+// free_kernel (persistent, 2 CTAs per SM, 7 consumer warps + 1 producer warp)
+//   The producer claims units from a global counter and streams each unit's
+//   rows twice through a 3-stage ring (a stage holds a 14 KB segment of each
+//   row) by TMA bulk copies: pass 1 reads HBM, pass 2 reads the same bytes
+//   again while they are still in L2.  Consumers work on 16-byte vectors in
+//   registers; per-thread sums are Kahan-compensated fp32, warp sums use an
+//   exact two-sum, and sums across warps and tiles are fp64.
+//   Every wait (ring and the consumers' own barrier) is bounded (2 s); on a
+//   timeout the CTA records kCntError and the affected sequences are marked.
+#include "sv_finalize.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kFStages = 3;
+constexpr int kFWarps = 7;  // with the producer, 8 warps: 2 CTAs per SM at up to 128 registers
+constexpr int kFConsumers = 32 * kFWarps;
+constexpr int kFThreads = kFConsumers + 32;
+constexpr int kFSegBytes = 14336;                     // one row's segment of a stage
+constexpr int kFVec = kFSegBytes / 16 / kFConsumers;  // 16-byte vectors per consumer per segment
+constexpr int kFMaxTiles = (SV_MAX_VOCAB * 4 + kFSegBytes - 1) / kFSegBytes;
+constexpr unsigned long long kFWaitNs = 2000000000ull;
+static_assert(kFVec * 16 * kFConsumers == kFSegBytes, "segment geometry");
+
+struct FreeSmem {
+    alignas(128) uint8_t buf[kFStages][2][kFSegBytes];  // [stage][target, draft segment]
+    uint64_t full[kFStages];
+    uint64_t empty[kFStages];
+    uint64_t gsync;
+    int4 hdr[kFStages];             // unit index (-1: no more work), pass, tile, elements
+    float wr[kFMaxTiles][kFWarps];  // pass 2: per tile and warp, sum of the residual weights
+    float wp[kFMaxTiles][kFWarps];  // pass 2: per tile and warp, sum of p (the Z = 0 fallback)
+    float red[kFWarps][8];
+    double bc[4];                   // broadcast of the residual search
+    int ired[kFWarps][2];
+};
+
+// ---------------------------------------------------------------------------
+// PTX helpers (mbarriers, TMA bulk copies); every wait is bounded
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t fs_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void fbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(fs_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(fs_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void fbar_expect(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fs_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool fbar_try(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(fs_u32(bar)), "r"(parity), "r"(1000000u)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long fs_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool fbar_wait(uint64_t* bar, uint32_t parity) {
+    if (fbar_try(bar, parity)) return true;
+    const unsigned long long t0 = fs_ns();
+    while (!fbar_try(bar, parity))
+        if (fs_ns() - t0 > kFWaitNs) return false;
+    return true;
+}
+__device__ __forceinline__ void ftma(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     fs_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(fs_u32(bar))
+                 : "memory");
+}
+// consumer-warp barrier on an mbarrier (one arrival per warp); false once a wait gave up
+struct FSync {
+    uint32_t ph;
+    bool ok;
+};
+__device__ __forceinline__ bool fsync(FreeSmem& sm, FSync& g) {
+    __syncwarp();
+    if (!g.ok) return false;
+    if ((threadIdx.x & 31) == 0) fbar_arrive(&sm.gsync);
+    g.ok = __all_sync(0xFFFFFFFFu, fbar_wait(&sm.gsync, g.ph));
+    g.ph ^= 1u;
+    return g.ok;
+}
+
+// ---------------------------------------------------------------------------
+// arithmetic
+// ---------------------------------------------------------------------------
+template <typename TIn>
+struct FE;
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+template <>
+struct FE<__nv_bfloat16> {
+    static constexpr int VEC = 8;
+    __device__ static void unpack(const uint4& v, float (&x)[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    // NaN-propagating maximum of the vector (packed)
+    __device__ static float vmax(const uint4& v) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+        const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+        const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+        return fmax_nan(__low2float(m), __high2float(m));
+    }
+    __device__ static float at(const uint4& v, int j) {
+        const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+        return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    }
+    __device__ static float load(const __nv_bfloat16* p, int i) {
+        return __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(p)[i] << 16);
+    }
+};
+template <>
+struct FE<float> {
+    static constexpr int VEC = 4;
+    __device__ static void unpack(const uint4& v, float (&x)[4]) {
+        x[0] = __uint_as_float(v.x);
+        x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z);
+        x[3] = __uint_as_float(v.w);
+    }
+    __device__ static float vmax(const uint4& v) {
+        return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                        fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+    __device__ static float at(const uint4& v, int j) {
+        return __uint_as_float(j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w);
+    }
+    __device__ static float load(const float* p, int i) { return p[i]; }
+};
+
+// fp32 sum with Kahan compensation: the value is s - c
+struct KSum {
+    float s, c;
+    __device__ __forceinline__ void add(float x) {
+        const float y = x - c;
+        const float t = s + y;
+        c = (t - s) - y;
+        s = t;
+    }
+};
+// warp sum of compensated values (an exact two-sum at every level), as a float
+__device__ __forceinline__ float warp_ksum(KSum k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, k.s, o);
+        const float c2 = __shfl_xor_sync(0xFFFFFFFFu, k.c, o);
+        const float t = k.s + s2;
+        const float bb = t - k.s;
+        const float e = (k.s - (t - bb)) + (s2 - bb);
+        k.c = (k.c + c2) - e;
+        k.s = t;
+    }
+    return k.s - k.c;
+}
+__device__ __forceinline__ float warp_maxf(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+    return x;
+}
+
+// Normalised probability of a logit: exp2((l - M) * c) * inv (c = log2(e) / T,
+// M the row's maximum logit, inv = 1 / sum); the same expression serves every
+// pass, so the re-read of a tile reproduces the sums of pass 2 exactly.
+// 2^x by the PTX approximate base-2 exponential (relative error about 2^-22),
+// results below the normal range flushed to zero
+__device__ __forceinline__ float fex2(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float prob_f(float l, float M, float c, float inv) { return fex2((l - M) * c) * inv; }
+__device__ __forceinline__ float resid_f(float p, float q) { return fmaxf(p - q, 0.0f); }
+
+// online softmax state of one row for one thread: running maximum logit m and
+// the compensated sum of exp2((l - m) * c)
+struct Online {
+    float m;
+    KSum s;
+    __device__ __forceinline__ void init() {
+        m = -INFINITY;
+        s = KSum{0.0f, 0.0f};
+    }
+    // a whole vector; vm is its NaN-propagating maximum (a NaN row is flagged
+    // by the caller and its sums are not used)
+    template <typename TIn>
+    __device__ __forceinline__ void add_full(const uint4& v, float vm, float c) {
+        if (!(vm > -INFINITY)) return;  // only -inf here (or NaN)
+        if (vm > m) {
+            const float f = m == -INFINITY ? 0.0f : fex2((m - vm) * c);
+            s.s *= f;
+            s.c *= f;
+            m = vm;
+        }
+        float x[FE<TIn>::VEC];
+        FE<TIn>::unpack(v, x);
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < FE<TIn>::VEC; ++j) acc += fex2((x[j] - m) * c);
+        s.add(acc);
+    }
+    // all kFVec vectors of a full tile at once: one rescale, then independent
+    // exponentials summed pairwise; vm is the NaN-propagating maximum of them all
+    template <typename TIn>
+    __device__ __forceinline__ void add_tile(const uint4 (&v)[kFVec], float vm, float c) {
+        if (!(vm > -INFINITY)) return;
+        if (vm > m) {
+            const float f = m == -INFINITY ? 0.0f : fex2((m - vm) * c);
+            s.s *= f;
+            s.c *= f;
+            m = vm;
+        }
+#pragma unroll
+        for (int i = 0; i < kFVec; ++i) {
+            float x[FE<TIn>::VEC];
+            FE<TIn>::unpack(v[i], x);
+#pragma unroll
+            for (int j = 0; j < FE<TIn>::VEC; ++j) x[j] = fex2((x[j] - m) * c);
+#pragma unroll
+            for (int w = FE<TIn>::VEC / 2; w > 0; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) x[j] += x[j + w];
+            s.add(x[0]);
+        }
+    }
+    // the first `valid` elements of a vector (the ragged end of a row)
+    template <typename TIn>
+    __device__ __forceinline__ void add_part(const uint4& v, int valid, float c) {
+        float x[FE<TIn>::VEC];
+        FE<TIn>::unpack(v, x);
+        float vm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < FE<TIn>::VEC; ++j)
+            if (j < valid) vm = fmaxf(vm, x[j]);
+        if (!(vm > -INFINITY)) return;
+        if (vm > m) {
+            const float f = m == -INFINITY ? 0.0f : fex2((m - vm) * c);
+            s.s *= f;
+            s.c *= f;
+            m = vm;
+        }
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < FE<TIn>::VEC; ++j)
+            if (j < valid) acc += fex2((x[j] - m) * c);
+        s.add(acc);
+    }
+};
+
+// maximum and rescaled sum of one row over all consumer threads (each warp
+// rescales to its maximum; warps are combined in fp64 in a fixed order)
+__device__ __forceinline__ void warp_online(const Online& o, float c, float* wm, float* ws) {
+    *wm = warp_maxf(o.m);
+    KSum k = o.s;
+    if (*wm > -INFINITY) {
+        const float f = o.m == -INFINITY ? 0.0f : fex2((o.m - *wm) * c);
+        k.s *= f;
+        k.c *= f;
+    } else {
+        k = KSum{0.0f, 0.0f};
+    }
+    *ws = warp_ksum(k);
+}
+__device__ __forceinline__ void combine_online(const FreeSmem& sm, int col, float c, float* M, double* S) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, sm.red[w][col]);
+    double s = 0.0;
+    if (m > -INFINITY)
+#pragma unroll
+        for (int w = 0; w < kFWarps; ++w)
+            if (sm.red[w][col] > -INFINITY) s += (double)sm.red[w][col + 1] * (double)fex2((sm.red[w][col] - m) * c);
+    *M = m;
+    *S = s;
+}
+
+template <typename TIn, bool TMA>
+__global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
+    using F = FE<TIn>;
+    constexpr int TS = kFSegBytes / (int)sizeof(TIn);  // elements per segment (tile)
+    constexpr int EPT = TS / kFConsumers;              // contiguous elements per thread in a re-read
+    extern __shared__ __align__(128) uint8_t fsm_raw[];
+    FreeSmem& sm = *reinterpret_cast<FreeSmem*>(fsm_raw);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int V = a.V, G = a.G;
+    const int ntiles = (V + TS - 1) / TS;
+
+    if (t == 0) {
+        for (int s = 0; s < kFStages; ++s) {
+            fbar_init(&sm.full[s], 1);
+            fbar_init(&sm.empty[s], kFWarps);
+        }
+        fbar_init(&sm.gsync, kFWarps);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const uint32_t n_units = a.counts[kCntFreeUnits];
+
+    if (warp == kFWarps) {
+        // ------------------------------ producer ------------------------------
+        if (!TMA || lane == 0) {
+            int stage = 0;
+            uint32_t ph = 1;  // fresh empty barriers count as released
+            int issued[kFStages];
+#pragma unroll
+            for (int s = 0; s < kFStages; ++s) issued[s] = -1;
+            bool ok = true;
+            while (ok) {
+                uint32_t w = 0;
+                if (lane == 0) w = atomicAdd(&a.counts[kCntFreeNext], 1u);
+                if (!TMA) w = __shfl_sync(0xFFFFFFFFu, w, 0);
+                if (w >= n_units) break;
+                const uint32_t item = a.free_units[w];
+                const int b = (int)(item >> 8), u = (int)(item & 0xFFu);
+                const bool pair = u < a.seq[b].gamma;
+                const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
+                const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
+                for (int pass = 0; pass < 2 && ok; ++pass)
+                    for (int tile = 0; tile < ntiles && ok; ++tile) {
+                        const int col = tile * TS, n = min(TS, V - col);
+                        if (!fbar_wait(&sm.empty[stage], ph)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) sm.hdr[stage] = make_int4((int)w, pass, tile, n);
+                        if (TMA) {
+                            const uint32_t bytes = (uint32_t)(n * sizeof(TIn));
+                            fbar_expect(&sm.full[stage], pair ? 2u * bytes : bytes);
+                            ftma(sm.buf[stage][0], trow + col, bytes, &sm.full[stage]);
+                            if (pair) ftma(sm.buf[stage][1], drow + col, bytes, &sm.full[stage]);
+                            issued[stage] = (int)(ph ^ 1u);
+                        } else {
+                            TIn* d0 = reinterpret_cast<TIn*>(sm.buf[stage][0]);
+                            TIn* d1 = reinterpret_cast<TIn*>(sm.buf[stage][1]);
+                            for (int i = lane; i < n; i += 32) {
+                                d0[i] = trow[col + i];
+                                if (pair) d1[i] = drow[col + i];
+                            }
+                            __syncwarp();
+                            if (lane == 0) fbar_arrive(&sm.full[stage]);
+                        }
+                        if (++stage == kFStages) {
+                            stage = 0;
+                            ph ^= 1u;
+                        }
+                    }
+            }
+            if (ok && fbar_wait(&sm.empty[stage], ph)) {
+                if (lane == 0) {
+                    sm.hdr[stage] = make_int4(-1, 0, 0, 0);
+                    fbar_arrive(&sm.full[stage]);
+                }
+            } else if (lane == 0) {
+                atomicOr(&a.counts[kCntError], 1u);
+                for (int s = 0; s < kFStages; ++s)  // let every copy already issued land
+                    if (issued[s] >= 0) (void)fbar_wait(&sm.full[s], (uint32_t)issued[s]);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------ consumers ------------------------------
+    int stage = 0;
+    uint32_t ph = 0;
+    FSync g{0u, true};
+    int b = 0, u = 0;
+    bool pair = false, nf = false, dead = false;
+    float c = 1.0f;
+    Online op, oq;
+    float Mp = 0.0f, Mq = 0.0f, invp = 0.0f, invq = 0.0f;
+    double Sp = 0.0, Sq = 0.0;
+    KSum alpha{0.0f, 0.0f};
+    while (true) {
+        if (!__all_sync(0xFFFFFFFFu, fbar_wait(&sm.full[stage], ph))) {
+            g.ok = false;
+            break;
+        }
+        const int4 h = sm.hdr[stage];
+        if (h.x < 0) break;
+        const int w = h.x, pass = h.y, tile = h.z, n = h.w;
+        const int col = tile * TS;
+        if (pass == 0 && tile == 0) {  // a new unit
+            const uint32_t item = a.free_units[w];
+            b = (int)(item >> 8);
+            u = (int)(item & 0xFFu);
+            const SeqInfo si = a.seq[b];
+            pair = u < si.gamma;
+            c = 1.4426950408889634f / si.T;
+            op.init();
+            oq.init();
+            nf = false;
+            alpha = KSum{0.0f, 0.0f};
+        }
+        uint4 vp[kFVec], vq[kFVec];
+        const uint4* sp4 = reinterpret_cast<const uint4*>(sm.buf[stage][0]);
+        const uint4* sq4 = reinterpret_cast<const uint4*>(sm.buf[stage][1]);
+#pragma unroll
+        for (int i = 0; i < kFVec; ++i) {
+            vp[i] = sp4[i * kFConsumers + t];
+            vq[i] = pair ? sq4[i * kFConsumers + t] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+        if (lane == 0) fbar_arrive(&sm.empty[stage]);
+        if (++stage == kFStages) {
+            stage = 0;
+            ph ^= 1u;
+        }
+
+        if (pass == 0) {
+            // ---- pass 1: online maximum and sum; non-finite logits flag the sequence
+            if (n == TS) {  // a full tile: every vector of this thread is whole
+                float mp = -INFINITY, mq = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kFVec; ++i) {
+                    mp = fmax_nan(mp, F::vmax(vp[i]));
+                    if (pair) mq = fmax_nan(mq, F::vmax(vq[i]));
+                }
+                nf |= isnan(mp) || mp == INFINITY || isnan(mq) || mq == INFINITY;
+                op.add_tile<TIn>(vp, mp, c);
+                if (pair) oq.add_tile<TIn>(vq, mq, c);
+            } else {
+#pragma unroll
+            for (int i = 0; i < kFVec; ++i) {
+                const int e0 = (i * kFConsumers + t) * F::VEC;
+                const int valid = min(F::VEC, n - e0);
+                if (valid <= 0) continue;
+                if (valid == F::VEC) {
+                    const float mp = F::vmax(vp[i]);
+                    nf |= isnan(mp) || mp == INFINITY;
+                    op.add_full<TIn>(vp[i], mp, c);
+                    if (pair) {
+                        const float mq = F::vmax(vq[i]);
+                        nf |= isnan(mq) || mq == INFINITY;
+                        oq.add_full<TIn>(vq[i], mq, c);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < F::VEC; ++j)
+                        if (j < valid) {
+                            const float x = F::at(vp[i], j);
+                            nf |= isnan(x) || x == INFINITY;
+                            if (pair) {
+                                const float y = F::at(vq[i], j);
+                                nf |= isnan(y) || y == INFINITY;
+                            }
+                        }
+                    op.add_part<TIn>(vp[i], valid, c);
+                    if (pair) oq.add_part<TIn>(vq[i], valid, c);
+                }
+            }
+            }
+            if (tile == ntiles - 1) {
+                float wm, ws, wm2, ws2;
+                warp_online(op, c, &wm, &ws);
+                warp_online(oq, c, &wm2, &ws2);
+                const bool wnf = __any_sync(0xFFFFFFFFu, nf);
+                if (lane == 0) {
+                    sm.red[warp][0] = wm;
+                    sm.red[warp][1] = ws;
+                    sm.red[warp][2] = wm2;
+                    sm.red[warp][3] = ws2;
+                    sm.red[warp][4] = wnf ? 1.0f : 0.0f;
+                }
+                if (!fsync(sm, g)) break;
+                combine_online(sm, 0, c, &Mp, &Sp);
+                combine_online(sm, 2, c, &Mq, &Sq);
+                bool anynf = false;
+#pragma unroll
+                for (int w2 = 0; w2 < kFWarps; ++w2) anynf |= sm.red[w2][4] != 0.0f;
+                // a row with a NaN or +inf logit, or without any finite one
+                dead = anynf || !(Mp > -INFINITY) || (pair && !(Mq > -INFINITY));
+                invp = dead ? 0.0f : (float)(1.0 / Sp);
+                invq = (dead || !pair) ? 0.0f : (float)(1.0 / Sq);
+                if (!fsync(sm, g)) break;  // red is reused below
+            }
+            continue;
+        }
+
+        // ---- pass 2: alpha, residual weights, per-tile sums (and the debug outputs)
+        float tr = 0.0f, tp = 0.0f;
+        if (!dead) {
+#pragma unroll
+            for (int i = 0; i < kFVec; ++i) {
+                const int e0 = (i * kFConsumers + t) * F::VEC;
+                const int valid = min(F::VEC, n - e0);
+                if (valid <= 0) continue;
+                float xp[F::VEC], xq[F::VEC];
+                F::unpack(vp[i], xp);
+                F::unpack(vq[i], xq);
+                float am = 0.0f;
+                if (pair) {
+                    float ma[F::VEC], ra[F::VEC], pa[F::VEC];
+#pragma unroll
+                    for (int j = 0; j < F::VEC; ++j) {
+                        const float p = j < valid ? prob_f(xp[j], Mp, c, invp) : 0.0f;
+                        const float q = j < valid ? prob_f(xq[j], Mq, c, invq) : 0.0f;
+                        ma[j] = fminf(p, q);
+                        ra[j] = resid_f(p, q);
+                        pa[j] = p;
+                    }
+#pragma unroll
+                    for (int w2 = F::VEC / 2; w2 > 0; w2 >>= 1)
+#pragma unroll
+                        for (int j = 0; j < w2; ++j) {
+                            ma[j] += ma[j + w2];
+                            ra[j] += ra[j + w2];
+                            pa[j] += pa[j + w2];
+                        }
+                    am = ma[0];
+                    tr += ra[0];
+                    tp += pa[0];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < F::VEC; ++j)
+                        if (j < valid) tp += prob_f(xp[j], Mp, c, invp);
+                    tr = tp;
+                }
+                alpha.add(am);
+                if (a.p_out || a.q_out) {  // debug outputs
+#pragma unroll
+                    for (int j = 0; j < F::VEC; ++j)
+                        if (j < valid) {
+                            if (a.p_out)
+                                a.p_out[((size_t)b * (G + 1) + u) * V + col + e0 + j] = prob_f(xp[j], Mp, c, invp);
+                            if (a.q_out && pair)
+                                a.q_out[((size_t)b * G + u) * V + col + e0 + j] = prob_f(xq[j], Mq, c, invq);
+                        }
+                }
+            }
+        }
+        {
+            const float wtr = warp_ksum(KSum{tr, 0.0f}), wtp = warp_ksum(KSum{tp, 0.0f});
+            if (lane == 0) {
+                sm.wr[tile][warp] = wtr;
+                sm.wp[tile][warp] = wtp;
+            }
+        }
+        if (tile != ntiles - 1) continue;
+
+        // ---- end of the unit ----
+        {
+            const float wa = warp_ksum(alpha);
+            if (lane == 0) sm.red[warp][5] = wa;
+        }
+        if (!fsync(sm, g)) break;  // every tile sum is in
+        const double ur = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 1u);
+        if (warp == 0 && !dead) {
+            // total residual mass; fall back to p when it is zero (p <= q everywhere)
+            double Z = 0.0, Zp = 0.0;
+            for (int tl = lane; tl < ntiles; tl += 32) {
+                double zr = 0.0, zp = 0.0;
+#pragma unroll
+                for (int w2 = 0; w2 < kFWarps; ++w2) {
+                    zr += (double)sm.wr[tl][w2];
+                    zp += (double)sm.wp[tl][w2];
+                }
+                Z += zr;
+                Zp += zp;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                Z += __shfl_xor_sync(0xFFFFFFFFu, Z, o);
+                Zp += __shfl_xor_sync(0xFFFFFFFFu, Zp, o);
+            }
+            const bool use_p = !(Z > 0.0);
+            const double Zt = use_p ? Zp : Z;
+            const double v = ur * Zt;
+            // the tile whose running sum passes v (else the last tile with weight)
+            int found = -1, lastpos = -1;
+            double carry = 0.0, before = 0.0;
+            for (int c0 = 0; c0 < ntiles && found < 0; c0 += 32) {
+                const int tl = c0 + lane;
+                double x = 0.0;
+                if (tl < ntiles)
+#pragma unroll
+                    for (int w2 = 0; w2 < kFWarps; ++w2) x += (double)(use_p ? sm.wp[tl][w2] : sm.wr[tl][w2]);
+                const double own = x;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                    if (lane >= o) x += y;
+                }
+                const unsigned pos = __ballot_sync(0xFFFFFFFFu, tl < ntiles && own > 0.0);
+                if (pos) {
+                    lastpos = c0 + 31 - __clz(pos);
+                    before = carry + __shfl_sync(0xFFFFFFFFu, x - own, 31 - __clz(pos));
+                }
+                const unsigned hit = __ballot_sync(0xFFFFFFFFu, tl < ntiles && own > 0.0 && carry + x > v);
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    found = c0 + l;
+                    before = carry + __shfl_sync(0xFFFFFFFFu, x - own, l);
+                }
+                carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+            }
+            if (lane == 0) {
+                sm.bc[0] = (double)(found >= 0 ? found : lastpos);
+                sm.bc[1] = before;
+                sm.bc[2] = v;
+                sm.bc[3] = use_p ? 1.0 : 0.0;
+            }
+        }
+        if (!fsync(sm, g)) break;
+        int token = -1;
+        if (!dead) {
+            const int tsel = (int)sm.bc[0];
+            const double before = sm.bc[1], v = sm.bc[2];
+            const bool use_p = sm.bc[3] != 0.0;
+            // re-read the tile: thread t takes EPT contiguous elements
+            const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
+            const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
+            const int e0 = (tsel < 0 ? 0 : tsel) * TS + t * EPT;
+            const int e1 = min(V, e0 + EPT);
+            float rv[EPT];
+            float own = 0.0f;
+            int last = -1;
+#pragma unroll
+            for (int j = 0; j < EPT; ++j) {
+                rv[j] = 0.0f;
+                if (tsel >= 0 && e0 + j < e1) {
+                    const float p = prob_f(F::load(trow, e0 + j), Mp, c, invp);
+                    const float q = pair ? prob_f(F::load(drow, e0 + j), Mq, c, invq) : 0.0f;
+                    rv[j] = (pair && !use_p) ? resid_f(p, q) : p;
+                    own += rv[j];
+                    if (rv[j] > 0.0f) last = e0 + j;
+                }
+            }
+            // exclusive prefix of the thread sums, in fp64
+            double x = (double)own;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            double* wtot = reinterpret_cast<double*>(sm.wr[0]);  // tile sums are no longer needed
+            __syncwarp();
+            if (lane == 31) wtot[warp] = x;
+            if (!fsync(sm, g)) break;
+            double pre = before;
+            for (int w2 = 0; w2 < warp; ++w2) pre += wtot[w2];
+            pre += x - (double)own;
+            int hit = INT_MAX;
+            if (own > 0.0f && pre + (double)own > v) {
+                double cum = pre;
+#pragma unroll
+                for (int j = 0; j < EPT; ++j)
+                    if (hit == INT_MAX && rv[j] > 0.0f) {
+                        cum += (double)rv[j];
+                        if (cum > v) hit = e0 + j;
+                    }
+            }
+            // the first element passing v over the tile, else its last one with weight
+            int wh = hit, wl = last;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                wh = min(wh, __shfl_xor_sync(0xFFFFFFFFu, wh, o));
+                wl = max(wl, __shfl_xor_sync(0xFFFFFFFFu, wl, o));
+            }
+            if (lane == 0) {
+                sm.ired[warp][0] = wh;
+                sm.ired[warp][1] = wl;
+            }
+            if (!fsync(sm, g)) break;
+            int bh = INT_MAX, bl = -1;
+#pragma unroll
+            for (int w2 = 0; w2 < kFWarps; ++w2) {
+                bh = min(bh, sm.ired[w2][0]);
+                bl = max(bl, sm.ired[w2][1]);
+            }
+            token = bh != INT_MAX ? bh : bl;
+        }
+        if (warp == 0) {
+            if (dead) {
+                if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+            } else if (lane == 0) {
+                int accept = 0;
+                if (pair) {
+                    // acceptance test u * q(x) < p(x) in fp64 from the logits of x
+                    const int xt = a.draft_tokens[(size_t)b * G + u];
+                    const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
+                    const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
+                    const double T = (double)a.seq[b].T;
+                    const double px = exp(((double)F::load(trow, xt) - (double)Mp) / T) / Sp;
+                    const double qx = exp(((double)F::load(drow, xt) - (double)Mq) / T) / Sq;
+                    const double ua = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 0u);
+                    accept = (ua * qx < px) ? 1 : 0;
+                    double al = 0.0;
+#pragma unroll
+                    for (int w2 = 0; w2 < kFWarps; ++w2) al += (double)sm.red[w2][5];
+                    a.alpha[(size_t)b * G + u] = (float)al;
+                    a.unit_acc[(size_t)b * G + u] = accept;
+                    if (a.pos_accept) a.pos_accept[(size_t)b * G + u] = accept;
+                }
+                a.unit_tok[(size_t)b * (G + 1) + u] = token;
+                if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + u] = token;
+            }
+            unit_finished_warp(a, b, lane);
+        }
+        // the next unit may reuse the shared sums only after warp 0 has read them
+        if (!fsync(sm, g)) break;
+    }
+    if (!g.ok && lane == 0) atomicOr(&a.counts[kCntError], 1u);
+}
+
+template <typename TIn, bool TMA>
+cudaError_t launch_free_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) {
+    auto k = free_kernel<TIn, TMA>;
+    const int smem = (int)sizeof(FreeSmem);
+    static const bool attr_ok = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+                                cudaSuccess;
+    if (!attr_ok) return cudaErrorInvalidValue;
+    static const int occ = [&] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kFThreads, smem) != cudaSuccess) n = 1;
+        return n > 0 ? n : 1;
+    }();
+    long long grid = (long long)occ * sms;
+    const long long units = (long long)a.B * (a.G + 1);
+    if (grid > units) grid = units;
+    if (grid < 1) grid = 1;
+    if (ev && ev[0]) cudaEventRecord((cudaEvent_t)ev[0], s);
+    k<<<(unsigned)grid, kFThreads, smem, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (ev && ev[1]) cudaEventRecord((cudaEvent_t)ev[1], s);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_free_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, void* const ev[2]) {
+    if (dtype == SV_BF16)
+        return vector ? launch_free_t<__nv_bfloat16, true>(a, sms, s, ev) : launch_free_t<__nv_bfloat16, false>(a, sms, s, ev);
+    return vector ? launch_free_t<float, true>(a, sms, s, ev) : launch_free_t<float, false>(a, sms, s, ev);
+}
+
+}  // namespace sv

@@ -41,9 +41,19 @@ constexpr int kSortCap = 2048;  // candidates per row sorted in shared memory by
 constexpr int kDenseThreads = 256;
 
 // counters at the head of the workspace list area
-enum : int { kCntStreamRows = 0, kCntDenseUnits = 1, kCntStreamUnits = 2, kCntPieceNext = 3, kCntError = 4 };
+enum : int {
+    kCntStreamRows = 0,
+    kCntDenseUnits = 1,
+    kCntStreamUnits = 2,
+    kCntPieceNext = 3,
+    kCntError = 4,
+    kCntFreeUnits = 5,
+    kCntFreeNext = 6
+};
 
-enum : uint32_t { kModeErr = 0, kModeStream = 1, kModeDense = 2 };
+// streaming top-k path; whole-row cluster path (top-p, large top-k); whole-row
+// path of unfiltered rows (no top-k, no top-p)
+enum : uint32_t { kModeErr = 0, kModeStream = 1, kModeDense = 2, kModeFree = 3 };
 
 // per-sequence plan (32 bytes)
 struct SeqInfo {
@@ -88,14 +98,15 @@ struct Args {
     uint32_t* stream_rows;
     uint32_t* dense_units;
     uint32_t* stream_units;
+    uint32_t* free_units;
     uint32_t* counts;         // kCnt* above
     unsigned long long* cand; // [stream rows * ppr * kListCap] (key << 32 | ~id), unsorted
     uint32_t* cand_cnt;       // [stream rows * ppr]
 };
 
 struct WsLayout {
-    size_t seq, seq_done, seq_status, unit_done, unit_acc, unit_tok, stream_rows, dense_units, stream_units, counts,
-        cand, cand_cnt, total;
+    size_t seq, seq_done, seq_status, unit_done, unit_acc, unit_tok, stream_rows, dense_units, stream_units, free_units,
+        counts, cand, cand_cnt, total;
     int ppr;
 };
 
@@ -124,6 +135,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int G, int V, int dtype) {
     L.stream_rows = o; o = align_up(o + 4 * rows, 256);
     L.dense_units = o; o = align_up(o + 4 * units, 256);
     L.stream_units = o; o = align_up(o + 4 * units, 256);
+    L.free_units = o;  o = align_up(o + 4 * units, 256);
     L.counts = o;      o = align_up(o + 64, 256);
     L.cand_cnt = o;    o = align_up(o + 4 * rows * L.ppr, 256);
     L.cand = o;        o = align_up(o + 8 * rows * L.ppr * kListCap, 256);
@@ -208,6 +220,7 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // host launchers, one per kernel translation unit
 cudaError_t launch_stream_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, void* const ev[2]);
+cudaError_t launch_free_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, void* const ev[2]);
 cudaError_t launch_dense_f32(bool vector, const Args& a, int sms, cudaStream_t s);
 cudaError_t launch_dense_bf16(bool vector, const Args& a, int sms, cudaStream_t s);
 

@@ -1036,22 +1036,79 @@ constexpr int kSelBuf = 512;      // a warp's scratch for a row's candidates
 static_assert(kSelBuf >= kStreamMaxK + 32, "the scratch holds a top-k plus one load step");
 
 struct CombWarp {
-    unsigned long long buf[kSelBuf];        // candidates of the row being selected
-    unsigned long long top[2][kStreamMaxK]; // kept entries of the target / draft row, (key desc, id asc)
-    double prob[2][kStreamMaxK];
-    double resid[kStreamMaxK];
-    int rid[kStreamMaxK];
+    unsigned long long buf[kSelBuf];          // candidates of the row being selected
+    unsigned long long top[2][kStreamMaxK];   // kept entries of the target / draft row, (key desc, id asc)
+    double prob[2][kStreamMaxK];              // their normalised probabilities, same order
+    unsigned long long byid[2][kStreamMaxK];  // (id << 32 | position in top), ascending
 };
+
+// Bitonic sort across the warp of 32 * P 64-bit keys held P per lane (element
+// m * 32 + lane in x[m]), descending or ascending.
+template <int P>
+__device__ __forceinline__ void warp_bitonic(unsigned long long (&x)[P], int lane, bool descending) {
+    constexpr int N = 32 * P;
+#pragma unroll
+    for (int k2 = 2; k2 <= N; k2 <<= 1) {
+#pragma unroll
+        for (int j = k2 >> 1; j > 0; j >>= 1) {
+            if (j >= 32) {  // partners in the same lane
+#pragma unroll
+                for (int m = 0; m < P; ++m) {
+                    const int mp = m ^ (j >> 5);
+                    if (mp > m) {
+                        const bool lower_max = (((m * 32 + lane) & k2) == 0) == descending;
+                        const unsigned long long lo = x[m], hi = x[mp];
+                        const bool sw = lower_max ? (lo < hi) : (lo > hi);
+                        x[m] = sw ? hi : lo;
+                        x[mp] = sw ? lo : hi;
+                    }
+                }
+            } else {  // partners in lane ^ j
+#pragma unroll
+                for (int m = 0; m < P; ++m) {
+                    const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, x[m], j);
+                    const bool lower = (lane & j) == 0;
+                    const bool lower_max = (((m * 32 + lane) & k2) == 0) == descending;
+                    const bool take_max = lower == lower_max;
+                    x[m] = take_max ? (x[m] > y ? x[m] : y) : (x[m] < y ? x[m] : y);
+                }
+            }
+        }
+    }
+}
+
+// Sort n <= 32 * P entries of src (pad: `pad`) into dst across the warp.
+template <int P>
+__device__ __forceinline__ void warp_sort_into(const unsigned long long* src, int n, unsigned long long* dst,
+                                               bool descending, unsigned long long pad, int lane) {
+    unsigned long long x[P];
+#pragma unroll
+    for (int m = 0; m < P; ++m) x[m] = m * 32 + lane < n ? src[m * 32 + lane] : pad;
+    warp_bitonic<P>(x, lane, descending);
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < P; ++m)
+        if (m * 32 + lane < n) dst[m * 32 + lane] = x[m];
+    __syncwarp();
+}
+__device__ __forceinline__ void warp_sort(const unsigned long long* src, int n, unsigned long long* dst,
+                                          bool descending, unsigned long long pad, int lane) {
+    if (n <= 32)
+        warp_sort_into<1>(src, n, dst, descending, pad, lane);
+    else if (n <= 64)
+        warp_sort_into<2>(src, n, dst, descending, pad, lane);
+    else if (n <= 128)
+        warp_sort_into<4>(src, n, dst, descending, pad, lane);
+    else
+        warp_sort_into<8>(src, n, dst, descending, pad, lane);
+}
 
 // Keep the exact top-k (key descending, then id ascending) of buf[0..m) in
 // buf[0..k), unordered; returns the count.  The k-th key is found bit by bit
 // below the common prefix of the smallest and largest key (warp reductions),
-// ties at it by id (ids < 2^18).
-template <int KB>
-__device__ int warp_keep_topk(unsigned long long* buf, int m, int k, int lane) {
-    __syncwarp();
-    if (m <= k) return m;
-    constexpr int M = kSelBuf / 32;
+// ties at it by id (ids < 2^18).  M slots per lane cover m.
+template <int KB, int M>
+__device__ int warp_keep_topk_m(unsigned long long* buf, int m, int k, int lane) {
     const int used = (m + 31) >> 5;
     unsigned long long e[M];
     uint32_t key[M];
@@ -1117,6 +1174,15 @@ __device__ int warp_keep_topk(unsigned long long* buf, int m, int k, int lane) {
     __syncwarp();
     return base;
 }
+template <int KB>
+__device__ int warp_keep_topk(unsigned long long* buf, int m, int k, int lane) {
+    __syncwarp();
+    if (m <= k) return m;
+    if (m <= 64) return warp_keep_topk_m<KB, 2>(buf, m, k, lane);
+    if (m <= 128) return warp_keep_topk_m<KB, 4>(buf, m, k, lane);
+    if (m <= 256) return warp_keep_topk_m<KB, 8>(buf, m, k, lane);
+    return warp_keep_topk_m<KB, kSelBuf / 32>(buf, m, k, lane);
+}
 
 // Exact top-k of a row, sorted by (logit desc, id asc), from its pieces' candidate
 // lists (each a superset of that piece's top-k); returns how many were found (k normally).
@@ -1138,15 +1204,44 @@ __device__ int row_topk(const Args& a, uint32_t row_slot, int k, CombWarp& sw, u
         }
     }
     kept = warp_keep_topk<KB>(sw.buf, kept, k, lane);
-    // order by composite, descending: an entry's rank is the number of larger ones
-    for (int i = lane; i < kept; i += 32) {
-        const unsigned long long e = sw.buf[i];
-        int r = 0;
-        for (int j = 0; j < kept; ++j) r += sw.buf[j] > e;
-        top[r] = e;
-    }
-    __syncwarp();
+    warp_sort(sw.buf, kept, top, true, 0ull, lane);
     return kept;
+}
+
+// (id << 32 | position) of the kept entries, ascending by id
+__device__ __forceinline__ void index_by_id(const unsigned long long* top, int n, CombWarp& sw,
+                                            unsigned long long* byid, int lane) {
+    for (int j = lane; j < n; j += 32) sw.buf[j] = ((unsigned long long)(uint32_t)comp_id(top[j]) << 32) | (uint32_t)j;
+    __syncwarp();
+    warp_sort(sw.buf, n, byid, false, ~0ull, lane);
+}
+
+// probability of token x in a kept list indexed by id (0 if not kept)
+__device__ __forceinline__ double prob_of(const unsigned long long* byid, const double* prob, int n, int x) {
+    int lo = 0, hi = n - 1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        const int id = (int)(byid[mid] >> 32);
+        if (id == x) return prob[(uint32_t)byid[mid]];
+        if (id < x)
+            lo = mid + 1;
+        else
+            hi = mid - 1;
+    }
+    return 0.0;
+}
+
+// 2^x for x <= 0, with the exponent split (Cody-Waite style) into an integer n
+// and a fraction f in [-1/2, 1/2] in fp64: only f goes through the fp32 exp2,
+// and 2^n is applied exactly, so the result keeps the fp32 exp2's relative
+// accuracy whatever the size of x, at the cost of a few fp64 operations
+// (instead of a full fp64 exponential).  Below 2^-1022 the result is 0.
+__device__ __forceinline__ double exp2_split(double x) {
+    const double n = rint(x);
+    if (n < -1022.0) return 0.0;
+    const double f = x - n;
+    const double pw = __longlong_as_double((long long)(n + 1023.0) << 52);
+    return (double)exp2f((float)f) * pw;
 }
 
 // fp64 normalisation of one sorted kept list by one warp: softmax over the kept
@@ -1161,15 +1256,16 @@ __device__ void normalise_kept(const unsigned long long* top, int k, float Tf, f
         return;
     }
     const double vmax = Elem<TIn>::key_value(comp_key(top[0]));
+    const double c2 = 1.4426950408889634 / T;  // log2(e) / T
     double s = 0.0;
     for (int j = lane; j < k; j += 32) {
-        const double v = Elem<TIn>::key_value(comp_key(top[j]));
-        const double w = exp((v - vmax) / T);
+        const double w = exp2_split((Elem<TIn>::key_value(comp_key(top[j])) - vmax) * c2);
         prob[j] = w;
         s += w;
     }
     s = warp_sum(s);
-    for (int j = lane; j < k; j += 32) prob[j] /= s;
+    const double inv = 1.0 / s;
+    for (int j = lane; j < k; j += 32) prob[j] *= inv;
     __syncwarp();
     if (P < 1.0) {  // shortest prefix (prob desc, id asc) whose mass reaches P, crossing token kept
         double carry = 0.0;
@@ -1196,7 +1292,8 @@ __device__ void normalise_kept(const unsigned long long* top, int k, float Tf, f
         }
         s2 = warp_sum(s2);
         __syncwarp();
-        for (int j = lane; j < keep; j += 32) prob[j] /= s2;
+        const double inv2 = 1.0 / s2;
+        for (int j = lane; j < keep; j += 32) prob[j] *= inv2;
     }
     __syncwarp();
 }
@@ -1210,122 +1307,98 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
     const int kt = row_topk<Elem<TIn>::KB>(a, slot_t, si.k, sm, sm.top[0], lane);  // exact top-k, ties to the lower id
     const int kd = pair ? row_topk<Elem<TIn>::KB>(a, slot_d, si.k, sm, sm.top[1], lane) : 0;
 
-    {
-        // a row without a finite logit (or with non-finite ones, already flagged)
-        const uint32_t ninf_key = Elem<TIn>::key(Elem<TIn>::kNegInfBits);
-        const bool dead = kt < 1 || comp_key(sm.top[0][0]) <= ninf_key ||
-                          (pair && (kd < 1 || comp_key(sm.top[1][0]) <= ninf_key));
-        if (dead) {
-            if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
-        } else {
-            normalise_kept<TIn>(sm.top[0], kt, si.T, si.P, sm.prob[0]);
-            if (pair) normalise_kept<TIn>(sm.top[1], kd, si.T, si.P, sm.prob[1]);
+    // a row without a finite logit (or with non-finite ones, already flagged)
+    const uint32_t ninf_key = Elem<TIn>::key(Elem<TIn>::kNegInfBits);
+    const bool dead = kt < 1 || comp_key(sm.top[0][0]) <= ninf_key ||
+                      (pair && (kd < 1 || comp_key(sm.top[1][0]) <= ninf_key));
+    if (dead) {
+        if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+        unit_finished_warp(a, b, lane);
+        return;
+    }
+    normalise_kept<TIn>(sm.top[0], kt, si.T, si.P, sm.prob[0]);
+    if (pair) normalise_kept<TIn>(sm.top[1], kd, si.T, si.P, sm.prob[1]);
+    index_by_id(sm.top[0], kt, sm, sm.byid[0], lane);
+    if (pair) index_by_id(sm.top[1], kd, sm, sm.byid[1], lane);
 
-            // alpha_i = sum_x min(p, q) over the ids kept in both rows; residual weights
-            double alpha = 0.0;
-            for (int j = lane; j < kt; j += 32) {
-                const int id = comp_id(sm.top[0][j]);
-                double q = 0.0;
-                if (pair)
-                    for (int e = 0; e < kd; ++e)
-                        if (comp_id(sm.top[1][e]) == id) q = sm.prob[1][e];
-                const double p = sm.prob[0][j];
-                alpha += fmin(p, q);
-                sm.resid[j] = pair ? fmax(p - q, 0.0) : p;  // bonus: q_{gamma+1} := 0
-            }
-            alpha = warp_sum(alpha);
-            __syncwarp();
+    // acceptance test u * q(x) < p(x)
+    int accept = 0;
+    if (pair) {
+        const int x = a.draft_tokens[(size_t)b * G + unit];
+        const double px = prob_of(sm.byid[0], sm.prob[0], kt, x);
+        const double qx = prob_of(sm.byid[1], sm.prob[1], kd, x);
+        const double u = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 0u);
+        accept = (u * qx < px) ? 1 : 0;
+    }
 
-            // acceptance test u * q(x) < p(x)
-            int accept = 0;
-            if (pair) {
-                const int x = a.draft_tokens[(size_t)b * G + unit];
-                double px = 0.0, qx = 0.0;
-                for (int j = lane; j < kt; j += 32)
-                    if (comp_id(sm.top[0][j]) == x) px = sm.prob[0][j];
-                for (int j = lane; j < kd; j += 32)
-                    if (comp_id(sm.top[1][j]) == x) qx = sm.prob[1][j];
-                px = warp_sum(px);
-                qx = warp_sum(qx);
-                const double u = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 0u);
-                accept = (u * qx < px) ? 1 : 0;
-            }
-
-            // residual (or bonus) draw: inverse CDF in ascending token id
-            double Z = 0.0;
-            for (int j = lane; j < kt; j += 32) Z += sm.resid[j];
-            Z = warp_sum(Z);
-            if (!(Z > 0.0)) {  // p <= q everywhere: fall back to p
-                Z = 0.0;
-                for (int j = lane; j < kt; j += 32) {
-                    sm.resid[j] = sm.prob[0][j];
-                    Z += sm.resid[j];
-                }
-                Z = warp_sum(Z);
-            }
-            __syncwarp();
-            double rr[kStreamMaxK / 32];
-            int rank[kStreamMaxK / 32];
+    // alpha_i = sum_x min(p, q) and the residual weights, in ascending token id
+    // over the target's kept ids (an id kept only by the draft has p = 0)
+    double rr[kStreamMaxK / 32];
+    double alpha = 0.0, Z = 0.0, Zp = 0.0;
 #pragma unroll
-            for (int m = 0; m < kStreamMaxK / 32; ++m) {
-                const int j = lane + 32 * m;
-                rank[m] = -1;
-                rr[m] = 0.0;
-                if (j < kt) {
-                    const int id = comp_id(sm.top[0][j]);
-                    int r = 0;
-                    for (int e = 0; e < kt; ++e) r += comp_id(sm.top[0][e]) < id;
-                    rank[m] = r;
-                    rr[m] = sm.resid[j];
-                }
-            }
-            __syncwarp();
-#pragma unroll
-            for (int m = 0; m < kStreamMaxK / 32; ++m) {
-                const int j = lane + 32 * m;
-                if (j < kt) {
-                    sm.resid[rank[m]] = rr[m];
-                    sm.rid[rank[m]] = comp_id(sm.top[0][j]);
-                }
-            }
-            __syncwarp();
-            const double v = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 1u) * Z;
-            int token = -1, last_pos = -1;
-            double carry = 0.0;
-            for (int c0 = 0; c0 < kt && token < 0; c0 += 32) {
-                const int j = c0 + lane;
-                const double r = (j < kt) ? sm.resid[j] : 0.0;
-                double x = r;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-                    if (lane >= o) x += y;
-                }
-                const unsigned pos = __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0);
-                if (pos) last_pos = c0 + 31 - __clz(pos);
-                const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0 && carry + x > v);
-                if (hit) token = sm.rid[c0 + __ffs(hit) - 1];
-                carry += __shfl_sync(0xFFFFFFFFu, x, 31);
-            }
-            if (token < 0 && last_pos >= 0) token = sm.rid[last_pos];
-
-            if (lane == 0) {
-                if (pair) {
-                    a.alpha[(size_t)b * G + unit] = (float)alpha;
-                    a.unit_acc[(size_t)b * G + unit] = accept;
-                    if (a.pos_accept) a.pos_accept[(size_t)b * G + unit] = accept;
-                }
-                a.unit_tok[(size_t)b * (G + 1) + unit] = token;
-                if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + unit] = token;
-            }
-            if (a.p_out)
-                for (int j = lane; j < kt; j += 32)
-                    a.p_out[((size_t)b * (G + 1) + unit) * a.V + comp_id(sm.top[0][j])] = (float)sm.prob[0][j];
-            if (a.q_out && pair)
-                for (int j = lane; j < kd; j += 32)
-                    a.q_out[((size_t)b * G + unit) * a.V + comp_id(sm.top[1][j])] = (float)sm.prob[1][j];
+    for (int m = 0; m < kStreamMaxK / 32; ++m) {
+        const int j = lane + 32 * m;
+        rr[m] = 0.0;
+        if (j < kt) {
+            const unsigned long long e = sm.byid[0][j];
+            const double p = sm.prob[0][(uint32_t)e];
+            const double q = pair ? prob_of(sm.byid[1], sm.prob[1], kd, (int)(e >> 32)) : 0.0;
+            alpha += fmin(p, q);
+            rr[m] = fmax(p - q, 0.0);  // bonus: q_{gamma+1} := 0
+            Z += rr[m];
+            Zp += p;
         }
     }
+    alpha = warp_sum(alpha);
+    Z = warp_sum(Z);
+    const bool use_p = !(Z > 0.0);  // p <= q everywhere: fall back to p
+    if (use_p) {
+        Z = warp_sum(Zp);
+#pragma unroll
+        for (int m = 0; m < kStreamMaxK / 32; ++m) {
+            const int j = lane + 32 * m;
+            rr[m] = j < kt ? sm.prob[0][(uint32_t)sm.byid[0][j]] : 0.0;
+        }
+    }
+    // inverse CDF: the first id whose running sum passes v
+    const double v = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 1u) * Z;
+    int token = -1, last_pos = -1;
+    double carry = 0.0;
+#pragma unroll
+    for (int m = 0; m < kStreamMaxK / 32; ++m) {
+        const int c0 = 32 * m;
+        if (c0 >= kt || token >= 0) break;
+        const int j = c0 + lane;
+        const double r = rr[m];
+        double x = r;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+        }
+        const unsigned pos = __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0);
+        if (pos) last_pos = c0 + 31 - __clz(pos);
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0 && carry + x > v);
+        if (hit) token = (int)(sm.byid[0][c0 + __ffs(hit) - 1] >> 32);
+        carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    if (token < 0 && last_pos >= 0) token = (int)(sm.byid[0][last_pos] >> 32);
+
+    if (lane == 0) {
+        if (pair) {
+            a.alpha[(size_t)b * G + unit] = (float)alpha;
+            a.unit_acc[(size_t)b * G + unit] = accept;
+            if (a.pos_accept) a.pos_accept[(size_t)b * G + unit] = accept;
+        }
+        a.unit_tok[(size_t)b * (G + 1) + unit] = token;
+        if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + unit] = token;
+    }
+    if (a.p_out)
+        for (int j = lane; j < kt; j += 32)
+            a.p_out[((size_t)b * (G + 1) + unit) * a.V + comp_id(sm.top[0][j])] = (float)sm.prob[0][j];
+    if (a.q_out && pair)
+        for (int j = lane; j < kd; j += 32)
+            a.q_out[((size_t)b * G + unit) * a.V + comp_id(sm.top[1][j])] = (float)sm.prob[1][j];
     unit_finished_warp(a, b, lane);
 }
 
