@@ -48,6 +48,8 @@ struct FreeSmem {
     float wp[kFMaxTiles][kFWarps];  // pass 2: per tile and warp, sum of p (the Z = 0 fallback)
     float red[kFWarps][8];
     double bc[4];                   // broadcast of the residual search
+    double st[4];                   // broadcast of the row statistics: Mp, Sp, Mq, Sq
+    int st_dead;
     int ired[kFWarps][2];
 };
 
@@ -495,16 +497,29 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                     sm.red[warp][4] = wnf ? 1.0f : 0.0f;
                 }
                 if (!fsync(sm, g)) break;
-                combine_online(sm, 0, c, &Mp, &Sp);
-                combine_online(sm, 2, c, &Mq, &Sq);
-                bool anynf = false;
+                if (t == 0) {  // one thread combines the warps (fp64) for everyone
+                    float m1, m2;
+                    double s1, s2;
+                    combine_online(sm, 0, c, &m1, &s1);
+                    combine_online(sm, 2, c, &m2, &s2);
+                    bool anynf = false;
 #pragma unroll
-                for (int w2 = 0; w2 < kFWarps; ++w2) anynf |= sm.red[w2][4] != 0.0f;
-                // a row with a NaN or +inf logit, or without any finite one
-                dead = anynf || !(Mp > -INFINITY) || (pair && !(Mq > -INFINITY));
+                    for (int w2 = 0; w2 < kFWarps; ++w2) anynf |= sm.red[w2][4] != 0.0f;
+                    sm.st[0] = (double)m1;
+                    sm.st[1] = s1;
+                    sm.st[2] = (double)m2;
+                    sm.st[3] = s2;
+                    // a row with a NaN or +inf logit, or without any finite one
+                    sm.st_dead = anynf || !(m1 > -INFINITY) || (pair && !(m2 > -INFINITY));
+                }
+                if (!fsync(sm, g)) break;  // red is reused below
+                Mp = (float)sm.st[0];
+                Sp = sm.st[1];
+                Mq = (float)sm.st[2];
+                Sq = sm.st[3];
+                dead = sm.st_dead != 0;
                 invp = dead ? 0.0f : (float)(1.0 / Sp);
                 invq = (dead || !pair) ? 0.0f : (float)(1.0 / Sq);
-                if (!fsync(sm, g)) break;  // red is reused below
             }
             continue;
         }
@@ -576,8 +591,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
             if (lane == 0) sm.red[warp][5] = wa;
         }
         if (!fsync(sm, g)) break;  // every tile sum is in
-        const double ur = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 1u);
         if (warp == 0 && !dead) {
+            const double ur = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 1u);
             // total residual mass; fall back to p when it is zero (p <= q everywhere)
             double Z = 0.0, Zp = 0.0;
             for (int tl = lane; tl < ntiles; tl += 32) {
@@ -629,7 +644,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
             if (lane == 0) {
                 sm.bc[0] = (double)(found >= 0 ? found : lastpos);
                 sm.bc[1] = before;
-                sm.bc[2] = v;
+                sm.bc[2] = v - before;  // v within the chosen tile
                 sm.bc[3] = use_p ? 1.0 : 0.0;
             }
         }
@@ -637,7 +652,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
         int token = -1;
         if (!dead) {
             const int tsel = (int)sm.bc[0];
-            const double before = sm.bc[1], v = sm.bc[2];
+            const float vrel = (float)sm.bc[2];
             const bool use_p = sm.bc[3] != 0.0;
             // re-read the tile: thread t takes EPT contiguous elements
             const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
@@ -658,28 +673,42 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                     if (rv[j] > 0.0f) last = e0 + j;
                 }
             }
-            // exclusive prefix of the thread sums, in fp64
-            double x = (double)own;
+            // running sums within the tile (from its start), compensated fp32:
+            // inclusive warp scan of the thread sums, then the warp bases
+            KSum x{own, 0.0f};
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-                if (lane >= o) x += y;
+                const float ys = __shfl_up_sync(0xFFFFFFFFu, x.s, o);
+                const float yc = __shfl_up_sync(0xFFFFFFFFu, x.c, o);
+                if (lane >= o) {
+                    const float tt = x.s + ys;
+                    const float bb = tt - x.s;
+                    const float e = (x.s - (tt - bb)) + (ys - bb);
+                    x.c = (x.c + yc) - e;
+                    x.s = tt;
+                }
             }
-            double* wtot = reinterpret_cast<double*>(sm.wr[0]);  // tile sums are no longer needed
+            float* wtot = sm.wr[0];  // the tile sums are no longer needed
             __syncwarp();
-            if (lane == 31) wtot[warp] = x;
+            if (lane == 31) {
+                wtot[2 * warp] = x.s;
+                wtot[2 * warp + 1] = x.c;
+            }
             if (!fsync(sm, g)) break;
-            double pre = before;
-            for (int w2 = 0; w2 < warp; ++w2) pre += wtot[w2];
-            pre += x - (double)own;
+            KSum pre{0.0f, 0.0f};
+            for (int w2 = 0; w2 < warp; ++w2) {
+                pre.add(wtot[2 * w2]);
+                pre.add(-wtot[2 * w2 + 1]);
+            }
+            pre.add(x.s - x.c - own);  // exclusive prefix within the warp
             int hit = INT_MAX;
-            if (own > 0.0f && pre + (double)own > v) {
-                double cum = pre;
+            if (own > 0.0f && (pre.s - pre.c) + own > vrel) {
+                KSum cum = pre;
 #pragma unroll
                 for (int j = 0; j < EPT; ++j)
                     if (hit == INT_MAX && rv[j] > 0.0f) {
-                        cum += (double)rv[j];
-                        if (cum > v) hit = e0 + j;
+                        cum.add(rv[j]);
+                        if (cum.s - cum.c > vrel) hit = e0 + j;
                     }
             }
             // the first element passing v over the tile, else its last one with weight

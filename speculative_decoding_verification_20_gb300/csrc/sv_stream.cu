@@ -1031,15 +1031,19 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
 // ---------------------------------------------------------------------------
 // combine kernel
 // ---------------------------------------------------------------------------
-constexpr int kCombineWarps = 4;  // one unit per warp
+constexpr int kCombineWarps = 4;  // two units per CTA, a warp pair per unit
+static_assert(kCombineWarps == 4, "pair_sync names two pairs");
 constexpr int kSelBuf = 512;      // a warp's scratch for a row's candidates
 static_assert(kSelBuf >= kStreamMaxK + 32, "the scratch holds a top-k plus one load step");
 
-struct CombWarp {
-    unsigned long long buf[kSelBuf];          // candidates of the row being selected
+// shared memory of one unit: row r = 0 (target) is handled by the pair's first
+// warp, r = 1 (draft) by the second
+struct CombPair {
+    unsigned long long buf[2][kSelBuf];       // candidates of the row being selected
     unsigned long long top[2][kStreamMaxK];   // kept entries of the target / draft row, (key desc, id asc)
     double prob[2][kStreamMaxK];              // their normalised probabilities, same order
     unsigned long long byid[2][kStreamMaxK];  // (id << 32 | position in top), ascending
+    int kept[2];                              // kept entries per row (-1: no finite logit)
 };
 
 // Bitonic sort across the warp of 32 * P 64-bit keys held P per lane (element
@@ -1187,7 +1191,8 @@ __device__ int warp_keep_topk(unsigned long long* buf, int m, int k, int lane) {
 // Exact top-k of a row, sorted by (logit desc, id asc), from its pieces' candidate
 // lists (each a superset of that piece's top-k); returns how many were found (k normally).
 template <int KB>
-__device__ int row_topk(const Args& a, uint32_t row_slot, int k, CombWarp& sw, unsigned long long* top, int lane) {
+__device__ int row_topk(const Args& a, uint32_t row_slot, int k, unsigned long long* buf, unsigned long long* top,
+                        int lane) {
     const int ppr = a.ppr;
     int kept = 0;
     for (int j = 0; j < ppr; ++j) {
@@ -1195,25 +1200,25 @@ __device__ int row_topk(const Args& a, uint32_t row_slot, int k, CombWarp& sw, u
         const int c = (int)__ldcg(&a.cand_cnt[piece]);
         const unsigned long long* src = a.cand + piece * kListCap;
         for (int i0 = 0; i0 < c;) {
-            if (kept + 32 > kSelBuf) kept = warp_keep_topk<KB>(sw.buf, kept, k, lane);
+            if (kept + 32 > kSelBuf) kept = warp_keep_topk<KB>(buf, kept, k, lane);
             const int take = min(c - i0, kSelBuf - kept);
 #pragma unroll 4
-            for (int i = lane; i < take; i += 32) sw.buf[kept + i] = __ldcg(&src[i0 + i]);
+            for (int i = lane; i < take; i += 32) buf[kept + i] = __ldcg(&src[i0 + i]);
             kept += take;
             i0 += take;
         }
     }
-    kept = warp_keep_topk<KB>(sw.buf, kept, k, lane);
-    warp_sort(sw.buf, kept, top, true, 0ull, lane);
+    kept = warp_keep_topk<KB>(buf, kept, k, lane);
+    warp_sort(buf, kept, top, true, 0ull, lane);
     return kept;
 }
 
 // (id << 32 | position) of the kept entries, ascending by id
-__device__ __forceinline__ void index_by_id(const unsigned long long* top, int n, CombWarp& sw,
+__device__ __forceinline__ void index_by_id(const unsigned long long* top, int n, unsigned long long* buf,
                                             unsigned long long* byid, int lane) {
-    for (int j = lane; j < n; j += 32) sw.buf[j] = ((unsigned long long)(uint32_t)comp_id(top[j]) << 32) | (uint32_t)j;
+    for (int j = lane; j < n; j += 32) buf[j] = ((unsigned long long)(uint32_t)comp_id(top[j]) << 32) | (uint32_t)j;
     __syncwarp();
-    warp_sort(sw.buf, n, byid, false, ~0ull, lane);
+    warp_sort(buf, n, byid, false, ~0ull, lane);
 }
 
 // probability of token x in a kept list indexed by id (0 if not kept)
@@ -1298,28 +1303,34 @@ __device__ void normalise_kept(const unsigned long long* top, int k, float Tf, f
     __syncwarp();
 }
 
+// One row of a unit, by one warp: exact top-k, normalisation (softmax at T,
+// then top-p) and the index by token id.
 template <typename TIn>
-__device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, CombWarp& sm, int lane) {
+__device__ void combine_row(const Args& a, const SeqInfo& si, int unit, int r, CombPair& sm, int lane) {
+    const uint32_t slot = si.row_off + (r == 0 ? (uint32_t)unit : (uint32_t)si.gamma + 1u + (uint32_t)unit);
+    const int kk = row_topk<Elem<TIn>::KB>(a, slot, si.k, sm.buf[r], sm.top[r], lane);  // ties to the lower id
+    // a row without a finite logit (non-finite ones are already flagged)
+    const uint32_t ninf_key = Elem<TIn>::key(Elem<TIn>::kNegInfBits);
+    const bool dead = kk < 1 || comp_key(sm.top[r][0]) <= ninf_key;
+    if (!dead) {
+        normalise_kept<TIn>(sm.top[r], kk, si.T, si.P, sm.prob[r]);
+        index_by_id(sm.top[r], kk, sm.buf[r], sm.byid[r], lane);
+    }
+    if (lane == 0) sm.kept[r] = dead ? -1 : kk;
+    __syncwarp();
+}
+
+// The rest of a unit, by the pair's first warp once both rows are done.
+template <typename TIn>
+__device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, CombPair& sm, int lane) {
     const int G = a.G;
     const bool pair = unit < si.gamma;
-    const uint32_t slot_t = si.row_off + (uint32_t)unit;
-    const uint32_t slot_d = si.row_off + (uint32_t)si.gamma + 1u + (uint32_t)unit;
-    const int kt = row_topk<Elem<TIn>::KB>(a, slot_t, si.k, sm, sm.top[0], lane);  // exact top-k, ties to the lower id
-    const int kd = pair ? row_topk<Elem<TIn>::KB>(a, slot_d, si.k, sm, sm.top[1], lane) : 0;
-
-    // a row without a finite logit (or with non-finite ones, already flagged)
-    const uint32_t ninf_key = Elem<TIn>::key(Elem<TIn>::kNegInfBits);
-    const bool dead = kt < 1 || comp_key(sm.top[0][0]) <= ninf_key ||
-                      (pair && (kd < 1 || comp_key(sm.top[1][0]) <= ninf_key));
-    if (dead) {
+    const int kt = sm.kept[0], kd = pair ? sm.kept[1] : 0;
+    if (kt < 0 || kd < 0) {
         if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
         unit_finished_warp(a, b, lane);
         return;
     }
-    normalise_kept<TIn>(sm.top[0], kt, si.T, si.P, sm.prob[0]);
-    if (pair) normalise_kept<TIn>(sm.top[1], kd, si.T, si.P, sm.prob[1]);
-    index_by_id(sm.top[0], kt, sm, sm.byid[0], lane);
-    if (pair) index_by_id(sm.top[1], kd, sm, sm.byid[1], lane);
 
     // acceptance test u * q(x) < p(x)
     int accept = 0;
@@ -1402,24 +1413,42 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
     unit_finished_warp(a, b, lane);
 }
 
-// one warp per unit (target row i with draft row i, or the bonus row alone)
+// named barrier of warp pair pr (ids 1 and 2; the ids are constants so the
+// kernel holds only the barriers it uses)
+__device__ __forceinline__ void pair_sync(int pr) {
+    if (pr == 0)
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+    else
+        asm volatile("bar.sync 2, 64;" ::: "memory");
+}
+
+// a warp pair per unit (target row i with draft row i, or the bonus row alone):
+// the two rows are selected and normalised at the same time
 template <typename TIn>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Args a) {
     extern __shared__ __align__(16) uint8_t comb_raw[];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    CombWarp& sw = reinterpret_cast<CombWarp*>(comb_raw)[wid];
+    const int pr = wid >> 1, r = wid & 1;
+    CombPair& sm = reinterpret_cast<CombPair*>(comb_raw)[pr];
+    constexpr int kPairs = kCombineWarps / 2;
     const uint32_t n_units = a.counts[kCntStreamUnits];
     const bool failed = a.counts[kCntError] != 0u;
-    for (uint32_t w = blockIdx.x * kCombineWarps + wid; w < n_units; w += gridDim.x * kCombineWarps) {
+    // both warps of a pair walk the same units, so they meet at the same barriers
+    for (uint32_t w = blockIdx.x * kPairs + pr; w < n_units; w += gridDim.x * kPairs) {
         const uint32_t item = a.stream_units[w];
         const int b = (int)(item >> 8), unit = (int)(item & 0xFFu);
         const SeqInfo si = a.seq[b];
         if (failed) {  // a select CTA gave up waiting: no result of this call can be trusted
-            if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_INTERNAL);
-            unit_finished_warp(a, b, lane);
+            if (r == 0) {
+                if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_INTERNAL);
+                unit_finished_warp(a, b, lane);
+            }
             continue;
         }
-        combine_unit<TIn>(a, b, unit, si, sw, lane);
+        if (r == 0 || unit < si.gamma) combine_row<TIn>(a, si, unit, r, sm, lane);
+        pair_sync(pr);
+        if (r == 0) combine_unit<TIn>(a, b, unit, si, sm, lane);
+        pair_sync(pr);  // the rows may be rebuilt
     }
 }
 
@@ -1449,7 +1478,7 @@ cudaError_t launch_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev && ev[1]) cudaEventRecord((cudaEvent_t)ev[1], s);
-    const int csmem = (int)(kCombineWarps * sizeof(CombWarp));
+    const int csmem = (int)((kCombineWarps / 2) * sizeof(CombPair));
     static const bool cattr_ok = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem) ==
                                  cudaSuccess;
     if (!cattr_ok) return cudaErrorInvalidValue;
@@ -1458,7 +1487,7 @@ cudaError_t launch_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) 
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, comb, kCombineThreads, csmem) != cudaSuccess) n = 1;
         return n > 0 ? n : 1;
     }();
-    long long cgrid = ((long long)a.B * (a.G + 1) + kCombineWarps - 1) / kCombineWarps;
+    long long cgrid = ((long long)a.B * (a.G + 1) + kCombineWarps / 2 - 1) / (kCombineWarps / 2);
     if (cgrid > (long long)sms * cocc) cgrid = (long long)sms * cocc;
     if (cgrid < 1) cgrid = 1;
     comb<<<(unsigned)cgrid, kCombineThreads, csmem, s>>>(a);
