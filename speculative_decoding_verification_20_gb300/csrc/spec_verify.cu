@@ -45,6 +45,7 @@ __device__ __forceinline__ uint32_t block_excl_scan_1024(uint32_t v, uint32_t* s
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
     __shared__ uint32_t s_warp[32];
+    grid_dependents_go();
     uint32_t base_rows = 0, base_units = 0, base_sunits = 0, base_funits = 0;
     const int G = a.G, V = a.V;
     for (int b0 = 0; b0 < a.B; b0 += blockDim.x) {
@@ -63,9 +64,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
             if (gamma < 1 || gamma > G) {
                 st |= SV_ROW_BAD_NUM_DRAFT;
             } else {
-                for (int i = 0; i < gamma; ++i) {
-                    const int x = a.draft_tokens[(size_t)b * G + i];
-                    if (x < 0 || x >= V) st |= SV_ROW_BAD_DRAFT_TOKEN;
+                const int32_t* tok = a.draft_tokens + (size_t)b * G;
+                for (int i0 = 0; i0 < gamma; i0 += 8) {  // independent loads, 8 at a time
+                    int x[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[j] = i0 + j < gamma ? tok[i0 + j] : 0;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (x[j] < 0 || x[j] >= V) st |= SV_ROW_BAD_DRAFT_TOKEN;
                 }
             }
             k = (kr > 0 && kr < V) ? kr : 0;

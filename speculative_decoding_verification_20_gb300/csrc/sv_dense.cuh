@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
     c.crank = (int)c.cl.block_rank();
     const int t = threadIdx.x;
     const int V = a.V, G = a.G;
+    grid_dependency_wait();  // the previous kernels of the call (the plan's lists)
     const uint32_t n_units = a.counts[kCntDenseUnits];
     const uint32_t cid = blockIdx.x / (uint32_t)c.cs, ncl = gridDim.x / (uint32_t)c.cs;
 
@@ -662,8 +663,7 @@ cudaError_t launch_dense_cluster(const Args& a, int cs, int sms, cudaStream_t s)
     long long n = clusters;
     if (n > upper) n = upper;
     if (n < 1) n = 1;
-    cfg.gridDim = dim3((unsigned)(n * cs));
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, k, a);
+    const cudaError_t e = launch_pdl(k, dim3((unsigned)(n * cs)), dim3(kDenseThreads), 0, s, a, attr, 1);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -329,6 +329,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    grid_dependency_wait();  // the previous kernels of the call (the plan's lists)
+    grid_dependents_go();
     const uint32_t n_units = a.counts[kCntFreeUnits];
 
     if (warp == kFWarps) {
@@ -781,8 +783,7 @@ cudaError_t launch_free_t(const Args& a, int sms, cudaStream_t s, void* const ev
     if (grid > units) grid = units;
     if (grid < 1) grid = 1;
     if (ev && ev[0]) cudaEventRecord((cudaEvent_t)ev[0], s);
-    k<<<(unsigned)grid, kFThreads, smem, s>>>(a);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(k, dim3((unsigned)grid), dim3(kFThreads), (size_t)smem, s, a);
     if (e != cudaSuccess) return e;
     if (ev && ev[1]) cudaEventRecord((cudaEvent_t)ev[1], s);
     return cudaSuccess;

@@ -148,6 +148,11 @@ __host__ __device__ inline WsLayout ws_layout(int B, int G, int V, int dtype) {
 // ---------------------------------------------------------------------------
 #ifdef __CUDACC__
 
+// wait for the previous kernel of the call (a no-op when launched without a
+// programmatic dependency), and let the next one be scheduled
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_go() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of two 32x32->64
 // multiplies with the Weyl-bumped key; only output word 0 is used here.
 __device__ __forceinline__ uint32_t philox_w0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
@@ -220,6 +225,30 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // host launchers, one per kernel translation unit
 cudaError_t launch_stream_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, void* const ev[2]);
+
+// Programmatic dependent launch: every kernel after the plan kernel is
+// launched so that it may start (and run its prologue) while the previous
+// kernel of the call is finishing; it waits for that kernel's completion and
+// memory with grid_dependency_wait() before reading anything it produced.
+// Each kernel lets the next one be scheduled once all its own blocks run.
+template <typename K>
+inline cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Args& a,
+                              const cudaLaunchAttribute* extra = nullptr, int n_extra = 0) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[4];
+    int n = 0;
+    for (int i = 0; i < n_extra && n < 3; ++i) attr[n++] = extra[i];
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)n;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 cudaError_t launch_free_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, void* const ev[2]);
 cudaError_t launch_dense_f32(bool vector, const Args& a, int sms, cudaStream_t s);
 cudaError_t launch_dense_bf16(bool vector, const Args& a, int sms, cudaStream_t s);

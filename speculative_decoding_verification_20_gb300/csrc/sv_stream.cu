@@ -884,6 +884,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
     }
     if (t < kConsumerWarps) sm.pub[t] = 0u;
     __syncthreads();
+    grid_dependency_wait();  // the plan kernel's lists and counters
+    grid_dependents_go();
     const uint32_t n_pieces = a.counts[kCntStreamRows] * (uint32_t)ppr;
 
     if (warp == kConsumerWarps) {
@@ -1431,6 +1433,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Args a) {
     const int pr = wid >> 1, r = wid & 1;
     CombPair& sm = reinterpret_cast<CombPair*>(comb_raw)[pr];
     constexpr int kPairs = kCombineWarps / 2;
+    grid_dependency_wait();  // the select kernel's candidate lists
+    grid_dependents_go();
     const uint32_t n_units = a.counts[kCntStreamUnits];
     const bool failed = a.counts[kCntError] != 0u;
     // both warps of a pair walk the same units, so they meet at the same barriers
@@ -1474,8 +1478,7 @@ cudaError_t launch_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) 
     if (grid > pieces) grid = pieces;
     if (grid < 1) grid = 1;
     if (ev && ev[0]) cudaEventRecord((cudaEvent_t)ev[0], s);
-    sel<<<(unsigned)grid, kSelThreads, smem, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(sel, dim3((unsigned)grid), dim3(kSelThreads), (size_t)smem, s, a);
     if (e != cudaSuccess) return e;
     if (ev && ev[1]) cudaEventRecord((cudaEvent_t)ev[1], s);
     const int csmem = (int)((kCombineWarps / 2) * sizeof(CombPair));
@@ -1490,8 +1493,7 @@ cudaError_t launch_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) 
     long long cgrid = ((long long)a.B * (a.G + 1) + kCombineWarps / 2 - 1) / (kCombineWarps / 2);
     if (cgrid > (long long)sms * cocc) cgrid = (long long)sms * cocc;
     if (cgrid < 1) cgrid = 1;
-    comb<<<(unsigned)cgrid, kCombineThreads, csmem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(comb, dim3((unsigned)cgrid), dim3(kCombineThreads), (size_t)csmem, s, a);
 }
 }  // namespace
 

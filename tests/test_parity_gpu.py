@@ -255,3 +255,32 @@ def test_determinism_and_seed_sensitivity():
     assert torch.equal(a["out_tokens"], b["out_tokens"]) and torch.equal(a["alpha"], b["alpha"])
     assert not torch.equal(a["out_tokens"], c["out_tokens"])
     assert torch.equal(a["alpha"], c["alpha"])  # alpha does not depend on the randomness
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_streaming_threshold_redo_and_overflow(dtype):
+    """Rows that defeat the streaming kernel's speculative threshold: logits that
+    fall along the row (the top-k all sit in the first tile, so fewer than k
+    logits reach a threshold taken from that tile and the piece is redone
+    conservatively), rows of equal logits (every logit passes, the warps'
+    lists overflow and are cut exactly, ties to the lower id) and rows that
+    rise along the row."""
+    B, G, V = 6, 2, 128256 if dtype == "bf16" else 65536
+    gen = torch.Generator().manual_seed(5)
+    base = torch.linspace(4.0, -4.0, V)
+    t = torch.empty(B, G + 1, V)
+    t[0:2] = base + 0.01 * torch.randn(2, G + 1, V, generator=gen)   # falling
+    t[2:4] = 1.5                                                       # all equal
+    t[4:6] = base.flip(0) + 0.01 * torch.randn(2, G + 1, V, generator=gen)  # rising
+    d = t[:, :G] + 0.05 * torch.randn(B, G, V, generator=gen)
+    d[2:4] = 1.5
+    if dtype == "bf16":
+        t, d = t.bfloat16(), d.bfloat16()
+    x = torch.randint(0, 64, (B, G), generator=gen, dtype=torch.int32)
+    x[4:6] = V - 1 - x[4:6]
+    for k in (1, 50, 200):
+        wl = workloads.Workload("redo", B, G, V, dtype, t.contiguous(), d.contiguous(), x, None,
+                                torch.full((B,), 0.9), torch.full((B,), k, dtype=torch.int32),
+                                torch.full((B,), 0.95, dtype=torch.float32), 40 + k)
+        rep, _, _ = run(wl, probs=True)
+        assert_ok(rep)
