@@ -82,8 +82,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
                     P = 1.0f;
                 }
                 const bool stream = (k >= 1 && k <= kStreamMaxK);
-                const bool unfiltered = k == 0 && P >= 1.0f;
-                mode = a.force_dense ? kModeDense : stream ? kModeStream : unfiltered ? kModeFree : kModeDense;
+                // no top-k: the whole-row kernel (with the nucleus cut when top-p < 1)
+                mode = a.force_dense ? kModeDense : stream ? kModeStream : k == 0 ? kModeFree : kModeDense;
                 if (mode == kModeStream)
                     nrows = 2 * gamma + 1;
                 else if (mode == kModeDense)

@@ -24,6 +24,7 @@
 //   Every wait (ring and the consumers' own barrier) is bounded (2 s); on a
 //   timeout the CTA records kCntError and the affected sequences are marked.
 #include "sv_finalize.cuh"
+#include "sv_warp_sort.cuh"
 
 namespace sv {
 namespace {
@@ -38,6 +39,18 @@ constexpr int kFMaxTiles = (SV_MAX_VOCAB * 4 + kFSegBytes - 1) / kFSegBytes;
 constexpr unsigned long long kFWaitNs = 2000000000ull;
 static_assert(kFVec * 16 * kFConsumers == kFSegBytes, "segment geometry");
 
+// nucleus (top-p) cut of a row: probability mass histograms over the distance
+// below the row maximum, d = (max - l) * log2(e) / T, in log2 units
+constexpr float kNDmax = 64.0f;  // beyond it a logit's mass is below 2^-64 of the maximum's
+constexpr int kNB1 = 512;        // coarse bins of 1/8 log2 unit
+constexpr int kNB2 = 512;        // fine bins inside the coarse bin where the running mass passes P
+constexpr int kNCap = 256;       // elements of the crossing fine bin sorted here (else: cluster kernel)
+constexpr float kMassScale = 1099511627776.0f;  // 2^40: masses are summed in 64-bit fixed point
+static_assert(kNCap <= kNB1, "the crossing elements are collected over the coarse histogram");
+// passes of a unit through the ring: 0 statistics, 1 coarse histogram, 2 fine
+// histogram, 3 collect the crossing elements, 4 alpha and residual weights
+constexpr int kPassFinal = 4;
+
 struct FreeSmem {
     alignas(128) uint8_t buf[kFStages][2][kFSegBytes];  // [stage][target, draft segment]
     uint64_t full[kFStages];
@@ -50,6 +63,14 @@ struct FreeSmem {
     double bc[4];                   // broadcast of the residual search
     double st[4];                   // broadcast of the row statistics: Mp, Sp, Mq, Sq
     int st_dead;
+    unsigned long long h1[2][kNB1];  // per row: coarse mass histogram (2^40 fixed point); then the crossing elements
+    unsigned long long h2[2][kNB2];  // per row: fine mass histogram
+    int nb[2][2];                    // per row: crossing coarse bin, crossing fine bin
+    unsigned long long nbase[2];     // per row: mass before the crossing fine bin
+    int ncnt[2];                     // per row: crossing elements collected
+    uint32_t cut_key[2], cut_id[2];  // per row: the last kept element (key, id)
+    double kmass[2];                 // per row: kept mass
+    int nfall;                       // the unit goes to the cluster kernel
     int ired[kFWarps][2];
 };
 
@@ -206,6 +227,13 @@ __device__ __forceinline__ float fex2(float x) {
 }
 __device__ __forceinline__ float prob_f(float l, float M, float c, float inv) { return fex2((l - M) * c) * inv; }
 __device__ __forceinline__ float resid_f(float p, float q) { return fmaxf(p - q, 0.0f); }
+// the (top-p renormalised) probability of element id with logit l: zero past
+// the row's last kept element `cut` (cut 0: the row is not filtered)
+__device__ __forceinline__ float kept_prob(float l, uint32_t id, float M, float c, float inv2, unsigned long long cut) {
+    if (cut != 0ull && ((unsigned long long)okey32(__float_as_uint(l)) << 32 | (unsigned long long)(~id)) < cut)
+        return 0.0f;
+    return fex2((l - M) * c) * inv2;
+}
 
 // online softmax state of one row for one thread: running maximum logit m and
 // the compensated sum of exp2((l - m) * c)
@@ -309,6 +337,147 @@ __device__ __forceinline__ void combine_online(const FreeSmem& sm, int col, floa
     *S = s;
 }
 
+// ---------------------------------------------------------------------------
+// nucleus cut helpers
+// ---------------------------------------------------------------------------
+// (key << 32 | ~id): descending order is logit descending, then id ascending
+__device__ __forceinline__ unsigned long long ncomp(float x, uint32_t id) {
+    return ((unsigned long long)okey32(__float_as_uint(x)) << 32) | (unsigned long long)(~id);
+}
+__device__ __forceinline__ unsigned long long mass_fix(float p) { return __float2ull_rz(p * kMassScale); }
+
+// For the warp: the first bin of h[0..n) (n a multiple of 32) at which the
+// running mass reaches target, and the mass before it; if the total falls
+// short (rounding), the last bin with mass.  -1 when h is empty.
+__device__ int warp_cross(const unsigned long long* h, int n, unsigned long long target, unsigned long long* before,
+                          int lane) {
+    const int per = n / 32;
+    const unsigned long long* mine = h + lane * per;
+    unsigned long long own = 0;
+    for (int i = 0; i < per; ++i) own += mine[i];
+    unsigned long long x = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    const unsigned long long excl = x - own;
+    int bin = -1;
+    unsigned long long bef = 0;
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, own > 0 && x >= target);
+    const unsigned nz = __ballot_sync(0xFFFFFFFFu, own > 0);
+    int src = 0;
+    if (hit) {
+        src = __ffs(hit) - 1;
+        if (lane == src) {
+            unsigned long long run = excl;
+            for (int i = 0; i < per; ++i) {
+                if (mine[i] > 0 && run + mine[i] >= target) {
+                    bin = lane * per + i;
+                    bef = run;
+                    break;
+                }
+                run += mine[i];
+            }
+        }
+    } else if (nz) {
+        src = 31 - __clz(nz);
+        if (lane == src) {
+            unsigned long long run = excl;
+            for (int i = 0; i < per; ++i) {
+                if (mine[i] > 0) {
+                    bin = lane * per + i;
+                    bef = run;
+                }
+                run += mine[i];
+            }
+        }
+    }
+    bin = __shfl_sync(0xFFFFFFFFu, bin, src);
+    *before = __shfl_sync(0xFFFFFFFFu, bef, src);
+    return bin;
+}
+
+// For the warp: sort the n collected crossing elements of a row (key desc,
+// id asc) and walk them from the mass before their fine bin to the first one
+// whose running mass reaches P (the nucleus' last token).  Returns false if
+// there are too many (or none) to decide here.
+__device__ bool warp_cut(unsigned long long* list, int n, unsigned long long base, double P, float M, float c,
+                         float inv, uint32_t* cut_key, uint32_t* cut_id, double* kept, int lane) {
+    if (n < 1 || n > kNCap) return false;
+    warp_sort(list, n, list, true, 0ull, lane);
+    double cum = (double)base / (double)kMassScale;
+    int idx = -1;
+    double K = 0.0;
+    for (int c0 = 0; c0 < n && idx < 0; c0 += 32) {
+        const int j = c0 + lane;
+        const double p = j < n ? (double)prob_f(key_value32((uint32_t)(list[j] >> 32)), M, c, inv) : 0.0;
+        double x = p;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < n && cum + x >= P);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            idx = c0 + l;
+            K = cum + __shfl_sync(0xFFFFFFFFu, x, l);
+        }
+        cum += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    if (idx < 0) {  // rounding: the running mass stops just short of P
+        idx = n - 1;
+        K = cum;
+    }
+    *cut_key = (uint32_t)(list[idx] >> 32);
+    *cut_id = ~(uint32_t)list[idx];
+    *kept = K;
+    return true;
+}
+
+// One tile of a nucleus pass for row r (max M, 1/sum inv): pass 1 adds the
+// masses to the coarse histogram, pass 2 those of the crossing coarse bin to
+// the fine histogram, pass 3 collects the elements of the crossing fine bin.
+template <typename TIn>
+__device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVec], int n, int t, int col, int pass,
+                                             int r, float M, float c, float inv) {
+    using F = FE<TIn>;
+    const float s1 = (float)kNB1 / kNDmax;
+    const float s2 = (float)kNB2 * (float)kNB1 / kNDmax;
+    const int b1 = pass >= 2 ? sm.nb[r][0] : -1;
+    const int b2 = pass >= 3 ? sm.nb[r][1] : -1;
+    const float d1 = (float)b1 * (kNDmax / (float)kNB1);
+#pragma unroll
+    for (int i = 0; i < kFVec; ++i) {
+        const int e0 = (i * kFConsumers + t) * F::VEC;
+        const int valid = min(F::VEC, n - e0);
+        if (valid <= 0) continue;
+        float x[F::VEC];
+        F::unpack(v[i], x);
+#pragma unroll
+        for (int j = 0; j < F::VEC; ++j) {
+            if (j >= valid) continue;
+            const float d = (M - x[j]) * c;
+            if (!(d < kNDmax)) continue;
+            const int bb = min(kNB1 - 1, (int)(d * s1));
+            if (pass == 1) {
+                const float p = prob_f(x[j], M, c, inv);
+                if (p > 0.0f) atomicAdd(&sm.h1[r][bb], mass_fix(p));
+            } else if (bb == b1) {
+                const int sb = min(kNB2 - 1, max(0, (int)((d - d1) * s2)));
+                if (pass == 2) {
+                    const float p = prob_f(x[j], M, c, inv);
+                    if (p > 0.0f) atomicAdd(&sm.h2[r][sb], mass_fix(p));
+                } else if (sb == b2) {
+                    const int slot = atomicAdd(&sm.ncnt[r], 1);
+                    if (slot < kNCap) sm.h1[r][slot] = ncomp(x[j], (uint32_t)(col + e0 + j));
+                }
+            }
+        }
+    }
+}
+
 template <typename TIn, bool TMA>
 __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
     using F = FE<TIn>;
@@ -349,10 +518,13 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 if (w >= n_units) break;
                 const uint32_t item = a.free_units[w];
                 const int b = (int)(item >> 8), u = (int)(item & 0xFFu);
-                const bool pair = u < a.seq[b].gamma;
+                const SeqInfo si = a.seq[b];
+                const bool pair = u < si.gamma;
+                const bool nucleus = si.P < 1.0f;
                 const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
                 const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
-                for (int pass = 0; pass < 2 && ok; ++pass)
+                for (int pi = 0; pi < (nucleus ? 5 : 2) && ok; ++pi) {
+                    const int pass = nucleus ? pi : (pi == 0 ? 0 : kPassFinal);
                     for (int tile = 0; tile < ntiles && ok; ++tile) {
                         const int col = tile * TS, n = min(TS, V - col);
                         if (!fbar_wait(&sm.empty[stage], ph)) {
@@ -381,6 +553,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                             ph ^= 1u;
                         }
                     }
+                }
             }
             if (ok && fbar_wait(&sm.empty[stage], ph)) {
                 if (lane == 0) {
@@ -407,6 +580,10 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
     float Mp = 0.0f, Mq = 0.0f, invp = 0.0f, invq = 0.0f;
     double Sp = 0.0, Sq = 0.0;
     KSum alpha{0.0f, 0.0f};
+    bool nuc = false, fall = false;  // top-p < 1; the unit goes to the cluster kernel
+    float Pf = 1.0f, invp2 = 0.0f, invq2 = 0.0f;
+    unsigned long long cutp = 0ull, cutq = 0ull;  // last kept element of each row (0: keep all)
+    double Kp = 1.0, Kq = 1.0;                    // kept mass of each row
     while (true) {
         if (!__all_sync(0xFFFFFFFFu, fbar_wait(&sm.full[stage], ph))) {
             g.ok = false;
@@ -423,6 +600,11 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
             const SeqInfo si = a.seq[b];
             pair = u < si.gamma;
             c = 1.4426950408889634f / si.T;
+            nuc = si.P < 1.0f;
+            Pf = si.P;
+            fall = false;
+            cutp = cutq = 0ull;
+            Kp = Kq = 1.0;
             op.init();
             oq.init();
             nf = false;
@@ -514,6 +696,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                     // a row with a NaN or +inf logit, or without any finite one
                     sm.st_dead = anynf || !(m1 > -INFINITY) || (pair && !(m2 > -INFINITY));
                 }
+                if (nuc)  // the coarse histograms start empty
+                    for (int i = t; i < 2 * kNB1; i += kFConsumers) (&sm.h1[0][0])[i] = 0ull;
                 if (!fsync(sm, g)) break;  // red is reused below
                 Mp = (float)sm.st[0];
                 Sp = sm.st[1];
@@ -522,9 +706,75 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 dead = sm.st_dead != 0;
                 invp = dead ? 0.0f : (float)(1.0 / Sp);
                 invq = (dead || !pair) ? 0.0f : (float)(1.0 / Sq);
+                invp2 = invp;
+                invq2 = invq;
             }
             continue;
         }
+
+        if (pass < kPassFinal) {
+            // ---- nucleus passes: the last kept token of each row (top-p < 1)
+            if (dead) continue;
+            nucleus_tile<TIn>(sm, vp, n, t, col, pass, 0, Mp, c, invp);
+            if (pair) nucleus_tile<TIn>(sm, vq, n, t, col, pass, 1, Mq, c, invq);
+            if (tile != ntiles - 1) continue;
+            if (!fsync(sm, g)) break;
+            const unsigned long long target = (unsigned long long)((double)Pf * (double)kMassScale);
+            if (warp < (pair ? 2 : 1)) {
+                const int r = warp;
+                unsigned long long bef = 0ull;
+                if (pass == 1) {
+                    const int bin = warp_cross(sm.h1[r], kNB1, target, &bef, lane);
+                    if (lane == 0) {
+                        sm.nb[r][0] = bin;
+                        sm.nbase[r] = bef;
+                    }
+                } else if (pass == 2) {
+                    const unsigned long long base = sm.nbase[r];
+                    const int bin = sm.nb[r][0] < 0 ? -1
+                                                    : warp_cross(sm.h2[r], kNB2, target > base ? target - base : 0ull,
+                                                                 &bef, lane);
+                    if (lane == 0) {
+                        sm.nb[r][1] = bin;
+                        sm.nbase[r] = base + bef;
+                    }
+                } else {
+                    uint32_t ck = 0u, ci = 0u;
+                    double K = 0.0;
+                    const int cnt = sm.ncnt[r];
+                    const bool ok = sm.nb[r][1] >= 0 &&
+                                    warp_cut(sm.h1[r], min(cnt, kNCap + 1), sm.nbase[r], (double)Pf,
+                                             r == 0 ? Mp : Mq, c, r == 0 ? invp : invq, &ck, &ci, &K, lane);
+                    if (lane == 0) {
+                        sm.cut_key[r] = ck;
+                        sm.cut_id[r] = ci;
+                        sm.kmass[r] = ok ? K : -1.0;
+                    }
+                }
+            }
+            if (pass == 1)  // the fine histograms start empty
+                for (int i = t; i < 2 * kNB2; i += kFConsumers) (&sm.h2[0][0])[i] = 0ull;
+            if (pass == 2 && t < 2) sm.ncnt[t] = 0;
+            if (!fsync(sm, g)) break;
+            if (pass == 3) {
+                fall = sm.kmass[0] < 0.0 || (pair && sm.kmass[1] < 0.0);
+                if (!fall) {
+                    cutp = ((unsigned long long)sm.cut_key[0] << 32) | (unsigned long long)(~sm.cut_id[0]);
+                    Kp = sm.kmass[0];
+                    invp2 = (float)(1.0 / (Sp * Kp));
+                    if (pair) {
+                        cutq = ((unsigned long long)sm.cut_key[1] << 32) | (unsigned long long)(~sm.cut_id[1]);
+                        Kq = sm.kmass[1];
+                        invq2 = (float)(1.0 / (Sq * Kq));
+                    }
+                } else if (t == 0) {  // too many logits at the cut to sort here: the cluster kernel takes the unit
+                    const uint32_t slot = atomicAdd(&a.counts[kCntDenseUnits], 1u);
+                    a.dense_units[slot] = a.free_units[w];
+                }
+            }
+            continue;
+        }
+        if (fall) continue;  // the cluster kernel finishes this unit
 
         // ---- pass 2: alpha, residual weights, per-tile sums (and the debug outputs)
         float tr = 0.0f, tp = 0.0f;
@@ -542,8 +792,9 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                     float ma[F::VEC], ra[F::VEC], pa[F::VEC];
 #pragma unroll
                     for (int j = 0; j < F::VEC; ++j) {
-                        const float p = j < valid ? prob_f(xp[j], Mp, c, invp) : 0.0f;
-                        const float q = j < valid ? prob_f(xq[j], Mq, c, invq) : 0.0f;
+                        const uint32_t id = (uint32_t)(col + e0 + j);
+                        const float p = j < valid ? kept_prob(xp[j], id, Mp, c, invp2, cutp) : 0.0f;
+                        const float q = j < valid ? kept_prob(xq[j], id, Mq, c, invq2, cutq) : 0.0f;
                         ma[j] = fminf(p, q);
                         ra[j] = resid_f(p, q);
                         pa[j] = p;
@@ -562,7 +813,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 } else {
 #pragma unroll
                     for (int j = 0; j < F::VEC; ++j)
-                        if (j < valid) tp += prob_f(xp[j], Mp, c, invp);
+                        if (j < valid) tp += kept_prob(xp[j], (uint32_t)(col + e0 + j), Mp, c, invp2, cutp);
                     tr = tp;
                 }
                 alpha.add(am);
@@ -571,9 +822,11 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                     for (int j = 0; j < F::VEC; ++j)
                         if (j < valid) {
                             if (a.p_out)
-                                a.p_out[((size_t)b * (G + 1) + u) * V + col + e0 + j] = prob_f(xp[j], Mp, c, invp);
+                                a.p_out[((size_t)b * (G + 1) + u) * V + col + e0 + j] =
+                                    kept_prob(xp[j], (uint32_t)(col + e0 + j), Mp, c, invp2, cutp);
                             if (a.q_out && pair)
-                                a.q_out[((size_t)b * G + u) * V + col + e0 + j] = prob_f(xq[j], Mq, c, invq);
+                                a.q_out[((size_t)b * G + u) * V + col + e0 + j] =
+                                    kept_prob(xq[j], (uint32_t)(col + e0 + j), Mq, c, invq2, cutq);
                         }
                 }
             }
@@ -668,8 +921,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
             for (int j = 0; j < EPT; ++j) {
                 rv[j] = 0.0f;
                 if (tsel >= 0 && e0 + j < e1) {
-                    const float p = prob_f(F::load(trow, e0 + j), Mp, c, invp);
-                    const float q = pair ? prob_f(F::load(drow, e0 + j), Mq, c, invq) : 0.0f;
+                    const float p = kept_prob(F::load(trow, e0 + j), (uint32_t)(e0 + j), Mp, c, invp2, cutp);
+                    const float q = pair ? kept_prob(F::load(drow, e0 + j), (uint32_t)(e0 + j), Mq, c, invq2, cutq) : 0.0f;
                     rv[j] = (pair && !use_p) ? resid_f(p, q) : p;
                     own += rv[j];
                     if (rv[j] > 0.0f) last = e0 + j;
@@ -744,8 +997,13 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                     const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
                     const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
                     const double T = (double)a.seq[b].T;
-                    const double px = exp(((double)F::load(trow, xt) - (double)Mp) / T) / Sp;
-                    const double qx = exp(((double)F::load(drow, xt) - (double)Mq) / T) / Sq;
+                    const float lpx = F::load(trow, xt), lqx = F::load(drow, xt);
+                    const unsigned long long kx = (unsigned long long)okey32(__float_as_uint(lpx)) << 32 |
+                                                  (unsigned long long)(~(uint32_t)xt);
+                    const unsigned long long kqx = (unsigned long long)okey32(__float_as_uint(lqx)) << 32 |
+                                                   (unsigned long long)(~(uint32_t)xt);
+                    const double px = (cutp != 0ull && kx < cutp) ? 0.0 : exp(((double)lpx - (double)Mp) / T) / (Sp * Kp);
+                    const double qx = (cutq != 0ull && kqx < cutq) ? 0.0 : exp(((double)lqx - (double)Mq) / T) / (Sq * Kq);
                     const double ua = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 0u);
                     accept = (ua * qx < px) ? 1 : 0;
                     double al = 0.0;

@@ -43,6 +43,7 @@
 // records kCntError, stops issuing copies, waits (bounded) for the copies it
 // issued and leaves; the combine kernel then marks the affected sequences.
 #include "sv_finalize.cuh"
+#include "sv_warp_sort.cuh"
 
 namespace sv {
 
@@ -1047,67 +1048,6 @@ struct CombPair {
     unsigned long long byid[2][kStreamMaxK];  // (id << 32 | position in top), ascending
     int kept[2];                              // kept entries per row (-1: no finite logit)
 };
-
-// Bitonic sort across the warp of 32 * P 64-bit keys held P per lane (element
-// m * 32 + lane in x[m]), descending or ascending.
-template <int P>
-__device__ __forceinline__ void warp_bitonic(unsigned long long (&x)[P], int lane, bool descending) {
-    constexpr int N = 32 * P;
-#pragma unroll
-    for (int k2 = 2; k2 <= N; k2 <<= 1) {
-#pragma unroll
-        for (int j = k2 >> 1; j > 0; j >>= 1) {
-            if (j >= 32) {  // partners in the same lane
-#pragma unroll
-                for (int m = 0; m < P; ++m) {
-                    const int mp = m ^ (j >> 5);
-                    if (mp > m) {
-                        const bool lower_max = (((m * 32 + lane) & k2) == 0) == descending;
-                        const unsigned long long lo = x[m], hi = x[mp];
-                        const bool sw = lower_max ? (lo < hi) : (lo > hi);
-                        x[m] = sw ? hi : lo;
-                        x[mp] = sw ? lo : hi;
-                    }
-                }
-            } else {  // partners in lane ^ j
-#pragma unroll
-                for (int m = 0; m < P; ++m) {
-                    const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, x[m], j);
-                    const bool lower = (lane & j) == 0;
-                    const bool lower_max = (((m * 32 + lane) & k2) == 0) == descending;
-                    const bool take_max = lower == lower_max;
-                    x[m] = take_max ? (x[m] > y ? x[m] : y) : (x[m] < y ? x[m] : y);
-                }
-            }
-        }
-    }
-}
-
-// Sort n <= 32 * P entries of src (pad: `pad`) into dst across the warp.
-template <int P>
-__device__ __forceinline__ void warp_sort_into(const unsigned long long* src, int n, unsigned long long* dst,
-                                               bool descending, unsigned long long pad, int lane) {
-    unsigned long long x[P];
-#pragma unroll
-    for (int m = 0; m < P; ++m) x[m] = m * 32 + lane < n ? src[m * 32 + lane] : pad;
-    warp_bitonic<P>(x, lane, descending);
-    __syncwarp();
-#pragma unroll
-    for (int m = 0; m < P; ++m)
-        if (m * 32 + lane < n) dst[m * 32 + lane] = x[m];
-    __syncwarp();
-}
-__device__ __forceinline__ void warp_sort(const unsigned long long* src, int n, unsigned long long* dst,
-                                          bool descending, unsigned long long pad, int lane) {
-    if (n <= 32)
-        warp_sort_into<1>(src, n, dst, descending, pad, lane);
-    else if (n <= 64)
-        warp_sort_into<2>(src, n, dst, descending, pad, lane);
-    else if (n <= 128)
-        warp_sort_into<4>(src, n, dst, descending, pad, lane);
-    else
-        warp_sort_into<8>(src, n, dst, descending, pad, lane);
-}
 
 // Keep the exact top-k (key descending, then id ascending) of buf[0..m) in
 // buf[0..k), unordered; returns the count.  The k-th key is found bit by bit
