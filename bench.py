@@ -36,7 +36,9 @@ FALLBACK_HBM_GBS = 6800.0
 # the unfiltered whole-row kernel and the dense cluster kernel (a kernel whose
 # path no row takes exits at once)
 LAUNCHES_PER_STEP = 5
+# sources of the select kernel, whose DRAM traffic profiles/traffic.json records
 KERNEL_SOURCES = ("speculative_decoding_verification_20_gb300/csrc/sv_stream.cu",
+                  "speculative_decoding_verification_20_gb300/csrc/sv_keys.cuh",
                   "speculative_decoding_verification_20_gb300/csrc/sv_internal.cuh",
                   "speculative_decoding_verification_20_gb300/csrc/sv_finalize.cuh")
 
@@ -201,6 +203,24 @@ def rank_seed(rank: int) -> int:
     return rank
 
 
+def bytes_by_path(wl, stream_max_k: int) -> dict:
+    """Algorithmic logit bytes each path of the library reads for this batch:
+    greedy or 1 <= top_k <= stream_max_k rows stream (select kernel); rows with
+    no top-k the whole-row kernel (free); larger top-k the cluster kernel."""
+    import numpy as np
+
+    gam = wl.gammas()
+    T = wl.temperature.detach().cpu().numpy()
+    k = np.zeros(wl.B, dtype=np.int64) if wl.top_k is None else wl.top_k.detach().cpu().numpy().astype(np.int64)
+    k = np.where((k > 0) & (k < wl.V), k, 0)
+    stream = (T == 0) | ((k >= 1) & (k <= stream_max_k))
+    free = ~stream & (k == 0)
+    es = 2 if wl.dtype == "bf16" else 4
+    rowb = (2 * gam + 1) * wl.V * es
+    return {"stream": int(rowb[stream].sum()), "free": int(rowb[free].sum()),
+            "dense": int(rowb[~stream & ~free].sum())}
+
+
 def workload_config(name: str, B: int | None = None) -> dict:
     from speculative_decoding_verification_20_gb300.workloads import CONFIGS
 
@@ -263,12 +283,8 @@ def main():
     torch.cuda.synchronize(dev)
 
     # per-step events around the dominant kernel, recorded by the library on the launching stream
-    if wl.top_k is not None and int(wl.top_k.max()) <= sv.SV_STREAM_MAX_TOP_K:
-        main = "stream"
-    elif wl.top_k is None and wl.top_p is None and float(wl.temperature.min()) > 0.0:
-        main = "free"
-    else:
-        main = "dense"
+    path_bytes = bytes_by_path(wl, sv.SV_STREAM_MAX_TOP_K)
+    main = max(path_bytes, key=path_bytes.get)  # the kernel that reads the most logits
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a_, b_ in kev:  # torch creates the underlying CUDA events on their first record
         a_.record(stream)
@@ -296,7 +312,8 @@ def main():
     kernel_ms = [a.elapsed_time(b) for a, b in kev]
     kernel_ms_avg = sum(kernel_ms) / len(kernel_ms)
     bytes_per_launch = wl.logit_bytes()
-    achieved = bytes_per_launch / (kernel_ms_avg * 1e-3) / 1e9
+    main_bytes = path_bytes[main]
+    achieved = main_bytes / (kernel_ms_avg * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
 
     # end to end through the host-buffer entry point: pinned inputs in, results out, every step
@@ -345,7 +362,7 @@ def main():
                      "kernel": {"stream": "select_kernel (streaming top-k path)",
                                 "free": "free_kernel (whole-row path of unfiltered rows)",
                                 "dense": "dense_kernel (cluster path)"}[main],
-                     "kernel_ms": kernel_ms_avg, "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "kernel_ms": kernel_ms_avg, "algorithmic_bytes_per_launch": main_bytes,
                      "traffic": traffic},
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,

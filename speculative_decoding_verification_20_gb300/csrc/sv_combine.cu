@@ -1,0 +1,460 @@
+// sv_combine.cu -- combine kernel of the streaming top-k path.
+//
+// A warp pair per unit (target row i with draft row i, or the bonus row
+// alone): each warp merges its row's candidate lists from the select kernel
+// into the exact top-k (ties to the lower id), normalises it (softmax over the
+// kept logits at T, then top-p), and the first warp finishes the unit:
+// alpha, the acceptance test and the residual / bonus draw (inverse CDF in
+// ascending token id) ("Fast Inference from Transformers via Speculative
+// Decoding" review page, Algorithm 1; "Speculative decoding: the art of
+// guessing well", section 投机采样).
+#include "sv_keys.cuh"
+#include "sv_warp_sort.cuh"
+
+namespace sv {
+
+constexpr int kCombineThreads = 128;  // 4 warps
+
+// ---------------------------------------------------------------------------
+// combine kernel
+// ---------------------------------------------------------------------------
+constexpr int kCombineWarps = 4;  // two units per CTA, a warp pair per unit
+static_assert(kCombineWarps == 4, "pair_sync names two pairs");
+constexpr int kSelBuf = 512;      // a warp's scratch for a row's candidates
+static_assert(kSelBuf >= kStreamMaxK + 32, "the scratch holds a top-k plus one load step");
+
+// shared memory of one unit: row r = 0 (target) is handled by the pair's first
+// warp, r = 1 (draft) by the second
+struct CombPair {
+    unsigned long long buf[2][kSelBuf];       // candidates of the row being selected
+    unsigned long long top[2][kStreamMaxK];   // kept entries of the target / draft row, (key desc, id asc)
+    float prob[2][kStreamMaxK];               // their normalised probabilities, same order
+    unsigned long long byid[2][kStreamMaxK];  // (id << 32 | position in top), ascending
+    int kept[2];                              // kept entries per row (-1: no finite logit)
+};
+
+// Keep the exact top-k (key descending, then id ascending) of buf[0..m) in
+// buf[0..k), unordered; returns the count.  The k-th key is found bit by bit
+// below the common prefix of the smallest and largest key (warp reductions),
+// ties at it by id (ids < 2^18).  M slots per lane cover m.
+template <int KB, int M>
+__device__ int warp_keep_topk_m(unsigned long long* buf, int m, int k, int lane) {
+    const int used = (m + 31) >> 5;
+    unsigned long long e[M];
+    uint32_t key[M];
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const int idx = lane + 32 * i;
+        e[i] = (i < used && idx < m) ? buf[idx] : 0ull;
+        key[i] = comp_key(e[i]);
+        if (key[i] != 0u) {
+            lo = min(lo, key[i]);
+            hi = max(hi, key[i]);
+        }
+    }
+    lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+    hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const uint32_t diff = lo ^ hi;
+    const int nb = diff ? 32 - __clz(diff) : 0;
+    uint32_t kth = nb >= 32 ? 0u : (lo & ~((1u << nb) - 1u));
+#pragma unroll 1
+    for (int bit = nb - 1; bit >= 0; --bit) {
+        const uint32_t c = kth | (1u << bit);
+        unsigned n = 0u;
+#pragma unroll
+        for (int i = 0; i < M; ++i)
+            if (i < used) n += key[i] >= c;
+        if (__reduce_add_sync(0xFFFFFFFFu, n) >= (unsigned)k) kth = c;
+    }
+    unsigned gt = 0u, eq = 0u;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        gt += key[i] > kth;
+        eq += key[i] == kth;
+    }
+    gt = __reduce_add_sync(0xFFFFFFFFu, gt);
+    eq = __reduce_add_sync(0xFFFFFFFFu, eq);
+    const unsigned need = (unsigned)k - gt;
+    uint32_t id_cut = 0xFFFFFFFFu;
+    if (eq > need) {
+        uint32_t idl = 0u;
+#pragma unroll 1
+        for (int bit = 17; bit >= 0; --bit) {
+            const uint32_t c = idl | (1u << bit);
+            unsigned nlt = 0u;
+#pragma unroll
+            for (int i = 0; i < M; ++i) nlt += key[i] == kth && (uint32_t)comp_id(e[i]) < c;
+            if (__reduce_add_sync(0xFFFFFFFFu, nlt) < need) idl = c;
+        }
+        id_cut = idl;
+    }
+    __syncwarp();
+    const unsigned lt = lanemask_lt();
+    int base = 0;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        if (i < used) {
+            const bool keep = key[i] > kth || (key[i] == kth && (uint32_t)comp_id(e[i]) <= id_cut);
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+            if (keep) buf[base + __popc(bal & lt)] = e[i];
+            base += __popc(bal);
+        }
+    }
+    __syncwarp();
+    return base;
+}
+template <int KB>
+__device__ int warp_keep_topk(unsigned long long* buf, int m, int k, int lane) {
+    __syncwarp();
+    if (m <= k) return m;
+    if (m <= 64) return warp_keep_topk_m<KB, 2>(buf, m, k, lane);
+    if (m <= 128) return warp_keep_topk_m<KB, 4>(buf, m, k, lane);
+    if (m <= 256) return warp_keep_topk_m<KB, 8>(buf, m, k, lane);
+    return warp_keep_topk_m<KB, kSelBuf / 32>(buf, m, k, lane);
+}
+
+// Exact top-k of a row, sorted by (logit desc, id asc), from its pieces' candidate
+// lists (each a superset of that piece's top-k); returns how many were found (k normally).
+template <int KB>
+__device__ int row_topk(const Args& a, uint32_t row_slot, int k, unsigned long long* buf, unsigned long long* top,
+                        int lane) {
+    const int ppr = a.ppr;
+    int kept = 0;
+    for (int j = 0; j < ppr; ++j) {
+        const size_t piece = (size_t)row_slot * ppr + j;
+        const int c = (int)__ldcg(&a.cand_cnt[piece]);
+        const unsigned long long* src = a.cand + piece * kListCap;
+        for (int i0 = 0; i0 < c;) {
+            if (kept + 32 > kSelBuf) kept = warp_keep_topk<KB>(buf, kept, k, lane);
+            const int take = min(c - i0, kSelBuf - kept);
+#pragma unroll 4
+            for (int i = lane; i < take; i += 32) buf[kept + i] = __ldcg(&src[i0 + i]);
+            kept += take;
+            i0 += take;
+        }
+    }
+    kept = warp_keep_topk<KB>(buf, kept, k, lane);
+    warp_sort(buf, kept, top, true, 0ull, lane);
+    return kept;
+}
+
+// (id << 32 | position) of the kept entries, ascending by id
+__device__ __forceinline__ void index_by_id(const unsigned long long* top, int n, unsigned long long* buf,
+                                            unsigned long long* byid, int lane) {
+    for (int j = lane; j < n; j += 32) buf[j] = ((unsigned long long)(uint32_t)comp_id(top[j]) << 32) | (uint32_t)j;
+    __syncwarp();
+    warp_sort(buf, n, byid, false, ~0ull, lane);
+}
+
+// probability of token x in a kept list indexed by id (0 if not kept)
+__device__ __forceinline__ float prob_of(const unsigned long long* byid, const float* prob, int n, int x) {
+    int lo = 0, hi = n - 1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        const int id = (int)(byid[mid] >> 32);
+        if (id == x) return prob[(uint32_t)byid[mid]];
+        if (id < x)
+            lo = mid + 1;
+        else
+            hi = mid - 1;
+    }
+    return 0.0f;
+}
+
+// 2^x for x <= 0, with the exponent split (Cody-Waite style) into an integer n
+// and a fraction f in [-1/2, 1/2] in fp64: only f goes through the fp32 exp2,
+// and 2^n is applied exactly, so the result keeps the fp32 exp2's relative
+// accuracy whatever the size of x, at the cost of a few fp64 operations
+// (instead of a full fp64 exponential).  Below 2^-1022 the result is 0.
+__device__ __forceinline__ double exp2_split(double x) {
+    const double n = rint(x);
+    if (n < -1022.0) return 0.0;
+    const double f = x - n;
+    const double pw = __longlong_as_double((long long)(n + 1023.0) << 52);
+    return (double)exp2f((float)f) * pw;
+}
+
+// compensated fp32 value s - c: sums of fp32 terms kept to about fp32
+// rounding of the total, whatever the number of terms
+struct CF {
+    float s, c;
+};
+__device__ __forceinline__ CF cf_add(CF a, CF b) {  // exact two-sum of the heads
+    const float t = a.s + b.s;
+    const float bb = t - a.s;
+    const float e = (a.s - (t - bb)) + (b.s - bb);
+    return CF{t, (a.c + b.c) - e};
+}
+__device__ __forceinline__ float cf_val(CF a) { return a.s - a.c; }
+__device__ __forceinline__ CF warp_cf_sum(CF a) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        a = cf_add(a, CF{__shfl_xor_sync(0xFFFFFFFFu, a.s, o), __shfl_xor_sync(0xFFFFFFFFu, a.c, o)});
+    return a;
+}
+__device__ __forceinline__ CF warp_cf_scan(CF a, int lane) {  // inclusive, in lane order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const CF y{__shfl_up_sync(0xFFFFFFFFu, a.s, o), __shfl_up_sync(0xFFFFFFFFu, a.c, o)};
+        if (lane >= o) a = cf_add(y, a);
+    }
+    return a;
+}
+
+// Unnormalised weight 2^((v - vmax) * log2(e) / T) of a kept logit.
+// bf16 logits: v - vmax is exact in fp32; the product with log2(e)/T (given
+// as a float pair chi + clo) is formed exactly by an FMA two-product (Dekker),
+// split into an integer n and a fraction in fp32, and only the fraction goes
+// through exp2f -- no fp64 arithmetic.  fp32 logits: the difference is not
+// always exact in fp32, so the exponent is formed in fp64 (exp2_split).
+template <typename TIn>
+struct KeptWeight;
+template <>
+struct KeptWeight<__nv_bfloat16> {
+    __device__ static float vmax_of(uint32_t k) { return key_value16(k); }
+    __device__ static float w(uint32_t k, float vmax, float chi, float clo, double) {
+        const float d = key_value16(k) - vmax;
+        const float p = d * chi;
+        const float e = fmaf(d, chi, -p);
+        const float n = rintf(p);
+        if (n < -126.0f) return 0.0f;
+        const float f = (p - n) + fmaf(d, clo, e);
+        return exp2f(f) * __int_as_float((int)(n + 127.0f) << 23);
+    }
+};
+template <>
+struct KeptWeight<float> {
+    __device__ static float vmax_of(uint32_t k) { return key_value32(k); }
+    __device__ static float w(uint32_t k, float vmax, float, float, double c2) {
+        return (float)exp2_split(((double)key_value32(k) - (double)vmax) * c2);
+    }
+};
+
+// Normalisation of one sorted kept list by one warp: softmax over the kept
+// logits at temperature T (one-hot if T == 0), then top-p.  prob[j] for j < k.
+template <typename TIn>
+__device__ void normalise_kept(const unsigned long long* top, int k, float Tf, float Pf, float* prob) {
+    const int lane = threadIdx.x & 31;
+    if (Tf == 0.0f) {
+        for (int j = lane; j < k; j += 32) prob[j] = (j == 0) ? 1.0f : 0.0f;
+        __syncwarp();
+        return;
+    }
+    const float vmax = KeptWeight<TIn>::vmax_of(comp_key(top[0]));
+    const double c2 = 1.4426950408889634 / (double)Tf;  // log2(e) / T
+    const float chi = (float)c2, clo = (float)(c2 - (double)chi);
+    CF s{0.0f, 0.0f};
+    for (int j = lane; j < k; j += 32) {
+        const float w = KeptWeight<TIn>::w(comp_key(top[j]), vmax, chi, clo, c2);
+        prob[j] = w;
+        s = cf_add(s, CF{w, 0.0f});
+    }
+    s = warp_cf_sum(s);
+    // probabilities and the top-p running mass in fp64 from the fp32 weights, so
+    // that exact ties (equal weights, 1/k each) sum as the fp64 definition does
+    const double inv = 1.0 / ((double)s.s - (double)s.c);
+    __syncwarp();
+    if (Pf < 1.0f) {  // shortest prefix (prob desc, id asc) whose mass reaches P, crossing token kept
+        const double P = (double)Pf;
+        double carry = 0.0;
+        int keep = k;
+        for (int c0 = 0; c0 < k; c0 += 32) {
+            const int j = c0 + lane;
+            double x = j < k ? (double)prob[j] * inv : 0.0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < k && carry + x >= P);
+            if (hit) {
+                keep = c0 + __ffs(hit);
+                break;
+            }
+            carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+        }
+        double s2 = 0.0;
+        for (int j = lane; j < keep; j += 32) s2 += (double)prob[j] * inv;
+        s2 = warp_sum(s2);
+        const double inv2 = inv / s2;
+        __syncwarp();
+        for (int j = lane; j < k; j += 32) prob[j] = j < keep ? (float)((double)prob[j] * inv2) : 0.0f;
+    } else {
+        for (int j = lane; j < k; j += 32) prob[j] = (float)((double)prob[j] * inv);
+    }
+    __syncwarp();
+}
+
+// One row of a unit, by one warp: exact top-k, normalisation (softmax at T,
+// then top-p) and the index by token id.
+template <typename TIn>
+__device__ void combine_row(const Args& a, const SeqInfo& si, int unit, int r, CombPair& sm, int lane) {
+    const uint32_t slot = si.row_off + (r == 0 ? (uint32_t)unit : (uint32_t)si.gamma + 1u + (uint32_t)unit);
+    const int kk = row_topk<Elem<TIn>::KB>(a, slot, si.k, sm.buf[r], sm.top[r], lane);  // ties to the lower id
+    // a row without a finite logit (non-finite ones are already flagged)
+    const uint32_t ninf_key = Elem<TIn>::key(Elem<TIn>::kNegInfBits);
+    const bool dead = kk < 1 || comp_key(sm.top[r][0]) <= ninf_key;
+    if (!dead) {
+        normalise_kept<TIn>(sm.top[r], kk, si.T, si.P, sm.prob[r]);
+        index_by_id(sm.top[r], kk, sm.buf[r], sm.byid[r], lane);
+    }
+    if (lane == 0) sm.kept[r] = dead ? -1 : kk;
+    __syncwarp();
+}
+
+// The rest of a unit, by the pair's first warp once both rows are done.
+template <typename TIn>
+__device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, CombPair& sm, int lane) {
+    const int G = a.G;
+    const bool pair = unit < si.gamma;
+    const int kt = sm.kept[0], kd = pair ? sm.kept[1] : 0;
+    if (kt < 0 || kd < 0) {
+        if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+        unit_finished_warp(a, b, lane);
+        return;
+    }
+
+    // acceptance test u * q(x) < p(x)
+    int accept = 0;
+    if (pair) {
+        const int x = a.draft_tokens[(size_t)b * G + unit];
+        const double px = (double)prob_of(sm.byid[0], sm.prob[0], kt, x);
+        const double qx = (double)prob_of(sm.byid[1], sm.prob[1], kd, x);
+        const double u = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 0u);
+        accept = (u * qx < px) ? 1 : 0;
+    }
+
+    // alpha_i = sum_x min(p, q) and the residual weights, in ascending token id
+    // over the target's kept ids (an id kept only by the draft has p = 0)
+    float rr[kStreamMaxK / 32];
+    CF alpha{0.0f, 0.0f}, Z{0.0f, 0.0f}, Zp{0.0f, 0.0f};
+#pragma unroll
+    for (int m = 0; m < kStreamMaxK / 32; ++m) {
+        const int j = lane + 32 * m;
+        rr[m] = 0.0f;
+        if (j < kt) {
+            const unsigned long long e = sm.byid[0][j];
+            const float p = sm.prob[0][(uint32_t)e];
+            const float q = pair ? prob_of(sm.byid[1], sm.prob[1], kd, (int)(e >> 32)) : 0.0f;
+            alpha = cf_add(alpha, CF{fminf(p, q), 0.0f});
+            rr[m] = fmaxf(p - q, 0.0f);  // bonus: q_{gamma+1} := 0
+            Z = cf_add(Z, CF{rr[m], 0.0f});
+            Zp = cf_add(Zp, CF{p, 0.0f});
+        }
+    }
+    const float alpha_v = cf_val(warp_cf_sum(alpha));
+    float Zt = cf_val(warp_cf_sum(Z));
+    const bool use_p = !(Zt > 0.0f);  // p <= q everywhere: fall back to p
+    if (use_p) {
+        Zt = cf_val(warp_cf_sum(Zp));
+#pragma unroll
+        for (int m = 0; m < kStreamMaxK / 32; ++m) {
+            const int j = lane + 32 * m;
+            rr[m] = j < kt ? sm.prob[0][(uint32_t)sm.byid[0][j]] : 0.0f;
+        }
+    }
+    // inverse CDF: the first id whose running sum passes v
+    const double v = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 1u) * (double)Zt;
+    int token = -1, last_pos = -1;
+    CF carry{0.0f, 0.0f};
+#pragma unroll
+    for (int m = 0; m < kStreamMaxK / 32; ++m) {
+        const int c0 = 32 * m;
+        if (c0 >= kt || token >= 0) break;
+        const int j = c0 + lane;
+        const float r = rr[m];
+        const CF x = cf_add(carry, warp_cf_scan(CF{r, 0.0f}, lane));
+        const unsigned pos = __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0f);
+        if (pos) last_pos = c0 + 31 - __clz(pos);
+        const unsigned hit =
+            __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0f && (double)x.s - (double)x.c > v);
+        if (hit) token = (int)(sm.byid[0][c0 + __ffs(hit) - 1] >> 32);
+        carry = CF{__shfl_sync(0xFFFFFFFFu, x.s, 31), __shfl_sync(0xFFFFFFFFu, x.c, 31)};
+    }
+    if (token < 0 && last_pos >= 0) token = (int)(sm.byid[0][last_pos] >> 32);
+
+    if (lane == 0) {
+        if (pair) {
+            a.alpha[(size_t)b * G + unit] = alpha_v;
+            a.unit_acc[(size_t)b * G + unit] = accept;
+            if (a.pos_accept) a.pos_accept[(size_t)b * G + unit] = accept;
+        }
+        a.unit_tok[(size_t)b * (G + 1) + unit] = token;
+        if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + unit] = token;
+    }
+    if (a.p_out)
+        for (int j = lane; j < kt; j += 32)
+            a.p_out[((size_t)b * (G + 1) + unit) * a.V + comp_id(sm.top[0][j])] = sm.prob[0][j];
+    if (a.q_out && pair)
+        for (int j = lane; j < kd; j += 32)
+            a.q_out[((size_t)b * G + unit) * a.V + comp_id(sm.top[1][j])] = sm.prob[1][j];
+    unit_finished_warp(a, b, lane);
+}
+
+// named barrier of warp pair pr (ids 1 and 2; the ids are constants so the
+// kernel holds only the barriers it uses)
+__device__ __forceinline__ void pair_sync(int pr) {
+    if (pr == 0)
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+    else
+        asm volatile("bar.sync 2, 64;" ::: "memory");
+}
+
+// a warp pair per unit (target row i with draft row i, or the bonus row alone):
+// the two rows are selected and normalised at the same time
+template <typename TIn>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(Args a) {
+    extern __shared__ __align__(16) uint8_t comb_raw[];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int pr = wid >> 1, r = wid & 1;
+    CombPair& sm = reinterpret_cast<CombPair*>(comb_raw)[pr];
+    constexpr int kPairs = kCombineWarps / 2;
+    grid_dependency_wait();  // the select kernel's candidate lists
+    grid_dependents_go();
+    const uint32_t n_units = a.counts[kCntStreamUnits];
+    const bool failed = a.counts[kCntError] != 0u;
+    // both warps of a pair walk the same units, so they meet at the same barriers
+    for (uint32_t w = blockIdx.x * kPairs + pr; w < n_units; w += gridDim.x * kPairs) {
+        const uint32_t item = a.stream_units[w];
+        const int b = (int)(item >> 8), unit = (int)(item & 0xFFu);
+        const SeqInfo si = a.seq[b];
+        if (failed) {  // a select CTA gave up waiting: no result of this call can be trusted
+            if (r == 0) {
+                if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_INTERNAL);
+                unit_finished_warp(a, b, lane);
+            }
+            continue;
+        }
+        if (r == 0 || unit < si.gamma) combine_row<TIn>(a, si, unit, r, sm, lane);
+        pair_sync(pr);
+        if (r == 0) combine_unit<TIn>(a, b, unit, si, sm, lane);
+        pair_sync(pr);  // the rows may be rebuilt
+    }
+}
+
+namespace {
+template <typename TIn>
+cudaError_t launch_comb_t(const Args& a, int sms, cudaStream_t s) {
+    auto comb = combine_kernel<TIn>;
+    const int csmem = (int)((kCombineWarps / 2) * sizeof(CombPair));
+    static const bool cattr_ok = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem) ==
+                                 cudaSuccess;
+    if (!cattr_ok) return cudaErrorInvalidValue;
+    static const int cocc = [&] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, comb, kCombineThreads, csmem) != cudaSuccess) n = 1;
+        return n > 0 ? n : 1;
+    }();
+    long long cgrid = ((long long)a.B * (a.G + 1) + kCombineWarps / 2 - 1) / (kCombineWarps / 2);
+    if (cgrid > (long long)sms * cocc) cgrid = (long long)sms * cocc;
+    if (cgrid < 1) cgrid = 1;
+    return launch_pdl(comb, dim3((unsigned)cgrid), dim3(kCombineThreads), (size_t)csmem, s, a);
+}
+}  // namespace
+
+cudaError_t launch_combine_kernel(int dtype, const Args& a, int sms, cudaStream_t s) {
+    return dtype == SV_BF16 ? launch_comb_t<__nv_bfloat16>(a, sms, s) : launch_comb_t<float>(a, sms, s);
+}
+
+}  // namespace sv

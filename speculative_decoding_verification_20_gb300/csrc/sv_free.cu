@@ -23,6 +23,8 @@
 //   exact two-sum, and sums across warps and tiles are fp64.
 //   Every wait (ring and the consumers' own barrier) is bounded (2 s); on a
 //   timeout the CTA records kCntError and the affected sequences are marked.
+#include <type_traits>
+
 #include "sv_finalize.cuh"
 #include "sv_warp_sort.cuh"
 
@@ -229,9 +231,10 @@ __device__ __forceinline__ float prob_f(float l, float M, float c, float inv) { 
 __device__ __forceinline__ float resid_f(float p, float q) { return fmaxf(p - q, 0.0f); }
 // the (top-p renormalised) probability of element id with logit l: zero past
 // the row's last kept element `cut` (cut 0: the row is not filtered)
+// (CUT: the row is filtered; else no test at all)
+template <bool CUT>
 __device__ __forceinline__ float kept_prob(float l, uint32_t id, float M, float c, float inv2, unsigned long long cut) {
-    if (cut != 0ull && ((unsigned long long)okey32(__float_as_uint(l)) << 32 | (unsigned long long)(~id)) < cut)
-        return 0.0f;
+    if (CUT && ((unsigned long long)okey32(__float_as_uint(l)) << 32 | (unsigned long long)(~id)) < cut) return 0.0f;
     return fex2((l - M) * c) * inv2;
 }
 
@@ -778,7 +781,10 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
 
         // ---- pass 2: alpha, residual weights, per-tile sums (and the debug outputs)
         float tr = 0.0f, tp = 0.0f;
-        if (!dead) {
+        // the per-element work, specialised on whether the rows are filtered (one
+        // branch per tile instead of a test per element)
+        auto final_tile = [&](auto cut_on) {
+            constexpr bool CUT = decltype(cut_on)::value;
 #pragma unroll
             for (int i = 0; i < kFVec; ++i) {
                 const int e0 = (i * kFConsumers + t) * F::VEC;
@@ -793,8 +799,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
 #pragma unroll
                     for (int j = 0; j < F::VEC; ++j) {
                         const uint32_t id = (uint32_t)(col + e0 + j);
-                        const float p = j < valid ? kept_prob(xp[j], id, Mp, c, invp2, cutp) : 0.0f;
-                        const float q = j < valid ? kept_prob(xq[j], id, Mq, c, invq2, cutq) : 0.0f;
+                        const float p = j < valid ? kept_prob<CUT>(xp[j], id, Mp, c, invp2, cutp) : 0.0f;
+                        const float q = j < valid ? kept_prob<CUT>(xq[j], id, Mq, c, invq2, cutq) : 0.0f;
                         ma[j] = fminf(p, q);
                         ra[j] = resid_f(p, q);
                         pa[j] = p;
@@ -813,7 +819,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 } else {
 #pragma unroll
                     for (int j = 0; j < F::VEC; ++j)
-                        if (j < valid) tp += kept_prob(xp[j], (uint32_t)(col + e0 + j), Mp, c, invp2, cutp);
+                        if (j < valid) tp += kept_prob<CUT>(xp[j], (uint32_t)(col + e0 + j), Mp, c, invp2, cutp);
                     tr = tp;
                 }
                 alpha.add(am);
@@ -823,13 +829,19 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                         if (j < valid) {
                             if (a.p_out)
                                 a.p_out[((size_t)b * (G + 1) + u) * V + col + e0 + j] =
-                                    kept_prob(xp[j], (uint32_t)(col + e0 + j), Mp, c, invp2, cutp);
+                                    kept_prob<CUT>(xp[j], (uint32_t)(col + e0 + j), Mp, c, invp2, cutp);
                             if (a.q_out && pair)
                                 a.q_out[((size_t)b * G + u) * V + col + e0 + j] =
-                                    kept_prob(xq[j], (uint32_t)(col + e0 + j), Mq, c, invq2, cutq);
+                                    kept_prob<CUT>(xq[j], (uint32_t)(col + e0 + j), Mq, c, invq2, cutq);
                         }
                 }
             }
+        };
+        if (!dead) {
+            if (nuc)
+                final_tile(std::true_type{});
+            else
+                final_tile(std::false_type{});
         }
         {
             const float wtr = warp_ksum(KSum{tr, 0.0f}), wtp = warp_ksum(KSum{tp, 0.0f});
@@ -921,8 +933,9 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
             for (int j = 0; j < EPT; ++j) {
                 rv[j] = 0.0f;
                 if (tsel >= 0 && e0 + j < e1) {
-                    const float p = kept_prob(F::load(trow, e0 + j), (uint32_t)(e0 + j), Mp, c, invp2, cutp);
-                    const float q = pair ? kept_prob(F::load(drow, e0 + j), (uint32_t)(e0 + j), Mq, c, invq2, cutq) : 0.0f;
+                    const float p = kept_prob<true>(F::load(trow, e0 + j), (uint32_t)(e0 + j), Mp, c, invp2, cutp);
+                    const float q =
+                        pair ? kept_prob<true>(F::load(drow, e0 + j), (uint32_t)(e0 + j), Mq, c, invq2, cutq) : 0.0f;
                     rv[j] = (pair && !use_p) ? resid_f(p, q) : p;
                     own += rv[j];
                     if (rv[j] > 0.0f) last = e0 + j;

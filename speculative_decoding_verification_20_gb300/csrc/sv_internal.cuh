@@ -249,6 +249,7 @@ inline cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
     cfg.numAttrs = (unsigned)n;
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
+cudaError_t launch_combine_kernel(int dtype, const Args& a, int sms, cudaStream_t s);
 cudaError_t launch_free_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, void* const ev[2]);
 cudaError_t launch_dense_f32(bool vector, const Args& a, int sms, cudaStream_t s);
 cudaError_t launch_dense_bf16(bool vector, const Args& a, int sms, cudaStream_t s);

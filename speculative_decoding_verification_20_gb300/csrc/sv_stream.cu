@@ -1,4 +1,4 @@
-// sv_stream.cu -- streaming top-k path (greedy and 1 <= top_k <= 256 sequences).
+// sv_stream.cu -- select kernel of the streaming top-k path (greedy and 1 <= top_k <= 256 sequences).
 //
 // Normalisation with top-k ("Fast Inference from Transformers via Speculative
 // Decoding" review page, section "Method: Speculative Decoding": top-k and
@@ -34,16 +34,13 @@
 //   mbarrier.  At the end of a piece the warps' lists (a superset of the
 //   piece's top-k, at most 512 entries; else cut to exactly k) are written to
 //   the workspace.
-// combine_kernel (one warp per unit)
-//   merges the pieces of the unit's target and draft rows and does, in fp64,
-//   softmax over the kept logits, top-p, alpha, the acceptance test and the
-//   residual / bonus draw (inverse CDF in ascending token id).
+// The candidate lists go to the combine kernel (sv_combine.cu), which keeps
+// the exact top-k of each row and finishes the unit.
 //
 // Every mbarrier wait is bounded (2 s on %globaltimer); on timeout the CTA
 // records kCntError, stops issuing copies, waits (bounded) for the copies it
 // issued and leaves; the combine kernel then marks the affected sequences.
-#include "sv_finalize.cuh"
-#include "sv_warp_sort.cuh"
+#include "sv_keys.cuh"
 
 namespace sv {
 
@@ -52,7 +49,6 @@ constexpr int kConsumerWarps = 7;  // with the producer, 8 warps: 2 CTAs per SM 
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kSelThreads = kConsumers + 32;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-constexpr int kCombineThreads = 128;  // 4 warps
 
 // ---------------------------------------------------------------------------
 // PTX helpers: mbarriers, TMA bulk copies, the consumer-only named barrier
@@ -100,116 +96,6 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
 }
 
 // ---------------------------------------------------------------------------
-// keys and composites
-// ---------------------------------------------------------------------------
-template <typename TIn>
-struct Elem;
-template <>
-struct Elem<__nv_bfloat16> {
-    static constexpr int VEC = 8, KB = 16;
-    __device__ static uint32_t bits(const uint4& v, int j) {
-        const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
-        return (j & 1) ? (w >> 16) : (w & 0xFFFFu);
-    }
-    __device__ static uint32_t key(uint32_t b) { return okey16(b); }
-    __device__ static float value(uint32_t b) { return __uint_as_float(b << 16); }
-    __device__ static double key_value(uint32_t k) { return (double)key_value16(k); }
-    __device__ static bool bad(uint32_t b) { return bad16(b); }
-    // bit pattern of a float that holds a bf16 value exactly
-    __device__ static uint32_t bits_of(float f) { return __float_as_uint(f) >> 16; }
-    __device__ static uint32_t load_bits(const __nv_bfloat16* p, int i) {
-        return reinterpret_cast<const unsigned short*>(p)[i];
-    }
-    static constexpr uint32_t kNegInfBits = 0xFF80u;
-};
-template <>
-struct Elem<float> {
-    static constexpr int VEC = 4, KB = 32;
-    __device__ static uint32_t bits(const uint4& v, int j) { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; }
-    __device__ static uint32_t key(uint32_t b) { return okey32(b); }
-    __device__ static float value(uint32_t b) { return __uint_as_float(b); }
-    __device__ static double key_value(uint32_t k) { return (double)key_value32(k); }
-    __device__ static bool bad(uint32_t b) { return bad32(b); }
-    __device__ static uint32_t bits_of(float f) { return __float_as_uint(f); }
-    __device__ static uint32_t load_bits(const float* p, int i) { return reinterpret_cast<const uint32_t*>(p)[i]; }
-    static constexpr uint32_t kNegInfBits = 0xFF800000u;
-};
-
-// composite sort key: logit key descending, then token id ascending
-__device__ __forceinline__ unsigned long long composite(uint32_t key, uint32_t id) {
-    return ((unsigned long long)key << 32) | (unsigned long long)(~id);
-}
-__device__ __forceinline__ uint32_t comp_key(unsigned long long c) { return (uint32_t)(c >> 32); }
-__device__ __forceinline__ int comp_id(unsigned long long c) { return (int)(~(uint32_t)c); }
-
-__device__ __forceinline__ int next_pow2(int n) {
-    int p = 1;
-    while (p < n) p <<= 1;
-    return p;
-}
-
-// NaN-propagating max of the 16-byte vector (as float), used both as the
-// fast-path filter and for non-finite detection
-__device__ __forceinline__ float vmax_nan(const uint4& v, __nv_bfloat16*) {
-    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
-    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
-    __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
-    __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
-    const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
-    return __bfloat162float(__hmax_nan(__low2bfloat16(m), __high2bfloat16(m)));
-}
-__device__ __forceinline__ float fmax_nan(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ float vmax_nan(const uint4& v, float*) {
-    return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
-                    fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
-}
-
-// Fast-path test of one full 16-byte vector: updates the running NaN-propagating
-// maximum and says whether any element may pass the threshold.
-struct RunBf16 {
-    __nv_bfloat162 run, th2;
-};
-__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
-__device__ __forceinline__ bool vec_test(const uint4& v, RunBf16& r, bool strict) {
-    const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(as_bf2(v.x), as_bf2(v.y)), __hmax2_nan(as_bf2(v.z), as_bf2(v.w)));
-    r.run = __hmax2_nan(r.run, m);
-    return (strict ? __hgt2_mask(m, r.th2) : __hge2_mask(m, r.th2)) != 0u;
-}
-__device__ __forceinline__ void run_init(RunBf16& r, float thv) {
-    r.run = __float2bfloat162_rn(-INFINITY);
-    r.th2 = __float2bfloat162_rn(thv);
-}
-__device__ __forceinline__ float run_value(const RunBf16& r) {
-    return __bfloat162float(__hmax_nan(__low2bfloat16(r.run), __high2bfloat16(r.run)));
-}
-struct RunF32 {
-    float run, th;
-};
-__device__ __forceinline__ bool vec_test(const uint4& v, RunF32& r, bool strict) {
-    const float m = fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
-                             fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
-    r.run = fmax_nan(r.run, m);
-    return strict ? (m > r.th) : (m >= r.th);
-}
-__device__ __forceinline__ void run_init(RunF32& r, float thv) {
-    r.run = -INFINITY;
-    r.th = thv;
-}
-__device__ __forceinline__ float run_value(const RunF32& r) { return r.run; }
-template <typename TIn>
-struct RunOf {
-    using type = RunF32;
-};
-template <>
-struct RunOf<__nv_bfloat16> {
-    using type = RunBf16;
-};
-
-// ---------------------------------------------------------------------------
 // select kernel
 // ---------------------------------------------------------------------------
 constexpr int kWarpCap = kStreamMaxK + 32;          // a warp's list: its exact top-k plus one step of appends
@@ -235,11 +121,6 @@ struct SelSmem {
     int hist[16];
 };
 
-__device__ __forceinline__ unsigned lanemask_lt() {
-    unsigned m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
 
 // Barrier of the consumer warps on an mbarrier (8 arrivals per phase): bounded
 // like every other wait, so a lost copy cannot leave warps parked for good.
@@ -1032,378 +913,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
 
 
 // ---------------------------------------------------------------------------
-// combine kernel
-// ---------------------------------------------------------------------------
-constexpr int kCombineWarps = 4;  // two units per CTA, a warp pair per unit
-static_assert(kCombineWarps == 4, "pair_sync names two pairs");
-constexpr int kSelBuf = 512;      // a warp's scratch for a row's candidates
-static_assert(kSelBuf >= kStreamMaxK + 32, "the scratch holds a top-k plus one load step");
-
-// shared memory of one unit: row r = 0 (target) is handled by the pair's first
-// warp, r = 1 (draft) by the second
-struct CombPair {
-    unsigned long long buf[2][kSelBuf];       // candidates of the row being selected
-    unsigned long long top[2][kStreamMaxK];   // kept entries of the target / draft row, (key desc, id asc)
-    double prob[2][kStreamMaxK];              // their normalised probabilities, same order
-    unsigned long long byid[2][kStreamMaxK];  // (id << 32 | position in top), ascending
-    int kept[2];                              // kept entries per row (-1: no finite logit)
-};
-
-// Keep the exact top-k (key descending, then id ascending) of buf[0..m) in
-// buf[0..k), unordered; returns the count.  The k-th key is found bit by bit
-// below the common prefix of the smallest and largest key (warp reductions),
-// ties at it by id (ids < 2^18).  M slots per lane cover m.
-template <int KB, int M>
-__device__ int warp_keep_topk_m(unsigned long long* buf, int m, int k, int lane) {
-    const int used = (m + 31) >> 5;
-    unsigned long long e[M];
-    uint32_t key[M];
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-        const int idx = lane + 32 * i;
-        e[i] = (i < used && idx < m) ? buf[idx] : 0ull;
-        key[i] = comp_key(e[i]);
-        if (key[i] != 0u) {
-            lo = min(lo, key[i]);
-            hi = max(hi, key[i]);
-        }
-    }
-    lo = __reduce_min_sync(0xFFFFFFFFu, lo);
-    hi = __reduce_max_sync(0xFFFFFFFFu, hi);
-    const uint32_t diff = lo ^ hi;
-    const int nb = diff ? 32 - __clz(diff) : 0;
-    uint32_t kth = nb >= 32 ? 0u : (lo & ~((1u << nb) - 1u));
-#pragma unroll 1
-    for (int bit = nb - 1; bit >= 0; --bit) {
-        const uint32_t c = kth | (1u << bit);
-        unsigned n = 0u;
-#pragma unroll
-        for (int i = 0; i < M; ++i)
-            if (i < used) n += key[i] >= c;
-        if (__reduce_add_sync(0xFFFFFFFFu, n) >= (unsigned)k) kth = c;
-    }
-    unsigned gt = 0u, eq = 0u;
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-        gt += key[i] > kth;
-        eq += key[i] == kth;
-    }
-    gt = __reduce_add_sync(0xFFFFFFFFu, gt);
-    eq = __reduce_add_sync(0xFFFFFFFFu, eq);
-    const unsigned need = (unsigned)k - gt;
-    uint32_t id_cut = 0xFFFFFFFFu;
-    if (eq > need) {
-        uint32_t idl = 0u;
-#pragma unroll 1
-        for (int bit = 17; bit >= 0; --bit) {
-            const uint32_t c = idl | (1u << bit);
-            unsigned nlt = 0u;
-#pragma unroll
-            for (int i = 0; i < M; ++i) nlt += key[i] == kth && (uint32_t)comp_id(e[i]) < c;
-            if (__reduce_add_sync(0xFFFFFFFFu, nlt) < need) idl = c;
-        }
-        id_cut = idl;
-    }
-    __syncwarp();
-    const unsigned lt = lanemask_lt();
-    int base = 0;
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-        if (i < used) {
-            const bool keep = key[i] > kth || (key[i] == kth && (uint32_t)comp_id(e[i]) <= id_cut);
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
-            if (keep) buf[base + __popc(bal & lt)] = e[i];
-            base += __popc(bal);
-        }
-    }
-    __syncwarp();
-    return base;
-}
-template <int KB>
-__device__ int warp_keep_topk(unsigned long long* buf, int m, int k, int lane) {
-    __syncwarp();
-    if (m <= k) return m;
-    if (m <= 64) return warp_keep_topk_m<KB, 2>(buf, m, k, lane);
-    if (m <= 128) return warp_keep_topk_m<KB, 4>(buf, m, k, lane);
-    if (m <= 256) return warp_keep_topk_m<KB, 8>(buf, m, k, lane);
-    return warp_keep_topk_m<KB, kSelBuf / 32>(buf, m, k, lane);
-}
-
-// Exact top-k of a row, sorted by (logit desc, id asc), from its pieces' candidate
-// lists (each a superset of that piece's top-k); returns how many were found (k normally).
-template <int KB>
-__device__ int row_topk(const Args& a, uint32_t row_slot, int k, unsigned long long* buf, unsigned long long* top,
-                        int lane) {
-    const int ppr = a.ppr;
-    int kept = 0;
-    for (int j = 0; j < ppr; ++j) {
-        const size_t piece = (size_t)row_slot * ppr + j;
-        const int c = (int)__ldcg(&a.cand_cnt[piece]);
-        const unsigned long long* src = a.cand + piece * kListCap;
-        for (int i0 = 0; i0 < c;) {
-            if (kept + 32 > kSelBuf) kept = warp_keep_topk<KB>(buf, kept, k, lane);
-            const int take = min(c - i0, kSelBuf - kept);
-#pragma unroll 4
-            for (int i = lane; i < take; i += 32) buf[kept + i] = __ldcg(&src[i0 + i]);
-            kept += take;
-            i0 += take;
-        }
-    }
-    kept = warp_keep_topk<KB>(buf, kept, k, lane);
-    warp_sort(buf, kept, top, true, 0ull, lane);
-    return kept;
-}
-
-// (id << 32 | position) of the kept entries, ascending by id
-__device__ __forceinline__ void index_by_id(const unsigned long long* top, int n, unsigned long long* buf,
-                                            unsigned long long* byid, int lane) {
-    for (int j = lane; j < n; j += 32) buf[j] = ((unsigned long long)(uint32_t)comp_id(top[j]) << 32) | (uint32_t)j;
-    __syncwarp();
-    warp_sort(buf, n, byid, false, ~0ull, lane);
-}
-
-// probability of token x in a kept list indexed by id (0 if not kept)
-__device__ __forceinline__ double prob_of(const unsigned long long* byid, const double* prob, int n, int x) {
-    int lo = 0, hi = n - 1;
-    while (lo <= hi) {
-        const int mid = (lo + hi) >> 1;
-        const int id = (int)(byid[mid] >> 32);
-        if (id == x) return prob[(uint32_t)byid[mid]];
-        if (id < x)
-            lo = mid + 1;
-        else
-            hi = mid - 1;
-    }
-    return 0.0;
-}
-
-// 2^x for x <= 0, with the exponent split (Cody-Waite style) into an integer n
-// and a fraction f in [-1/2, 1/2] in fp64: only f goes through the fp32 exp2,
-// and 2^n is applied exactly, so the result keeps the fp32 exp2's relative
-// accuracy whatever the size of x, at the cost of a few fp64 operations
-// (instead of a full fp64 exponential).  Below 2^-1022 the result is 0.
-__device__ __forceinline__ double exp2_split(double x) {
-    const double n = rint(x);
-    if (n < -1022.0) return 0.0;
-    const double f = x - n;
-    const double pw = __longlong_as_double((long long)(n + 1023.0) << 52);
-    return (double)exp2f((float)f) * pw;
-}
-
-// fp64 normalisation of one sorted kept list by one warp: softmax over the kept
-// logits at temperature T (one-hot if T == 0), then top-p.  prob[j] for j < k.
-template <typename TIn>
-__device__ void normalise_kept(const unsigned long long* top, int k, float Tf, float Pf, double* prob) {
-    const int lane = threadIdx.x & 31;
-    const double T = (double)Tf, P = (double)Pf;
-    if (Tf == 0.0f) {
-        for (int j = lane; j < k; j += 32) prob[j] = (j == 0) ? 1.0 : 0.0;
-        __syncwarp();
-        return;
-    }
-    const double vmax = Elem<TIn>::key_value(comp_key(top[0]));
-    const double c2 = 1.4426950408889634 / T;  // log2(e) / T
-    double s = 0.0;
-    for (int j = lane; j < k; j += 32) {
-        const double w = exp2_split((Elem<TIn>::key_value(comp_key(top[j])) - vmax) * c2);
-        prob[j] = w;
-        s += w;
-    }
-    s = warp_sum(s);
-    const double inv = 1.0 / s;
-    for (int j = lane; j < k; j += 32) prob[j] *= inv;
-    __syncwarp();
-    if (P < 1.0) {  // shortest prefix (prob desc, id asc) whose mass reaches P, crossing token kept
-        double carry = 0.0;
-        int keep = k;
-        for (int c0 = 0; c0 < k; c0 += 32) {
-            const int j = c0 + lane;
-            double x = (j < k) ? prob[j] : 0.0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-                if (lane >= o) x += y;
-            }
-            const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < k && carry + x >= P);
-            if (hit) {
-                keep = c0 + __ffs(hit);
-                break;
-            }
-            carry += __shfl_sync(0xFFFFFFFFu, x, 31);
-        }
-        double s2 = 0.0;
-        for (int j = lane; j < k; j += 32) {
-            if (j >= keep) prob[j] = 0.0;
-            s2 += prob[j];
-        }
-        s2 = warp_sum(s2);
-        __syncwarp();
-        const double inv2 = 1.0 / s2;
-        for (int j = lane; j < keep; j += 32) prob[j] *= inv2;
-    }
-    __syncwarp();
-}
-
-// One row of a unit, by one warp: exact top-k, normalisation (softmax at T,
-// then top-p) and the index by token id.
-template <typename TIn>
-__device__ void combine_row(const Args& a, const SeqInfo& si, int unit, int r, CombPair& sm, int lane) {
-    const uint32_t slot = si.row_off + (r == 0 ? (uint32_t)unit : (uint32_t)si.gamma + 1u + (uint32_t)unit);
-    const int kk = row_topk<Elem<TIn>::KB>(a, slot, si.k, sm.buf[r], sm.top[r], lane);  // ties to the lower id
-    // a row without a finite logit (non-finite ones are already flagged)
-    const uint32_t ninf_key = Elem<TIn>::key(Elem<TIn>::kNegInfBits);
-    const bool dead = kk < 1 || comp_key(sm.top[r][0]) <= ninf_key;
-    if (!dead) {
-        normalise_kept<TIn>(sm.top[r], kk, si.T, si.P, sm.prob[r]);
-        index_by_id(sm.top[r], kk, sm.buf[r], sm.byid[r], lane);
-    }
-    if (lane == 0) sm.kept[r] = dead ? -1 : kk;
-    __syncwarp();
-}
-
-// The rest of a unit, by the pair's first warp once both rows are done.
-template <typename TIn>
-__device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, CombPair& sm, int lane) {
-    const int G = a.G;
-    const bool pair = unit < si.gamma;
-    const int kt = sm.kept[0], kd = pair ? sm.kept[1] : 0;
-    if (kt < 0 || kd < 0) {
-        if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
-        unit_finished_warp(a, b, lane);
-        return;
-    }
-
-    // acceptance test u * q(x) < p(x)
-    int accept = 0;
-    if (pair) {
-        const int x = a.draft_tokens[(size_t)b * G + unit];
-        const double px = prob_of(sm.byid[0], sm.prob[0], kt, x);
-        const double qx = prob_of(sm.byid[1], sm.prob[1], kd, x);
-        const double u = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 0u);
-        accept = (u * qx < px) ? 1 : 0;
-    }
-
-    // alpha_i = sum_x min(p, q) and the residual weights, in ascending token id
-    // over the target's kept ids (an id kept only by the draft has p = 0)
-    double rr[kStreamMaxK / 32];
-    double alpha = 0.0, Z = 0.0, Zp = 0.0;
-#pragma unroll
-    for (int m = 0; m < kStreamMaxK / 32; ++m) {
-        const int j = lane + 32 * m;
-        rr[m] = 0.0;
-        if (j < kt) {
-            const unsigned long long e = sm.byid[0][j];
-            const double p = sm.prob[0][(uint32_t)e];
-            const double q = pair ? prob_of(sm.byid[1], sm.prob[1], kd, (int)(e >> 32)) : 0.0;
-            alpha += fmin(p, q);
-            rr[m] = fmax(p - q, 0.0);  // bonus: q_{gamma+1} := 0
-            Z += rr[m];
-            Zp += p;
-        }
-    }
-    alpha = warp_sum(alpha);
-    Z = warp_sum(Z);
-    const bool use_p = !(Z > 0.0);  // p <= q everywhere: fall back to p
-    if (use_p) {
-        Z = warp_sum(Zp);
-#pragma unroll
-        for (int m = 0; m < kStreamMaxK / 32; ++m) {
-            const int j = lane + 32 * m;
-            rr[m] = j < kt ? sm.prob[0][(uint32_t)sm.byid[0][j]] : 0.0;
-        }
-    }
-    // inverse CDF: the first id whose running sum passes v
-    const double v = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 1u) * Z;
-    int token = -1, last_pos = -1;
-    double carry = 0.0;
-#pragma unroll
-    for (int m = 0; m < kStreamMaxK / 32; ++m) {
-        const int c0 = 32 * m;
-        if (c0 >= kt || token >= 0) break;
-        const int j = c0 + lane;
-        const double r = rr[m];
-        double x = r;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-            if (lane >= o) x += y;
-        }
-        const unsigned pos = __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0);
-        if (pos) last_pos = c0 + 31 - __clz(pos);
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0 && carry + x > v);
-        if (hit) token = (int)(sm.byid[0][c0 + __ffs(hit) - 1] >> 32);
-        carry += __shfl_sync(0xFFFFFFFFu, x, 31);
-    }
-    if (token < 0 && last_pos >= 0) token = (int)(sm.byid[0][last_pos] >> 32);
-
-    if (lane == 0) {
-        if (pair) {
-            a.alpha[(size_t)b * G + unit] = (float)alpha;
-            a.unit_acc[(size_t)b * G + unit] = accept;
-            if (a.pos_accept) a.pos_accept[(size_t)b * G + unit] = accept;
-        }
-        a.unit_tok[(size_t)b * (G + 1) + unit] = token;
-        if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + unit] = token;
-    }
-    if (a.p_out)
-        for (int j = lane; j < kt; j += 32)
-            a.p_out[((size_t)b * (G + 1) + unit) * a.V + comp_id(sm.top[0][j])] = (float)sm.prob[0][j];
-    if (a.q_out && pair)
-        for (int j = lane; j < kd; j += 32)
-            a.q_out[((size_t)b * G + unit) * a.V + comp_id(sm.top[1][j])] = (float)sm.prob[1][j];
-    unit_finished_warp(a, b, lane);
-}
-
-// named barrier of warp pair pr (ids 1 and 2; the ids are constants so the
-// kernel holds only the barriers it uses)
-__device__ __forceinline__ void pair_sync(int pr) {
-    if (pr == 0)
-        asm volatile("bar.sync 1, 64;" ::: "memory");
-    else
-        asm volatile("bar.sync 2, 64;" ::: "memory");
-}
-
-// a warp pair per unit (target row i with draft row i, or the bonus row alone):
-// the two rows are selected and normalised at the same time
-template <typename TIn>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(Args a) {
-    extern __shared__ __align__(16) uint8_t comb_raw[];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int pr = wid >> 1, r = wid & 1;
-    CombPair& sm = reinterpret_cast<CombPair*>(comb_raw)[pr];
-    constexpr int kPairs = kCombineWarps / 2;
-    grid_dependency_wait();  // the select kernel's candidate lists
-    grid_dependents_go();
-    const uint32_t n_units = a.counts[kCntStreamUnits];
-    const bool failed = a.counts[kCntError] != 0u;
-    // both warps of a pair walk the same units, so they meet at the same barriers
-    for (uint32_t w = blockIdx.x * kPairs + pr; w < n_units; w += gridDim.x * kPairs) {
-        const uint32_t item = a.stream_units[w];
-        const int b = (int)(item >> 8), unit = (int)(item & 0xFFu);
-        const SeqInfo si = a.seq[b];
-        if (failed) {  // a select CTA gave up waiting: no result of this call can be trusted
-            if (r == 0) {
-                if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_INTERNAL);
-                unit_finished_warp(a, b, lane);
-            }
-            continue;
-        }
-        if (r == 0 || unit < si.gamma) combine_row<TIn>(a, si, unit, r, sm, lane);
-        pair_sync(pr);
-        if (r == 0) combine_unit<TIn>(a, b, unit, si, sm, lane);
-        pair_sync(pr);  // the rows may be rebuilt
-    }
-}
-
-// ---------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------
 namespace {
 template <typename TIn, bool TMA>
 cudaError_t launch_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) {
     auto sel = select_kernel<TIn, TMA>;
-    auto comb = combine_kernel<TIn>;
     const int smem = (int)sizeof(SelSmem);
     static const bool attr_ok = cudaFuncSetAttribute(sel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
                                 cudaSuccess;
@@ -1421,19 +936,7 @@ cudaError_t launch_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) 
     cudaError_t e = launch_pdl(sel, dim3((unsigned)grid), dim3(kSelThreads), (size_t)smem, s, a);
     if (e != cudaSuccess) return e;
     if (ev && ev[1]) cudaEventRecord((cudaEvent_t)ev[1], s);
-    const int csmem = (int)((kCombineWarps / 2) * sizeof(CombPair));
-    static const bool cattr_ok = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem) ==
-                                 cudaSuccess;
-    if (!cattr_ok) return cudaErrorInvalidValue;
-    static const int cocc = [&] {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, comb, kCombineThreads, csmem) != cudaSuccess) n = 1;
-        return n > 0 ? n : 1;
-    }();
-    long long cgrid = ((long long)a.B * (a.G + 1) + kCombineWarps / 2 - 1) / (kCombineWarps / 2);
-    if (cgrid > (long long)sms * cocc) cgrid = (long long)sms * cocc;
-    if (cgrid < 1) cgrid = 1;
-    return launch_pdl(comb, dim3((unsigned)cgrid), dim3(kCombineThreads), (size_t)csmem, s, a);
+    return launch_combine_kernel(sizeof(TIn) == 2 ? SV_BF16 : SV_F32, a, sms, s);
 }
 }  // namespace
 
