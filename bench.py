@@ -33,9 +33,9 @@ METRIC = "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 
 UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
 # kernels one spec_verify call launches: plan, select (streaming top-k), combine,
-# the unfiltered whole-row kernel and the dense cluster kernel (a kernel whose
-# path no row takes exits at once)
-LAUNCHES_PER_STEP = 5
+# the whole-row kernel of rows without top-k and its per-unit tail, and the
+# dense cluster kernel (a kernel whose path no row takes exits at once)
+LAUNCHES_PER_STEP = 6
 # sources of the select kernel, whose DRAM traffic profiles/traffic.json records
 KERNEL_SOURCES = ("speculative_decoding_verification_20_gb300/csrc/sv_stream.cu",
                   "speculative_decoding_verification_20_gb300/csrc/sv_keys.cuh",

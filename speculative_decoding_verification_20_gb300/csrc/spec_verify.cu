@@ -271,6 +271,9 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
     a.counts = (uint32_t*)(ws + L.counts);
     a.cand = (unsigned long long*)(ws + L.cand);
     a.cand_cnt = (uint32_t*)(ws + L.cand_cnt);
+    a.free_rec = (FreeRec*)(ws + L.free_rec);
+    a.free_blk = (float*)(ws + L.free_blk);
+    a.free_nblk = L.free_nblk;
 
     const size_t es = dtype == SV_BF16 ? 2 : 4;
     if (p_out && cudaMemsetAsync(p_out, 0, sizeof(float) * (size_t)B * (gamma_max + 1) * V, s) != cudaSuccess)

@@ -8,6 +8,7 @@
 // ascending token id) ("Fast Inference from Transformers via Speculative
 // Decoding" review page, Algorithm 1; "Speculative decoding: the art of
 // guessing well", section 投机采样).
+#include "sv_cf.cuh"
 #include "sv_keys.cuh"
 #include "sv_warp_sort.cuh"
 
@@ -173,33 +174,6 @@ __device__ __forceinline__ double exp2_split(double x) {
     const double f = x - n;
     const double pw = __longlong_as_double((long long)(n + 1023.0) << 52);
     return (double)exp2f((float)f) * pw;
-}
-
-// compensated fp32 value s - c: sums of fp32 terms kept to about fp32
-// rounding of the total, whatever the number of terms
-struct CF {
-    float s, c;
-};
-__device__ __forceinline__ CF cf_add(CF a, CF b) {  // exact two-sum of the heads
-    const float t = a.s + b.s;
-    const float bb = t - a.s;
-    const float e = (a.s - (t - bb)) + (b.s - bb);
-    return CF{t, (a.c + b.c) - e};
-}
-__device__ __forceinline__ float cf_val(CF a) { return a.s - a.c; }
-__device__ __forceinline__ CF warp_cf_sum(CF a) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        a = cf_add(a, CF{__shfl_xor_sync(0xFFFFFFFFu, a.s, o), __shfl_xor_sync(0xFFFFFFFFu, a.c, o)});
-    return a;
-}
-__device__ __forceinline__ CF warp_cf_scan(CF a, int lane) {  // inclusive, in lane order
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const CF y{__shfl_up_sync(0xFFFFFFFFu, a.s, o), __shfl_up_sync(0xFFFFFFFFu, a.c, o)};
-        if (lane >= o) a = cf_add(y, a);
-    }
-    return a;
 }
 
 // Unnormalised weight 2^((v - vmax) * log2(e) / T) of a kept logit.

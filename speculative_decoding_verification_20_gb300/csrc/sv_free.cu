@@ -1,30 +1,44 @@
-// sv_free.cu -- whole-row path of unfiltered sequences (no top-k, no top-p,
-// temperature > 0).
+// sv_free.cu -- whole-row path of sequences with no top-k and temperature > 0
+// (top-p or no filter at all).
 //
-// A unit is (target row i, draft row i) for i <= gamma_b, or the bonus unit
-// (target row gamma_b+1 alone, q := 0).  With no filter, p and q are plain
-// softmaxes of the whole vocabulary at temperature T ("Fast Inference from
-// Transformers via Speculative Decoding" review page, section "Method:
-// Speculative Decoding"), and each unit needs:
-//   - the normaliser of each row (pass 1: online maximum and sum of exp),
+// A unit is (target row i, draft row i) for i < gamma_b, or the bonus unit
+// (target row gamma_b alone, q := 0).  p and q are softmaxes of the whole
+// vocabulary at temperature T, cut to the nucleus when top-p < 1 ("Fast
+// Inference from Transformers via Speculative Decoding" review page, section
+// "Method: Speculative Decoding"), and each unit needs:
+//   - the normaliser of each row (online maximum and sum of exp),
+//   - for top-p < 1, the last token of each row's nucleus (the shortest prefix,
+//     by probability descending then id ascending, whose mass reaches P),
 //   - alpha = sum_x min(p, q) and the residual weights r = max(0, p - q)
-//     (p for the bonus row), summed per tile (pass 2),
+//     (p for the bonus row),
 //   - the acceptance test u * q(x) < p(x) of the draft token
 //     ("Speculative decoding: the art of guessing well", section 投机采样),
-//   - the residual / bonus draw: v = u * sum r, the tile where the running sum
-//     of r passes v, then the token inside it (a re-read of that one tile).
+//   - the residual / bonus draw: v = u * sum r and the first token id at which
+//     the running sum of r passes v.
 //
 // free_kernel (persistent, 2 CTAs per SM, 7 consumer warps + 1 producer warp)
 //   The producer claims units from a global counter and streams each unit's
-//   rows twice through a 3-stage ring (a stage holds a 14 KB segment of each
-//   row) by TMA bulk copies: pass 1 reads HBM, pass 2 reads the same bytes
-//   again while they are still in L2.  Consumers work on 16-byte vectors in
-//   registers; per-thread sums are Kahan-compensated fp32, warp sums use an
-//   exact two-sum, and sums across warps and tiles are fp64.
-//   Every wait (ring and the consumers' own barrier) is bounded (2 s); on a
-//   timeout the CTA records kCntError and the affected sequences are marked.
+//   rows through a 3-stage ring (a stage holds a 14 KB segment of each row) by
+//   TMA bulk copies: pass 0 for the row statistics, passes 1-3 for the nucleus
+//   cut when top-p < 1, and the final pass for alpha and the residual weights.
+//   Every pass after the first reads the rows again while they are in L2.
+//   Consumer warp w owns the contiguous 2 KB block w of each segment, so its
+//   sums of r and of p over that block are sums over consecutive token ids;
+//   they go to the unit's record in the workspace with the warp's share of
+//   alpha.  Per-thread sums are Kahan-compensated fp32 and warp sums an exact
+//   two-sum.  Only the row statistics need a barrier of the consumer warps
+//   (and each nucleus pass one or two); a unit ends without one.
+// free_tail_kernel (a warp per unit, after free_kernel)
+//   Sums the unit's block sums, finds the block where the running sum passes
+//   v, re-reads that 2 KB block of each row to find the token inside it, runs
+//   the acceptance test from the two logits of the draft token and writes the
+//   unit's outputs.
+// Every wait of free_kernel (ring and the consumers' own barrier) is bounded
+// (2 s); on a timeout the CTA records kCntError and the tail kernel marks every
+// sequence of the path as failed.
 #include <type_traits>
 
+#include "sv_cf.cuh"
 #include "sv_finalize.cuh"
 #include "sv_warp_sort.cuh"
 
@@ -32,14 +46,14 @@ namespace sv {
 namespace {
 
 constexpr int kFStages = 3;
-constexpr int kFWarps = 7;  // with the producer, 8 warps: 2 CTAs per SM at up to 128 registers
+constexpr int kFWarps = kFreeWarps;  // with the producer, 8 warps: 2 CTAs per SM at up to 128 registers
 constexpr int kFConsumers = 32 * kFWarps;
 constexpr int kFThreads = kFConsumers + 32;
-constexpr int kFSegBytes = 14336;                     // one row's segment of a stage
-constexpr int kFVec = kFSegBytes / 16 / kFConsumers;  // 16-byte vectors per consumer per segment
-constexpr int kFMaxTiles = (SV_MAX_VOCAB * 4 + kFSegBytes - 1) / kFSegBytes;
+constexpr int kFSegBytes = kFreeSegBytes;
+constexpr int kFVec = kFreeBlockBytes / 16 / 32;  // 16-byte vectors per lane per segment (4)
 constexpr unsigned long long kFWaitNs = 2000000000ull;
 static_assert(kFVec * 16 * kFConsumers == kFSegBytes, "segment geometry");
+constexpr int kTailWarps = 8;
 
 // nucleus (top-p) cut of a row: probability mass histograms over the distance
 // below the row maximum, d = (max - l) * log2(e) / T, in log2 units
@@ -58,22 +72,15 @@ struct FreeSmem {
     uint64_t full[kFStages];
     uint64_t empty[kFStages];
     uint64_t gsync;
-    int4 hdr[kFStages];             // unit index (-1: no more work), pass, tile, elements
-    float wr[kFMaxTiles][kFWarps];  // pass 2: per tile and warp, sum of the residual weights
-    float wp[kFMaxTiles][kFWarps];  // pass 2: per tile and warp, sum of p (the Z = 0 fallback)
-    float red[kFWarps][8];
-    double bc[4];                   // broadcast of the residual search
-    double st[4];                   // broadcast of the row statistics: Mp, Sp, Mq, Sq
-    int st_dead;
-    unsigned long long h1[2][kNB1];  // per row: coarse mass histogram (2^40 fixed point); then the crossing elements
-    unsigned long long h2[2][kNB2];  // per row: fine mass histogram
-    int nb[2][2];                    // per row: crossing coarse bin, crossing fine bin
-    unsigned long long nbase[2];     // per row: mass before the crossing fine bin
-    int ncnt[2];                     // per row: crossing elements collected
-    uint32_t cut_key[2], cut_id[2];  // per row: the last kept element (key, id)
-    double kmass[2];                 // per row: kept mass
-    int nfall;                       // the unit goes to the cluster kernel
-    int ired[kFWarps][2];
+    int4 hdr[kFStages];               // unit index (-1: no more work), pass, tile, elements
+    float red[2][kFWarps][8];         // per warp: row statistics (by the parity of the CTA's unit count)
+    unsigned long long h1[2][kNB1];   // per row: coarse mass histogram (2^40 fixed point); then the crossing elements
+    unsigned long long h2[2][kNB2];   // per row: fine mass histogram
+    int nb[2][2];                     // per row: crossing coarse bin, crossing fine bin
+    unsigned long long nbase[2];      // per row: mass before the crossing fine bin
+    int ncnt[2];                      // per row: crossing elements collected
+    uint32_t cut_key[2], cut_id[2];   // per row: the last kept element (key, id)
+    float kinv[2];                    // per row: 1 / (sum x kept mass); -1: too many ties at the cut
 };
 
 // ---------------------------------------------------------------------------
@@ -327,17 +334,34 @@ __device__ __forceinline__ void warp_online(const Online& o, float c, float* wm,
     }
     *ws = warp_ksum(k);
 }
-__device__ __forceinline__ void combine_online(const FreeSmem& sm, int col, float c, float* M, double* S) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, sm.red[w][col]);
-    double s = 0.0;
-    if (m > -INFINITY)
-#pragma unroll
-        for (int w = 0; w < kFWarps; ++w)
-            if (sm.red[w][col] > -INFINITY) s += (double)sm.red[w][col + 1] * (double)fex2((sm.red[w][col] - m) * c);
+// Statistics of one row over all consumer warps, computed by every warp from
+// the seven warps' (maximum, rescaled sum) pairs in red[w][col], [col + 1]:
+// lane w rescales warp w's sum to the common maximum, and the warp adds them
+// with a compensated sum.  M = -inf when the row has no finite logit.
+__device__ __forceinline__ void combine_stats(const float (*red)[8], int col, float c, int lane, float* M, float* S) {
+    const float wm = lane < kFWarps ? red[lane][col] : -INFINITY;
+    const float m = warp_maxf(wm);
+    float x = 0.0f;
+    if (m > -INFINITY && wm > -INFINITY) x = red[lane][col + 1] * fex2((wm - m) * c);
     *M = m;
-    *S = s;
+    *S = cf_val(warp_cf_sum(CF{x, 0.0f}));
+}
+
+// 2^((l - M) * c) to about fp32 rounding for any l <= M, where c = chi + clo
+// is log2(e) / T as a float pair: the difference is formed exactly (two-sum),
+// the product with c by an FMA two-product, the integer part n is applied
+// exactly and only the fraction f in [-1/2, 1/2] goes through exp2f.  Results
+// below 2^-126 are 0.  Used for the two probabilities of the acceptance test.
+__device__ __forceinline__ float exp2_prod(float l, float M, float chi, float clo) {
+    const float d = l - M;
+    const float p = d * chi;
+    const float n = rintf(p);
+    if (!(n >= -126.0f)) return 0.0f;  // also l = -inf
+    const float bb = d - l;
+    const float dlo = (l - (d - bb)) + (-M - bb);  // l - M = d + dlo exactly
+    const float e = fmaf(d, chi, -p);               // d * chi = p + e exactly
+    const float f = (p - n) + (e + fmaf(d, clo, dlo * chi));
+    return exp2f(f) * __int_as_float((int)(n + 127.0f) << 23);
 }
 
 // ---------------------------------------------------------------------------
@@ -439,12 +463,13 @@ __device__ bool warp_cut(unsigned long long* list, int n, unsigned long long bas
     return true;
 }
 
-// One tile of a nucleus pass for row r (max M, 1/sum inv): pass 1 adds the
+// One tile of a nucleus pass for row r (max M, 1/sum inv); the thread holds the
+// vectors vbase + 32 i of the segment.  Pass 1 adds the
 // masses to the coarse histogram, pass 2 those of the crossing coarse bin to
 // the fine histogram, pass 3 collects the elements of the crossing fine bin.
 template <typename TIn>
-__device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVec], int n, int t, int col, int pass,
-                                             int r, float M, float c, float inv) {
+__device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVec], int n, int vbase, int col,
+                                             int pass, int r, float M, float c, float inv) {
     using F = FE<TIn>;
     const float s1 = (float)kNB1 / kNDmax;
     const float s2 = (float)kNB2 * (float)kNB1 / kNDmax;
@@ -453,7 +478,7 @@ __device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVe
     const float d1 = (float)b1 * (kNDmax / (float)kNB1);
 #pragma unroll
     for (int i = 0; i < kFVec; ++i) {
-        const int e0 = (i * kFConsumers + t) * F::VEC;
+        const int e0 = (vbase + 32 * i) * F::VEC;
         const int valid = min(F::VEC, n - e0);
         if (valid <= 0) continue;
         float x[F::VEC];
@@ -485,7 +510,6 @@ template <typename TIn, bool TMA>
 __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
     using F = FE<TIn>;
     constexpr int TS = kFSegBytes / (int)sizeof(TIn);  // elements per segment (tile)
-    constexpr int EPT = TS / kFConsumers;              // contiguous elements per thread in a re-read
     extern __shared__ __align__(128) uint8_t fsm_raw[];
     FreeSmem& sm = *reinterpret_cast<FreeSmem*>(fsm_raw);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -572,21 +596,32 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
         return;
     }
 
+
     // ------------------------------ consumers ------------------------------
     int stage = 0;
     uint32_t ph = 0;
     FSync g{0u, true};
-    int b = 0, u = 0;
+    const int vbase = warp * (32 * kFVec) + lane;  // this thread's vectors of a segment: vbase + 32 i
+    const size_t nblk = (size_t)a.free_nblk;
+    int b = 0, u = 0, par = 1;
     bool pair = false, nf = false, dead = false;
-    float c = 1.0f;
-    Online op, oq;
-    float Mp = 0.0f, Mq = 0.0f, invp = 0.0f, invq = 0.0f;
-    double Sp = 0.0, Sq = 0.0;
-    KSum alpha{0.0f, 0.0f};
     bool nuc = false, fall = false;  // top-p < 1; the unit goes to the cluster kernel
-    float Pf = 1.0f, invp2 = 0.0f, invq2 = 0.0f;
+    float c = 1.0f, Pf = 1.0f;
+    Online op, oq;
+    float Mp = 0.0f, Mq = 0.0f, Sp = 0.0f, Sq = 0.0f, invp = 0.0f, invq = 0.0f, invp2 = 0.0f, invq2 = 0.0f;
     unsigned long long cutp = 0ull, cutq = 0ull;  // last kept element of each row (0: keep all)
-    double Kp = 1.0, Kq = 1.0;                    // kept mass of each row
+    KSum alpha{0.0f, 0.0f};
+    // the unit's record for the tail kernel (one thread writes it)
+    auto write_rec = [&](int w, uint32_t flags) {
+        FreeRec& R = a.free_rec[w];
+        R.Mp = Mp;
+        R.Mq = Mq;
+        R.invp = invp2;
+        R.invq = invq2;
+        R.cutp = cutp;
+        R.cutq = cutq;
+        R.flags = flags;
+    };
     while (true) {
         if (!__all_sync(0xFFFFFFFFu, fbar_wait(&sm.full[stage], ph))) {
             g.ok = false;
@@ -607,19 +642,19 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
             Pf = si.P;
             fall = false;
             cutp = cutq = 0ull;
-            Kp = Kq = 1.0;
             op.init();
             oq.init();
             nf = false;
             alpha = KSum{0.0f, 0.0f};
+            par ^= 1;
         }
         uint4 vp[kFVec], vq[kFVec];
         const uint4* sp4 = reinterpret_cast<const uint4*>(sm.buf[stage][0]);
         const uint4* sq4 = reinterpret_cast<const uint4*>(sm.buf[stage][1]);
 #pragma unroll
         for (int i = 0; i < kFVec; ++i) {
-            vp[i] = sp4[i * kFConsumers + t];
-            vq[i] = pair ? sq4[i * kFConsumers + t] : make_uint4(0u, 0u, 0u, 0u);
+            vp[i] = sp4[vbase + 32 * i];
+            vq[i] = pair ? sq4[vbase + 32 * i] : make_uint4(0u, 0u, 0u, 0u);
         }
         __syncwarp();
         if (lane == 0) fbar_arrive(&sm.empty[stage]);
@@ -629,7 +664,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
         }
 
         if (pass == 0) {
-            // ---- pass 1: online maximum and sum; non-finite logits flag the sequence
+            // ---- pass 0: online maximum and sum; non-finite logits flag the sequence
             if (n == TS) {  // a full tile: every vector of this thread is whole
                 float mp = -INFINITY, mq = -INFINITY;
 #pragma unroll
@@ -642,75 +677,65 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 if (pair) oq.add_tile<TIn>(vq, mq, c);
             } else {
 #pragma unroll
-            for (int i = 0; i < kFVec; ++i) {
-                const int e0 = (i * kFConsumers + t) * F::VEC;
-                const int valid = min(F::VEC, n - e0);
-                if (valid <= 0) continue;
-                if (valid == F::VEC) {
-                    const float mp = F::vmax(vp[i]);
-                    nf |= isnan(mp) || mp == INFINITY;
-                    op.add_full<TIn>(vp[i], mp, c);
-                    if (pair) {
-                        const float mq = F::vmax(vq[i]);
-                        nf |= isnan(mq) || mq == INFINITY;
-                        oq.add_full<TIn>(vq[i], mq, c);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < F::VEC; ++j)
-                        if (j < valid) {
-                            const float x = F::at(vp[i], j);
-                            nf |= isnan(x) || x == INFINITY;
-                            if (pair) {
-                                const float y = F::at(vq[i], j);
-                                nf |= isnan(y) || y == INFINITY;
-                            }
+                for (int i = 0; i < kFVec; ++i) {
+                    const int e0 = (vbase + 32 * i) * F::VEC;
+                    const int valid = min(F::VEC, n - e0);
+                    if (valid <= 0) continue;
+                    if (valid == F::VEC) {
+                        const float mp = F::vmax(vp[i]);
+                        nf |= isnan(mp) || mp == INFINITY;
+                        op.add_full<TIn>(vp[i], mp, c);
+                        if (pair) {
+                            const float mq = F::vmax(vq[i]);
+                            nf |= isnan(mq) || mq == INFINITY;
+                            oq.add_full<TIn>(vq[i], mq, c);
                         }
-                    op.add_part<TIn>(vp[i], valid, c);
-                    if (pair) oq.add_part<TIn>(vq[i], valid, c);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < F::VEC; ++j)
+                            if (j < valid) {
+                                const float x = F::at(vp[i], j);
+                                nf |= isnan(x) || x == INFINITY;
+                                if (pair) {
+                                    const float y = F::at(vq[i], j);
+                                    nf |= isnan(y) || y == INFINITY;
+                                }
+                            }
+                        op.add_part<TIn>(vp[i], valid, c);
+                        if (pair) oq.add_part<TIn>(vq[i], valid, c);
+                    }
                 }
-            }
             }
             if (tile == ntiles - 1) {
                 float wm, ws, wm2, ws2;
                 warp_online(op, c, &wm, &ws);
                 warp_online(oq, c, &wm2, &ws2);
                 const bool wnf = __any_sync(0xFFFFFFFFu, nf);
+                float(*red)[8] = sm.red[par];
                 if (lane == 0) {
-                    sm.red[warp][0] = wm;
-                    sm.red[warp][1] = ws;
-                    sm.red[warp][2] = wm2;
-                    sm.red[warp][3] = ws2;
-                    sm.red[warp][4] = wnf ? 1.0f : 0.0f;
+                    red[warp][0] = wm;
+                    red[warp][1] = ws;
+                    red[warp][2] = wm2;
+                    red[warp][3] = ws2;
+                    red[warp][4] = wnf ? 1.0f : 0.0f;
                 }
-                if (!fsync(sm, g)) break;
-                if (t == 0) {  // one thread combines the warps (fp64) for everyone
-                    float m1, m2;
-                    double s1, s2;
-                    combine_online(sm, 0, c, &m1, &s1);
-                    combine_online(sm, 2, c, &m2, &s2);
-                    bool anynf = false;
-#pragma unroll
-                    for (int w2 = 0; w2 < kFWarps; ++w2) anynf |= sm.red[w2][4] != 0.0f;
-                    sm.st[0] = (double)m1;
-                    sm.st[1] = s1;
-                    sm.st[2] = (double)m2;
-                    sm.st[3] = s2;
-                    // a row with a NaN or +inf logit, or without any finite one
-                    sm.st_dead = anynf || !(m1 > -INFINITY) || (pair && !(m2 > -INFINITY));
-                }
-                if (nuc)  // the coarse histograms start empty
+                // the coarse histograms start empty (nothing reads them between
+                // the previous unit's cut and this barrier)
+                if (nuc)
                     for (int i = t; i < 2 * kNB1; i += kFConsumers) (&sm.h1[0][0])[i] = 0ull;
-                if (!fsync(sm, g)) break;  // red is reused below
-                Mp = (float)sm.st[0];
-                Sp = sm.st[1];
-                Mq = (float)sm.st[2];
-                Sq = sm.st[3];
-                dead = sm.st_dead != 0;
-                invp = dead ? 0.0f : (float)(1.0 / Sp);
-                invq = (dead || !pair) ? 0.0f : (float)(1.0 / Sq);
+                if (!fsync(sm, g)) break;
+                // every warp combines the seven warps' statistics itself; red is
+                // double-buffered by unit, so no second barrier is needed
+                combine_stats(red, 0, c, lane, &Mp, &Sp);
+                combine_stats(red, 2, c, lane, &Mq, &Sq);
+                const bool anynf = __any_sync(0xFFFFFFFFu, lane < kFWarps && red[lane][4] != 0.0f);
+                // a row with a NaN or +inf logit, or without any finite one
+                dead = anynf || !(Mp > -INFINITY) || (pair && !(Mq > -INFINITY));
+                invp = dead ? 0.0f : 1.0f / Sp;
+                invq = (dead || !pair) ? 0.0f : 1.0f / Sq;
                 invp2 = invp;
                 invq2 = invq;
+                if (t == 0 && (dead || !nuc)) write_rec(w, dead ? kRecDead : 0u);
             }
             continue;
         }
@@ -718,8 +743,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
         if (pass < kPassFinal) {
             // ---- nucleus passes: the last kept token of each row (top-p < 1)
             if (dead) continue;
-            nucleus_tile<TIn>(sm, vp, n, t, col, pass, 0, Mp, c, invp);
-            if (pair) nucleus_tile<TIn>(sm, vq, n, t, col, pass, 1, Mq, c, invq);
+            nucleus_tile<TIn>(sm, vp, n, vbase, col, pass, 0, Mp, c, invp);
+            if (pair) nucleus_tile<TIn>(sm, vq, n, vbase, col, pass, 1, Mq, c, invq);
             if (tile != ntiles - 1) continue;
             if (!fsync(sm, g)) break;
             const unsigned long long target = (unsigned long long)((double)Pf * (double)kMassScale);
@@ -751,7 +776,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                     if (lane == 0) {
                         sm.cut_key[r] = ck;
                         sm.cut_id[r] = ci;
-                        sm.kmass[r] = ok ? K : -1.0;
+                        sm.kinv[r] = ok ? (float)(1.0 / ((double)(r == 0 ? Sp : Sq) * K)) : -1.0f;
                     }
                 }
             }
@@ -760,26 +785,28 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
             if (pass == 2 && t < 2) sm.ncnt[t] = 0;
             if (!fsync(sm, g)) break;
             if (pass == 3) {
-                fall = sm.kmass[0] < 0.0 || (pair && sm.kmass[1] < 0.0);
+                fall = sm.kinv[0] < 0.0f || (pair && sm.kinv[1] < 0.0f);
                 if (!fall) {
                     cutp = ((unsigned long long)sm.cut_key[0] << 32) | (unsigned long long)(~sm.cut_id[0]);
-                    Kp = sm.kmass[0];
-                    invp2 = (float)(1.0 / (Sp * Kp));
+                    invp2 = sm.kinv[0];
                     if (pair) {
                         cutq = ((unsigned long long)sm.cut_key[1] << 32) | (unsigned long long)(~sm.cut_id[1]);
-                        Kq = sm.kmass[1];
-                        invq2 = (float)(1.0 / (Sq * Kq));
+                        invq2 = sm.kinv[1];
                     }
-                } else if (t == 0) {  // too many logits at the cut to sort here: the cluster kernel takes the unit
-                    const uint32_t slot = atomicAdd(&a.counts[kCntDenseUnits], 1u);
-                    a.dense_units[slot] = a.free_units[w];
+                }
+                if (t == 0) {
+                    write_rec(w, fall ? kRecFall : 0u);
+                    if (fall) {  // too many logits at the cut to sort here: the cluster kernel takes the unit
+                        const uint32_t slot = atomicAdd(&a.counts[kCntDenseUnits], 1u);
+                        a.dense_units[slot] = a.free_units[w];
+                    }
                 }
             }
             continue;
         }
-        if (fall) continue;  // the cluster kernel finishes this unit
+        if (fall || dead) continue;  // nothing more to sum (the cluster kernel, or the tail kernel's flags)
 
-        // ---- pass 2: alpha, residual weights, per-tile sums (and the debug outputs)
+        // ---- final pass: alpha and the residual weights, summed per block
         float tr = 0.0f, tp = 0.0f;
         // the per-element work, specialised on whether the rows are filtered (one
         // branch per tile instead of a test per element)
@@ -787,7 +814,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
             constexpr bool CUT = decltype(cut_on)::value;
 #pragma unroll
             for (int i = 0; i < kFVec; ++i) {
-                const int e0 = (i * kFConsumers + t) * F::VEC;
+                const int e0 = (vbase + 32 * i) * F::VEC;
                 const int valid = min(F::VEC, n - e0);
                 if (valid <= 0) continue;
                 float xp[F::VEC], xq[F::VEC];
@@ -820,7 +847,6 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
 #pragma unroll
                     for (int j = 0; j < F::VEC; ++j)
                         if (j < valid) tp += kept_prob<CUT>(xp[j], (uint32_t)(col + e0 + j), Mp, c, invp2, cutp);
-                    tr = tp;
                 }
                 alpha.add(am);
                 if (a.p_out || a.q_out) {  // debug outputs
@@ -837,204 +863,194 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 }
             }
         };
-        if (!dead) {
-            if (nuc)
-                final_tile(std::true_type{});
-            else
-                final_tile(std::false_type{});
+        if (nuc)
+            final_tile(std::true_type{});
+        else
+            final_tile(std::false_type{});
+        // this warp's block of the tile: sums of r (pairs only) and of p, in the record
+        const float wtr = warp_ksum(KSum{tr, 0.0f}), wtp = warp_ksum(KSum{tp, 0.0f});
+        if (lane == 0) {
+            float* blk = a.free_blk + (size_t)w * 2 * nblk + (size_t)tile * kFWarps + warp;
+            if (pair) blk[0] = wtr;
+            blk[nblk] = wtp;
         }
-        {
-            const float wtr = warp_ksum(KSum{tr, 0.0f}), wtp = warp_ksum(KSum{tp, 0.0f});
-            if (lane == 0) {
-                sm.wr[tile][warp] = wtr;
-                sm.wp[tile][warp] = wtp;
-            }
-        }
-        if (tile != ntiles - 1) continue;
-
-        // ---- end of the unit ----
-        {
+        if (tile == ntiles - 1 && pair) {
             const float wa = warp_ksum(alpha);
-            if (lane == 0) sm.red[warp][5] = wa;
+            if (lane == 0) a.free_rec[w].alpha[warp] = wa;
         }
-        if (!fsync(sm, g)) break;  // every tile sum is in
-        if (warp == 0 && !dead) {
-            const double ur = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 1u);
-            // total residual mass; fall back to p when it is zero (p <= q everywhere)
-            double Z = 0.0, Zp = 0.0;
-            for (int tl = lane; tl < ntiles; tl += 32) {
-                double zr = 0.0, zp = 0.0;
-#pragma unroll
-                for (int w2 = 0; w2 < kFWarps; ++w2) {
-                    zr += (double)sm.wr[tl][w2];
-                    zp += (double)sm.wp[tl][w2];
-                }
-                Z += zr;
-                Zp += zp;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                Z += __shfl_xor_sync(0xFFFFFFFFu, Z, o);
-                Zp += __shfl_xor_sync(0xFFFFFFFFu, Zp, o);
-            }
-            const bool use_p = !(Z > 0.0);
-            const double Zt = use_p ? Zp : Z;
-            const double v = ur * Zt;
-            // the tile whose running sum passes v (else the last tile with weight)
-            int found = -1, lastpos = -1;
-            double carry = 0.0, before = 0.0;
-            for (int c0 = 0; c0 < ntiles && found < 0; c0 += 32) {
-                const int tl = c0 + lane;
-                double x = 0.0;
-                if (tl < ntiles)
-#pragma unroll
-                    for (int w2 = 0; w2 < kFWarps; ++w2) x += (double)(use_p ? sm.wp[tl][w2] : sm.wr[tl][w2]);
-                const double own = x;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-                    if (lane >= o) x += y;
-                }
-                const unsigned pos = __ballot_sync(0xFFFFFFFFu, tl < ntiles && own > 0.0);
-                if (pos) {
-                    lastpos = c0 + 31 - __clz(pos);
-                    before = carry + __shfl_sync(0xFFFFFFFFu, x - own, 31 - __clz(pos));
-                }
-                const unsigned hit = __ballot_sync(0xFFFFFFFFu, tl < ntiles && own > 0.0 && carry + x > v);
-                if (hit) {
-                    const int l = __ffs(hit) - 1;
-                    found = c0 + l;
-                    before = carry + __shfl_sync(0xFFFFFFFFu, x - own, l);
-                }
-                carry += __shfl_sync(0xFFFFFFFFu, x, 31);
-            }
-            if (lane == 0) {
-                sm.bc[0] = (double)(found >= 0 ? found : lastpos);
-                sm.bc[1] = before;
-                sm.bc[2] = v - before;  // v within the chosen tile
-                sm.bc[3] = use_p ? 1.0 : 0.0;
-            }
-        }
-        if (!fsync(sm, g)) break;
-        int token = -1;
-        if (!dead) {
-            const int tsel = (int)sm.bc[0];
-            const float vrel = (float)sm.bc[2];
-            const bool use_p = sm.bc[3] != 0.0;
-            // re-read the tile: thread t takes EPT contiguous elements
-            const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
-            const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
-            const int e0 = (tsel < 0 ? 0 : tsel) * TS + t * EPT;
-            const int e1 = min(V, e0 + EPT);
-            float rv[EPT];
-            float own = 0.0f;
-            int last = -1;
-#pragma unroll
-            for (int j = 0; j < EPT; ++j) {
-                rv[j] = 0.0f;
-                if (tsel >= 0 && e0 + j < e1) {
-                    const float p = kept_prob<true>(F::load(trow, e0 + j), (uint32_t)(e0 + j), Mp, c, invp2, cutp);
-                    const float q =
-                        pair ? kept_prob<true>(F::load(drow, e0 + j), (uint32_t)(e0 + j), Mq, c, invq2, cutq) : 0.0f;
-                    rv[j] = (pair && !use_p) ? resid_f(p, q) : p;
-                    own += rv[j];
-                    if (rv[j] > 0.0f) last = e0 + j;
-                }
-            }
-            // running sums within the tile (from its start), compensated fp32:
-            // inclusive warp scan of the thread sums, then the warp bases
-            KSum x{own, 0.0f};
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float ys = __shfl_up_sync(0xFFFFFFFFu, x.s, o);
-                const float yc = __shfl_up_sync(0xFFFFFFFFu, x.c, o);
-                if (lane >= o) {
-                    const float tt = x.s + ys;
-                    const float bb = tt - x.s;
-                    const float e = (x.s - (tt - bb)) + (ys - bb);
-                    x.c = (x.c + yc) - e;
-                    x.s = tt;
-                }
-            }
-            float* wtot = sm.wr[0];  // the tile sums are no longer needed
-            __syncwarp();
-            if (lane == 31) {
-                wtot[2 * warp] = x.s;
-                wtot[2 * warp + 1] = x.c;
-            }
-            if (!fsync(sm, g)) break;
-            KSum pre{0.0f, 0.0f};
-            for (int w2 = 0; w2 < warp; ++w2) {
-                pre.add(wtot[2 * w2]);
-                pre.add(-wtot[2 * w2 + 1]);
-            }
-            pre.add(x.s - x.c - own);  // exclusive prefix within the warp
-            int hit = INT_MAX;
-            if (own > 0.0f && (pre.s - pre.c) + own > vrel) {
-                KSum cum = pre;
-#pragma unroll
-                for (int j = 0; j < EPT; ++j)
-                    if (hit == INT_MAX && rv[j] > 0.0f) {
-                        cum.add(rv[j]);
-                        if (cum.s - cum.c > vrel) hit = e0 + j;
-                    }
-            }
-            // the first element passing v over the tile, else its last one with weight
-            int wh = hit, wl = last;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                wh = min(wh, __shfl_xor_sync(0xFFFFFFFFu, wh, o));
-                wl = max(wl, __shfl_xor_sync(0xFFFFFFFFu, wl, o));
-            }
-            if (lane == 0) {
-                sm.ired[warp][0] = wh;
-                sm.ired[warp][1] = wl;
-            }
-            if (!fsync(sm, g)) break;
-            int bh = INT_MAX, bl = -1;
-#pragma unroll
-            for (int w2 = 0; w2 < kFWarps; ++w2) {
-                bh = min(bh, sm.ired[w2][0]);
-                bl = max(bl, sm.ired[w2][1]);
-            }
-            token = bh != INT_MAX ? bh : bl;
-        }
-        if (warp == 0) {
-            if (dead) {
-                if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
-            } else if (lane == 0) {
-                int accept = 0;
-                if (pair) {
-                    // acceptance test u * q(x) < p(x) in fp64 from the logits of x
-                    const int xt = a.draft_tokens[(size_t)b * G + u];
-                    const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
-                    const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
-                    const double T = (double)a.seq[b].T;
-                    const float lpx = F::load(trow, xt), lqx = F::load(drow, xt);
-                    const unsigned long long kx = (unsigned long long)okey32(__float_as_uint(lpx)) << 32 |
-                                                  (unsigned long long)(~(uint32_t)xt);
-                    const unsigned long long kqx = (unsigned long long)okey32(__float_as_uint(lqx)) << 32 |
-                                                   (unsigned long long)(~(uint32_t)xt);
-                    const double px = (cutp != 0ull && kx < cutp) ? 0.0 : exp(((double)lpx - (double)Mp) / T) / (Sp * Kp);
-                    const double qx = (cutq != 0ull && kqx < cutq) ? 0.0 : exp(((double)lqx - (double)Mq) / T) / (Sq * Kq);
-                    const double ua = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 0u);
-                    accept = (ua * qx < px) ? 1 : 0;
-                    double al = 0.0;
-#pragma unroll
-                    for (int w2 = 0; w2 < kFWarps; ++w2) al += (double)sm.red[w2][5];
-                    a.alpha[(size_t)b * G + u] = (float)al;
-                    a.unit_acc[(size_t)b * G + u] = accept;
-                    if (a.pos_accept) a.pos_accept[(size_t)b * G + u] = accept;
-                }
-                a.unit_tok[(size_t)b * (G + 1) + u] = token;
-                if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + u] = token;
-            }
-            unit_finished_warp(a, b, lane);
-        }
-        // the next unit may reuse the shared sums only after warp 0 has read them
-        if (!fsync(sm, g)) break;
     }
     if (!g.ok && lane == 0) atomicOr(&a.counts[kCntError], 1u);
+}
+
+// The residual / bonus draw, the acceptance test and the outputs of the free
+// kernel's units, a warp per unit, from the units' records.
+template <typename TIn>
+__global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
+    using F = FE<TIn>;
+    constexpr int TS = kFSegBytes / (int)sizeof(TIn);       // elements per segment
+    constexpr int BS = kFreeBlockBytes / (int)sizeof(TIn);  // elements per block
+    constexpr int CH = 32 * F::VEC;                         // a block is read in chunks of VEC per lane
+    constexpr int NCH = BS / CH;
+    static_assert(NCH * CH == BS && BS * kFWarps == TS, "block geometry");
+    const int lane = threadIdx.x & 31;
+    grid_dependency_wait();  // the free kernel's records
+    grid_dependents_go();
+    const uint32_t n_units = a.counts[kCntFreeUnits];
+    const bool failed = a.counts[kCntError] != 0u;
+    const int G = a.G, V = a.V, nblk = a.free_nblk;
+    const uint32_t stride = gridDim.x * kTailWarps;
+    for (uint32_t w = blockIdx.x * kTailWarps + (threadIdx.x >> 5); w < n_units; w += stride) {
+        const uint32_t item = a.free_units[w];
+        const int b = (int)(item >> 8), u = (int)(item & 0xFFu);
+        const SeqInfo si = a.seq[b];
+        const bool pair = u < si.gamma;
+        if (failed) {  // a free CTA gave up waiting: no record of this call can be trusted
+            if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_INTERNAL);
+            unit_finished_warp(a, b, lane);
+            continue;
+        }
+        const FreeRec* rec = a.free_rec + w;
+        const uint32_t flags = rec->flags;
+        if (flags & kRecFall) continue;  // the cluster kernel finishes this unit
+        if (flags & kRecDead) {
+            if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+            unit_finished_warp(a, b, lane);
+            continue;
+        }
+        const float Mp = rec->Mp, Mq = rec->Mq, invp2 = rec->invp, invq2 = rec->invq;
+        const unsigned long long cutp = rec->cutp, cutq = rec->cutq;
+        const float c = 1.4426950408889634f / si.T;  // the free kernel's expression
+        const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
+        const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
+
+        // total residual mass; fall back to p when it is zero (p <= q everywhere)
+        const float* br = a.free_blk + (size_t)w * 2 * nblk;
+        const float* bp = br + nblk;
+        CF zr{0.0f, 0.0f}, zp{0.0f, 0.0f};
+        for (int j = lane; j < nblk; j += 32) {
+            if (pair) zr = cf_add(zr, CF{br[j], 0.0f});
+            zp = cf_add(zp, CF{bp[j], 0.0f});
+        }
+        zr = warp_cf_sum(zr);
+        zp = warp_cf_sum(zp);
+        const bool use_p = !pair || !(cf_val(zr) > 0.0f);
+        const float* bs = use_p ? bp : br;
+        const CF zt = use_p ? zp : zr;
+        const double v = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 1u) * ((double)zt.s - (double)zt.c);
+
+        // the block (blocks are in token-id order) whose running sum passes v,
+        // else the last block with weight
+        int blk = -1, lastb = -1;
+        double bef = 0.0, bef_last = 0.0;
+        CF carry{0.0f, 0.0f};
+        for (int c0 = 0; c0 < nblk; c0 += 32) {
+            const int j = c0 + lane;
+            const float x = j < nblk ? bs[j] : 0.0f;
+            const CF inc = cf_add(carry, warp_cf_scan(CF{x, 0.0f}, lane));
+            const double incd = (double)inc.s - (double)inc.c;
+            const double excd = incd - (double)x;
+            const unsigned hit = __ballot_sync(0xFFFFFFFFu, x > 0.0f && incd > v);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                blk = c0 + l;
+                bef = __shfl_sync(0xFFFFFFFFu, excd, l);
+                break;
+            }
+            const unsigned pos = __ballot_sync(0xFFFFFFFFu, x > 0.0f);
+            if (pos) {
+                const int l = 31 - __clz(pos);
+                lastb = c0 + l;
+                bef_last = __shfl_sync(0xFFFFFFFFu, excd, l);
+            }
+            carry = CF{__shfl_sync(0xFFFFFFFFu, inc.s, 31), __shfl_sync(0xFFFFFFFFu, inc.c, 31)};
+        }
+        if (blk < 0) {
+            blk = lastb;
+            bef = bef_last;
+        }
+
+        // the token inside the block: re-read it (each row) and recompute the
+        // free kernel's per-element values; the first id whose running sum
+        // passes v, else the block's last id with weight
+        int token = -1;
+        if (blk >= 0) {
+            const double vrel = v - bef;
+            const int e_start = (blk / kFWarps) * TS + (blk % kFWarps) * BS;
+            const int e_end = min(V, e_start + BS);
+            CF run{0.0f, 0.0f};
+            int lastel = -1;
+            for (int ch = 0; ch < NCH && token < 0; ++ch) {
+                const int e0 = e_start + ch * CH + lane * F::VEC;
+                float rv[F::VEC];
+                float own = 0.0f;
+                int mylast = -1;
+#pragma unroll
+                for (int j = 0; j < F::VEC; ++j) {
+                    const int e = e0 + j;
+                    rv[j] = 0.0f;
+                    if (e < e_end) {
+                        const float p = kept_prob<true>(F::load(trow, e), (uint32_t)e, Mp, c, invp2, cutp);
+                        const float q =
+                            use_p ? 0.0f : kept_prob<true>(F::load(drow, e), (uint32_t)e, Mq, c, invq2, cutq);
+                        rv[j] = use_p ? p : resid_f(p, q);
+                        own += rv[j];
+                        if (rv[j] > 0.0f) mylast = e;
+                    }
+                }
+                lastel = max(lastel, __reduce_max_sync(0xFFFFFFFFu, mylast));
+                const CF inc = cf_add(run, warp_cf_scan(CF{own, 0.0f}, lane));
+                const unsigned hit =
+                    __ballot_sync(0xFFFFFFFFu, own > 0.0f && (double)inc.s - (double)inc.c > vrel);
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    int tk = mylast;  // rounding: the lane's last id with weight
+                    if (lane == l) {
+                        CF cum = cf_add(inc, CF{-own, 0.0f});  // the sum before this lane's ids
+#pragma unroll
+                        for (int j = 0; j < F::VEC; ++j)
+                            if (rv[j] > 0.0f && tk == mylast) {
+                                cum = cf_add(cum, CF{rv[j], 0.0f});
+                                if ((double)cum.s - (double)cum.c > vrel) tk = e0 + j;
+                            }
+                    }
+                    token = __shfl_sync(0xFFFFFFFFu, tk, l);
+                }
+                run = CF{__shfl_sync(0xFFFFFFFFu, inc.s, 31), __shfl_sync(0xFFFFFFFFu, inc.c, 31)};
+            }
+            if (token < 0) token = lastel;
+        }
+
+        // alpha and the acceptance test u * q(x) < p(x), from the two logits of x
+        int accept = 0;
+        float alpha_v = 0.0f;
+        if (pair) {
+            alpha_v = cf_val(warp_cf_sum(CF{lane < kFWarps ? rec->alpha[lane] : 0.0f, 0.0f}));
+            if (lane == 0) {
+                const int xt = a.draft_tokens[(size_t)b * G + u];
+                const float lpx = F::load(trow, xt), lqx = F::load(drow, xt);
+                const double c2 = 1.4426950408889634 / (double)si.T;
+                const float chi = (float)c2, clo = (float)(c2 - (double)chi);
+                const unsigned long long kx =
+                    ((unsigned long long)okey32(__float_as_uint(lpx)) << 32) | (unsigned long long)(~(uint32_t)xt);
+                const unsigned long long kqx =
+                    ((unsigned long long)okey32(__float_as_uint(lqx)) << 32) | (unsigned long long)(~(uint32_t)xt);
+                const double px = kx < cutp ? 0.0 : (double)exp2_prod(lpx, Mp, chi, clo) * (double)invp2;
+                const double qx = kqx < cutq ? 0.0 : (double)exp2_prod(lqx, Mq, chi, clo) * (double)invq2;
+                const double ua = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 0u);
+                accept = (ua * qx < px) ? 1 : 0;
+            }
+        }
+        if (lane == 0) {
+            if (pair) {
+                a.alpha[(size_t)b * G + u] = alpha_v;
+                a.unit_acc[(size_t)b * G + u] = accept;
+                if (a.pos_accept) a.pos_accept[(size_t)b * G + u] = accept;
+            }
+            a.unit_tok[(size_t)b * (G + 1) + u] = token;
+            if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + u] = token;
+        }
+        unit_finished_warp(a, b, lane);
+    }
 }
 
 template <typename TIn, bool TMA>
@@ -1049,15 +1065,19 @@ cudaError_t launch_free_t(const Args& a, int sms, cudaStream_t s, void* const ev
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kFThreads, smem) != cudaSuccess) n = 1;
         return n > 0 ? n : 1;
     }();
-    long long grid = (long long)occ * sms;
     const long long units = (long long)a.B * (a.G + 1);
+    long long grid = (long long)occ * sms;
     if (grid > units) grid = units;
     if (grid < 1) grid = 1;
     if (ev && ev[0]) cudaEventRecord((cudaEvent_t)ev[0], s);
-    const cudaError_t e = launch_pdl(k, dim3((unsigned)grid), dim3(kFThreads), (size_t)smem, s, a);
+    cudaError_t e = launch_pdl(k, dim3((unsigned)grid), dim3(kFThreads), (size_t)smem, s, a);
     if (e != cudaSuccess) return e;
     if (ev && ev[1]) cudaEventRecord((cudaEvent_t)ev[1], s);
-    return cudaSuccess;
+    // the tail: a warp per unit, up to 4 CTAs of 8 warps per SM in flight
+    long long tgrid = (units + kTailWarps - 1) / kTailWarps;
+    if (tgrid > 4LL * sms) tgrid = 4LL * sms;
+    if (tgrid < 1) tgrid = 1;
+    return launch_pdl(free_tail_kernel<TIn>, dim3((unsigned)tgrid), dim3(32 * kTailWarps), 0, s, a);
 }
 
 }  // namespace

@@ -1,22 +1,30 @@
 // sv_internal.cuh -- shared device/host internals of the GB300 verification library.
 //
-// Layout of one call on the GPU (all on the caller's stream, no host sync):
+// Layout of one call on the GPU (all on the caller's stream, no host sync;
+// each kernel after the plan is a programmatic dependent launch):
 //   plan kernel    (1 CTA)  validates the per-sequence parameters, picks a path
 //                           per sequence, zeroes the per-call counters and
 //                           writes the work lists;
-//   select kernel           greedy and top-k <= 256 sequences: every row is cut
-//                           into pieces of up to 8 x 32 KB tiles, streamed once
-//                           from HBM by TMA bulk copies into a shared-memory
-//                           ring; each piece keeps only its exact top-k
-//                           (logit key, token id) candidates;
-//   combine kernel          one CTA per (target row, draft row) unit merges the
-//                           pieces' lists and does the per-position arithmetic
-//                           in fp64 (softmax over the kept logits, top-p,
-//                           alpha, acceptance, residual / bonus draw);
-//   dense kernel            every other sequence: one thread-block cluster holds
-//                           a whole (target row, draft row) unit in registers
-//                           (DSMEM reductions between the CTAs) and does softmax,
-//                           top-k/top-p, alpha, acceptance and the residual draw.
+//   select kernel           top-k <= 256 (and greedy) sequences: rows are cut
+//                           into pieces of up to 10 x 28 KB tiles, streamed
+//                           once from HBM by TMA bulk copies into a shared-
+//                           memory ring; each piece keeps a superset of its
+//                           top-k (logit key, token id) candidates;
+//   combine kernel          a warp pair per (target row, draft row) unit merges
+//                           the pieces' lists into the exact top-k and does the
+//                           per-position arithmetic (softmax over the kept
+//                           logits, top-p, alpha, acceptance, residual draw);
+//   free kernel             sequences with no top-k and temperature > 0 (top-p
+//                           or none): each unit's two rows are streamed through
+//                           a ring by TMA, once for the row statistics, three
+//                           more times for an exact nucleus cut when top-p < 1,
+//                           and once for alpha and the residual weights, summed
+//                           per 2 KB block into a per-unit record;
+//   free tail kernel        a warp per unit of the free kernel: residual draw
+//                           (block search, re-read of one block), acceptance;
+//   dense kernel            every other sequence (large top-k, and units the
+//                           free kernel hands over): one thread-block cluster
+//                           holds a whole unit in registers (DSMEM reductions).
 // The last unit of a sequence to finish writes that sequence's outputs
 // (last-block-done counters; no thread ever waits on another block).
 #pragma once
@@ -39,6 +47,12 @@ constexpr int kStreamMaxK = SV_STREAM_MAX_TOP_K;
 constexpr int kListCap = 512;   // candidates one piece hands to the combine kernel
 constexpr int kSortCap = 2048;  // candidates per row sorted in shared memory by the combine kernel
 constexpr int kDenseThreads = 256;
+// free kernel geometry: a ring stage holds one 14 KB segment of each row of a
+// unit; each of the 7 consumer warps owns a contiguous 2 KB block of it
+constexpr int kFreeWarps = 7;
+constexpr int kFreeSegBytes = 14336;
+constexpr int kFreeBlockBytes = kFreeSegBytes / kFreeWarps;
+static_assert(kFreeBlockBytes * kFreeWarps == kFreeSegBytes && kFreeBlockBytes % 512 == 0, "free block geometry");
 
 // counters at the head of the workspace list area
 enum : int {
@@ -54,6 +68,20 @@ enum : int {
 // streaming top-k path; whole-row cluster path (top-p, large top-k); whole-row
 // path of unfiltered rows (no top-k, no top-p)
 enum : uint32_t { kModeErr = 0, kModeStream = 1, kModeDense = 2, kModeFree = 3 };
+
+// Per-unit record of the free kernel for its tail kernel (one per entry of the
+// free unit list).  flags: kRecDead (a row without a finite logit, or with a
+// NaN / +inf), kRecFall (the unit was handed to the dense kernel).
+enum : uint32_t { kRecDead = 1u, kRecFall = 2u };
+struct FreeRec {
+    float Mp, Mq;                   // row maxima (logits)
+    float invp, invq;               // 1 / (sum x kept mass) of each row
+    unsigned long long cutp, cutq;  // last kept element (okey << 32 | ~id); 0: the row is not cut
+    uint32_t flags;
+    float alpha[kFreeWarps];        // per-warp partial sums of min(p, q)
+    uint32_t pad[4];
+};
+static_assert(sizeof(FreeRec) == 80, "free record size");
 
 // per-sequence plan (32 bytes)
 struct SeqInfo {
@@ -102,12 +130,15 @@ struct Args {
     uint32_t* counts;         // kCnt* above
     unsigned long long* cand; // [stream rows * ppr * kListCap] (key << 32 | ~id), unsorted
     uint32_t* cand_cnt;       // [stream rows * ppr]
+    FreeRec* free_rec;        // [units] by free list index
+    float* free_blk;          // [units][2][free_nblk]: per block sums of r (residual weights) and p
+    int free_nblk;            // blocks per row
 };
 
 struct WsLayout {
     size_t seq, seq_done, seq_status, unit_done, unit_acc, unit_tok, stream_rows, dense_units, stream_units, free_units,
-        counts, cand, cand_cnt, total;
-    int ppr;
+        counts, cand, cand_cnt, free_rec, free_blk, total;
+    int ppr, free_nblk;
 };
 
 __host__ __device__ inline int tile_elems(int dtype) { return kTileBytes / (dtype == SV_BF16 ? 2 : 4); }
@@ -117,6 +148,11 @@ static_assert(((SV_MAX_VOCAB + kTilesPerPiece * (kTileBytes / 4) - 1) / (kTilesP
                       kListCap <=
                   kSortCap,
               "pieces per row times the list cap must fit the combine sort");
+
+__host__ __device__ inline int free_seg_elems(int dtype) { return kFreeSegBytes / (dtype == SV_BF16 ? 2 : 4); }
+__host__ __device__ inline int free_blocks(int V, int dtype) {
+    return (V + free_seg_elems(dtype) - 1) / free_seg_elems(dtype) * kFreeWarps;
+}
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -139,6 +175,9 @@ __host__ __device__ inline WsLayout ws_layout(int B, int G, int V, int dtype) {
     L.counts = o;      o = align_up(o + 64, 256);
     L.cand_cnt = o;    o = align_up(o + 4 * rows * L.ppr, 256);
     L.cand = o;        o = align_up(o + 8 * rows * L.ppr * kListCap, 256);
+    L.free_nblk = free_blocks(V, dtype);
+    L.free_rec = o;    o = align_up(o + sizeof(FreeRec) * units, 256);
+    L.free_blk = o;    o = align_up(o + 4 * units * 2 * (size_t)L.free_nblk, 256);
     L.total = o;
     return L;
 }
