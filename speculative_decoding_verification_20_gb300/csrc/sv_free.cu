@@ -174,6 +174,12 @@ struct FE<__nv_bfloat16> {
     __device__ static float load(const __nv_bfloat16* p, int i) {
         return __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(p)[i] << 16);
     }
+    // the vector as float pairs (element 2k, element 2k + 1)
+    __device__ static void pairs(const uint4& v, float2 (&x)[4]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+    }
 };
 template <>
 struct FE<float> {
@@ -192,6 +198,10 @@ struct FE<float> {
         return __uint_as_float(j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w);
     }
     __device__ static float load(const float* p, int i) { return p[i]; }
+    __device__ static void pairs(const uint4& v, float2 (&x)[2]) {
+        x[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        x[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
 };
 
 // fp32 sum with Kahan compensation: the value is s - c
@@ -224,9 +234,6 @@ __device__ __forceinline__ float warp_maxf(float x) {
     return x;
 }
 
-// Normalised probability of a logit: exp2((l - M) * c) * inv (c = log2(e) / T,
-// M the row's maximum logit, inv = 1 / sum); the same expression serves every
-// pass, so the re-read of a tile reproduces the sums of pass 2 exactly.
 // 2^x by the PTX approximate base-2 exponential (relative error about 2^-22),
 // results below the normal range flushed to zero
 __device__ __forceinline__ float fex2(float x) {
@@ -234,67 +241,90 @@ __device__ __forceinline__ float fex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
-__device__ __forceinline__ float prob_f(float l, float M, float c, float inv) { return fex2((l - M) * c) * inv; }
+__device__ __forceinline__ float2 fex2x2(float2 x) { return make_float2(fex2(x.x), fex2(x.y)); }
+
+// Unnormalised weight of a logit l of a row with maximum M at c = log2(e) / T:
+// 2^(l * c - mc) with mc = fp32(M * c), one FMA (nmc = -mc).  The rounding of
+// mc shifts every exponent of the row by the same amount, so it cancels
+// against the row's sum, which is formed from the same weights; what remains
+// is the FMA's single rounding, relative to l * c - mc.  Every pass, and the
+// tail kernel's re-read, use this expression, so a weight is the same number
+// wherever it is computed.
+__device__ __forceinline__ float row_nmc(float M, float c) { return -(M * c); }
+__device__ __forceinline__ float prob_f(float l, float c, float nmc, float inv) { return fex2(fmaf(l, c, nmc)) * inv; }
 __device__ __forceinline__ float resid_f(float p, float q) { return fmaxf(p - q, 0.0f); }
 // the (top-p renormalised) probability of element id with logit l: zero past
-// the row's last kept element `cut` (cut 0: the row is not filtered)
-// (CUT: the row is filtered; else no test at all)
+// the row's last kept element `cut` (CUT: the row is filtered; else no test at all)
 template <bool CUT>
-__device__ __forceinline__ float kept_prob(float l, uint32_t id, float M, float c, float inv2, unsigned long long cut) {
+__device__ __forceinline__ float kept_prob(float l, uint32_t id, float c, float nmc, float inv2, unsigned long long cut) {
     if (CUT && ((unsigned long long)okey32(__float_as_uint(l)) << 32 | (unsigned long long)(~id)) < cut) return 0.0f;
-    return fex2((l - M) * c) * inv2;
+    return fex2(fmaf(l, c, nmc)) * inv2;
+}
+// is (l, id) at or before the cut element (logit lc, id ic) in (logit desc, id asc) order
+__device__ __forceinline__ bool kept_at(float l, uint32_t id, float lc, uint32_t ic) {
+    return l > lc || (l == lc && id <= ic);
 }
 
-// online softmax state of one row for one thread: running maximum logit m and
-// the compensated sum of exp2((l - m) * c)
+// online softmax state of one row for one thread: running maximum logit m,
+// nmc = -fp32(m * c), and the compensated sum of the weights 2^(l * c + nmc).
+// When the maximum grows the sum is rescaled by 2^(nmc_new - nmc_old), so it
+// stays the sum of the weights at the current nmc.
 struct Online {
-    float m;
+    float m, nmc;
     KSum s;
     __device__ __forceinline__ void init() {
         m = -INFINITY;
+        nmc = 0.0f;
         s = KSum{0.0f, 0.0f};
+    }
+    __device__ __forceinline__ void raise(float vm, float c) {
+        const float n2 = row_nmc(vm, c);
+        const float f = m == -INFINITY ? 0.0f : fex2(n2 - nmc);
+        s.s *= f;
+        s.c *= f;
+        m = vm;
+        nmc = n2;
     }
     // a whole vector; vm is its NaN-propagating maximum (a NaN row is flagged
     // by the caller and its sums are not used)
     template <typename TIn>
     __device__ __forceinline__ void add_full(const uint4& v, float vm, float c) {
         if (!(vm > -INFINITY)) return;  // only -inf here (or NaN)
-        if (vm > m) {
-            const float f = m == -INFINITY ? 0.0f : fex2((m - vm) * c);
-            s.s *= f;
-            s.c *= f;
-            m = vm;
-        }
+        if (vm > m) raise(vm, c);
         float x[FE<TIn>::VEC];
         FE<TIn>::unpack(v, x);
         float acc = 0.0f;
 #pragma unroll
-        for (int j = 0; j < FE<TIn>::VEC; ++j) acc += fex2((x[j] - m) * c);
+        for (int j = 0; j < FE<TIn>::VEC; ++j) acc += fex2(fmaf(x[j], c, nmc));
         s.add(acc);
     }
     // all kFVec vectors of a full tile at once: one rescale, then independent
-    // exponentials summed pairwise; vm is the NaN-propagating maximum of them all
+    // weights (packed pairs) summed as a tree; vm is the NaN-propagating
+    // maximum of them all
     template <typename TIn>
     __device__ __forceinline__ void add_tile(const uint4 (&v)[kFVec], float vm, float c) {
+        constexpr int H = FE<TIn>::VEC / 2;
         if (!(vm > -INFINITY)) return;
-        if (vm > m) {
-            const float f = m == -INFINITY ? 0.0f : fex2((m - vm) * c);
-            s.s *= f;
-            s.c *= f;
-            m = vm;
-        }
+        if (vm > m) raise(vm, c);
+        const float2 c2 = make_float2(c, c), n2 = make_float2(nmc, nmc);
+        float2 acc[kFVec];
 #pragma unroll
         for (int i = 0; i < kFVec; ++i) {
-            float x[FE<TIn>::VEC];
-            FE<TIn>::unpack(v[i], x);
+            float2 x[H];
+            FE<TIn>::pairs(v[i], x);
 #pragma unroll
-            for (int j = 0; j < FE<TIn>::VEC; ++j) x[j] = fex2((x[j] - m) * c);
+            for (int k = 0; k < H; ++k) x[k] = fex2x2(__ffma2_rn(x[k], c2, n2));
 #pragma unroll
-            for (int w = FE<TIn>::VEC / 2; w > 0; w >>= 1)
+            for (int w = H / 2; w > 0; w >>= 1)
 #pragma unroll
-                for (int j = 0; j < w; ++j) x[j] += x[j + w];
-            s.add(x[0]);
+                for (int k = 0; k < w; ++k) x[k] = __fadd2_rn(x[k], x[k + w]);
+            acc[i] = x[0];
         }
+#pragma unroll
+        for (int w = kFVec / 2; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) acc[i] = __fadd2_rn(acc[i], acc[i + w]);
+        s.add(acc[0].x + acc[0].y);
     }
     // the first `valid` elements of a vector (the ragged end of a row)
     template <typename TIn>
@@ -306,27 +336,21 @@ struct Online {
         for (int j = 0; j < FE<TIn>::VEC; ++j)
             if (j < valid) vm = fmaxf(vm, x[j]);
         if (!(vm > -INFINITY)) return;
-        if (vm > m) {
-            const float f = m == -INFINITY ? 0.0f : fex2((m - vm) * c);
-            s.s *= f;
-            s.c *= f;
-            m = vm;
-        }
+        if (vm > m) raise(vm, c);
         float acc = 0.0f;
 #pragma unroll
         for (int j = 0; j < FE<TIn>::VEC; ++j)
-            if (j < valid) acc += fex2((x[j] - m) * c);
+            if (j < valid) acc += fex2(fmaf(x[j], c, nmc));
         s.add(acc);
     }
 };
 
-// maximum and rescaled sum of one row over all consumer threads (each warp
-// rescales to its maximum; warps are combined in fp64 in a fixed order)
+// maximum and rescaled sum of one row over the lanes of a warp
 __device__ __forceinline__ void warp_online(const Online& o, float c, float* wm, float* ws) {
     *wm = warp_maxf(o.m);
     KSum k = o.s;
     if (*wm > -INFINITY) {
-        const float f = o.m == -INFINITY ? 0.0f : fex2((o.m - *wm) * c);
+        const float f = o.m == -INFINITY ? 0.0f : fex2(row_nmc(*wm, c) - o.nmc);
         k.s *= f;
         k.c *= f;
     } else {
@@ -334,6 +358,7 @@ __device__ __forceinline__ void warp_online(const Online& o, float c, float* wm,
     }
     *ws = warp_ksum(k);
 }
+
 // Statistics of one row over all consumer warps, computed by every warp from
 // the seven warps' (maximum, rescaled sum) pairs in red[w][col], [col + 1]:
 // lane w rescales warp w's sum to the common maximum, and the warp adds them
@@ -342,17 +367,21 @@ __device__ __forceinline__ void combine_stats(const float (*red)[8], int col, fl
     const float wm = lane < kFWarps ? red[lane][col] : -INFINITY;
     const float m = warp_maxf(wm);
     float x = 0.0f;
-    if (m > -INFINITY && wm > -INFINITY) x = red[lane][col + 1] * fex2((wm - m) * c);
+    if (m > -INFINITY && wm > -INFINITY) x = red[lane][col + 1] * fex2(row_nmc(m, c) - row_nmc(wm, c));
     *M = m;
     *S = cf_val(warp_cf_sum(CF{x, 0.0f}));
 }
 
-// 2^((l - M) * c) to about fp32 rounding for any l <= M, where c = chi + clo
-// is log2(e) / T as a float pair: the difference is formed exactly (two-sum),
-// the product with c by an FMA two-product, the integer part n is applied
-// exactly and only the fraction f in [-1/2, 1/2] goes through exp2f.  Results
-// below 2^-126 are 0.  Used for the two probabilities of the acceptance test.
-__device__ __forceinline__ float exp2_prod(float l, float M, float chi, float clo) {
+// The weight 2^(l * chi + nmc) of prob_f / kept_prob, with chi = fp32(c),
+// computed to about fp32 rounding of the exact 2^((l - M) * c - delta) for
+// any l <= M, where c = chi + clo is log2(e) / T as a float pair and delta =
+// fp32(M * chi) - M * chi is the row's common shift (so the weight matches the
+// row's sum).  The difference l - M is formed exactly (two-sum), the product
+// with c by an FMA two-product, -delta = fma(M, chi, nmc) exactly, the integer
+// part n is applied exactly and only the fraction f in [-1/2, 1/2] goes
+// through exp2f.  Results below 2^-126 are 0.  Used for the two probabilities
+// of the acceptance test.
+__device__ __forceinline__ float exp2_prod(float l, float M, float chi, float clo, float nmc) {
     const float d = l - M;
     const float p = d * chi;
     const float n = rintf(p);
@@ -360,7 +389,7 @@ __device__ __forceinline__ float exp2_prod(float l, float M, float chi, float cl
     const float bb = d - l;
     const float dlo = (l - (d - bb)) + (-M - bb);  // l - M = d + dlo exactly
     const float e = fmaf(d, chi, -p);               // d * chi = p + e exactly
-    const float f = (p - n) + (e + fmaf(d, clo, dlo * chi));
+    const float f = (p - n) + ((e + fmaf(M, chi, nmc)) + fmaf(d, clo, dlo * chi));
     return exp2f(f) * __int_as_float((int)(n + 127.0f) << 23);
 }
 
@@ -429,7 +458,7 @@ __device__ int warp_cross(const unsigned long long* h, int n, unsigned long long
 // id asc) and walk them from the mass before their fine bin to the first one
 // whose running mass reaches P (the nucleus' last token).  Returns false if
 // there are too many (or none) to decide here.
-__device__ bool warp_cut(unsigned long long* list, int n, unsigned long long base, double P, float M, float c,
+__device__ bool warp_cut(unsigned long long* list, int n, unsigned long long base, double P, float c, float nmc,
                          float inv, uint32_t* cut_key, uint32_t* cut_id, double* kept, int lane) {
     if (n < 1 || n > kNCap) return false;
     warp_sort(list, n, list, true, 0ull, lane);
@@ -438,7 +467,7 @@ __device__ bool warp_cut(unsigned long long* list, int n, unsigned long long bas
     double K = 0.0;
     for (int c0 = 0; c0 < n && idx < 0; c0 += 32) {
         const int j = c0 + lane;
-        const double p = j < n ? (double)prob_f(key_value32((uint32_t)(list[j] >> 32)), M, c, inv) : 0.0;
+        const double p = j < n ? (double)prob_f(key_value32((uint32_t)(list[j] >> 32)), c, nmc, inv) : 0.0;
         double x = p;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -463,13 +492,14 @@ __device__ bool warp_cut(unsigned long long* list, int n, unsigned long long bas
     return true;
 }
 
-// One tile of a nucleus pass for row r (max M, 1/sum inv); the thread holds the
+// One tile of a nucleus pass for row r (max M, nmc = row_nmc(M, c), 1/sum inv);
+// the thread holds the
 // vectors vbase + 32 i of the segment.  Pass 1 adds the
 // masses to the coarse histogram, pass 2 those of the crossing coarse bin to
 // the fine histogram, pass 3 collects the elements of the crossing fine bin.
 template <typename TIn>
 __device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVec], int n, int vbase, int col,
-                                             int pass, int r, float M, float c, float inv) {
+                                             int pass, int r, float M, float c, float nmc, float inv) {
     using F = FE<TIn>;
     const float s1 = (float)kNB1 / kNDmax;
     const float s2 = (float)kNB2 * (float)kNB1 / kNDmax;
@@ -490,12 +520,12 @@ __device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVe
             if (!(d < kNDmax)) continue;
             const int bb = min(kNB1 - 1, (int)(d * s1));
             if (pass == 1) {
-                const float p = prob_f(x[j], M, c, inv);
+                const float p = prob_f(x[j], c, nmc, inv);
                 if (p > 0.0f) atomicAdd(&sm.h1[r][bb], mass_fix(p));
             } else if (bb == b1) {
                 const int sb = min(kNB2 - 1, max(0, (int)((d - d1) * s2)));
                 if (pass == 2) {
-                    const float p = prob_f(x[j], M, c, inv);
+                    const float p = prob_f(x[j], c, nmc, inv);
                     if (p > 0.0f) atomicAdd(&sm.h2[r][sb], mass_fix(p));
                 } else if (sb == b2) {
                     const int slot = atomicAdd(&sm.ncnt[r], 1);
@@ -609,6 +639,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
     float c = 1.0f, Pf = 1.0f;
     Online op, oq;
     float Mp = 0.0f, Mq = 0.0f, Sp = 0.0f, Sq = 0.0f, invp = 0.0f, invq = 0.0f, invp2 = 0.0f, invq2 = 0.0f;
+    float nmcp = 0.0f, nmcq = 0.0f;  // row_nmc of each row's maximum
     unsigned long long cutp = 0ull, cutq = 0ull;  // last kept element of each row (0: keep all)
     KSum alpha{0.0f, 0.0f};
     // the unit's record for the tail kernel (one thread writes it)
@@ -733,6 +764,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 dead = anynf || !(Mp > -INFINITY) || (pair && !(Mq > -INFINITY));
                 invp = dead ? 0.0f : 1.0f / Sp;
                 invq = (dead || !pair) ? 0.0f : 1.0f / Sq;
+                nmcp = row_nmc(Mp, c);
+                nmcq = pair ? row_nmc(Mq, c) : 0.0f;
                 invp2 = invp;
                 invq2 = invq;
                 if (t == 0 && (dead || !nuc)) write_rec(w, dead ? kRecDead : 0u);
@@ -743,8 +776,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
         if (pass < kPassFinal) {
             // ---- nucleus passes: the last kept token of each row (top-p < 1)
             if (dead) continue;
-            nucleus_tile<TIn>(sm, vp, n, vbase, col, pass, 0, Mp, c, invp);
-            if (pair) nucleus_tile<TIn>(sm, vq, n, vbase, col, pass, 1, Mq, c, invq);
+            nucleus_tile<TIn>(sm, vp, n, vbase, col, pass, 0, Mp, c, nmcp, invp);
+            if (pair) nucleus_tile<TIn>(sm, vq, n, vbase, col, pass, 1, Mq, c, nmcq, invq);
             if (tile != ntiles - 1) continue;
             if (!fsync(sm, g)) break;
             const unsigned long long target = (unsigned long long)((double)Pf * (double)kMassScale);
@@ -772,7 +805,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                     const int cnt = sm.ncnt[r];
                     const bool ok = sm.nb[r][1] >= 0 &&
                                     warp_cut(sm.h1[r], min(cnt, kNCap + 1), sm.nbase[r], (double)Pf,
-                                             r == 0 ? Mp : Mq, c, r == 0 ? invp : invq, &ck, &ci, &K, lane);
+                                             c, r == 0 ? nmcp : nmcq, r == 0 ? invp : invq, &ck, &ci, &K, lane);
                     if (lane == 0) {
                         sm.cut_key[r] = ck;
                         sm.cut_id[r] = ci;
@@ -826,8 +859,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
 #pragma unroll
                     for (int j = 0; j < F::VEC; ++j) {
                         const uint32_t id = (uint32_t)(col + e0 + j);
-                        const float p = j < valid ? kept_prob<CUT>(xp[j], id, Mp, c, invp2, cutp) : 0.0f;
-                        const float q = j < valid ? kept_prob<CUT>(xq[j], id, Mq, c, invq2, cutq) : 0.0f;
+                        const float p = j < valid ? kept_prob<CUT>(xp[j], id, c, nmcp, invp2, cutp) : 0.0f;
+                        const float q = j < valid ? kept_prob<CUT>(xq[j], id, c, nmcq, invq2, cutq) : 0.0f;
                         ma[j] = fminf(p, q);
                         ra[j] = resid_f(p, q);
                         pa[j] = p;
@@ -846,7 +879,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 } else {
 #pragma unroll
                     for (int j = 0; j < F::VEC; ++j)
-                        if (j < valid) tp += kept_prob<CUT>(xp[j], (uint32_t)(col + e0 + j), Mp, c, invp2, cutp);
+                        if (j < valid) tp += kept_prob<CUT>(xp[j], (uint32_t)(col + e0 + j), c, nmcp, invp2, cutp);
                 }
                 alpha.add(am);
                 if (a.p_out || a.q_out) {  // debug outputs
@@ -855,18 +888,66 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                         if (j < valid) {
                             if (a.p_out)
                                 a.p_out[((size_t)b * (G + 1) + u) * V + col + e0 + j] =
-                                    kept_prob<CUT>(xp[j], (uint32_t)(col + e0 + j), Mp, c, invp2, cutp);
+                                    kept_prob<CUT>(xp[j], (uint32_t)(col + e0 + j), c, nmcp, invp2, cutp);
                             if (a.q_out && pair)
                                 a.q_out[((size_t)b * G + u) * V + col + e0 + j] =
-                                    kept_prob<CUT>(xq[j], (uint32_t)(col + e0 + j), Mq, c, invq2, cutq);
+                                    kept_prob<CUT>(xq[j], (uint32_t)(col + e0 + j), c, nmcq, invq2, cutq);
                         }
                 }
             }
         };
-        if (nuc)
+        // a full tile without the debug outputs: packed pairs, no bounds per element;
+        // the sums run over the thread's pairs in order
+        auto final_fast = [&](auto cut_on) {
+            constexpr bool CUT = decltype(cut_on)::value;
+            constexpr int H = F::VEC / 2;
+            const float2 c2 = make_float2(c, c), np2 = make_float2(nmcp, nmcp), nq2 = make_float2(nmcq, nmcq);
+            const float2 ip2 = make_float2(invp2, invp2), iq2 = make_float2(invq2, invq2);
+            const float2 m1 = make_float2(-1.0f, -1.0f);
+            // the cut element of each row as (logit, id)
+            const float lcp = key_value32((uint32_t)(cutp >> 32)), lcq = key_value32((uint32_t)(cutq >> 32));
+            const uint32_t icp = ~(uint32_t)cutp, icq = ~(uint32_t)cutq;
+            float2 am = make_float2(0.0f, 0.0f), ar = am, ap = am;
+#pragma unroll
+            for (int i = 0; i < kFVec; ++i) {
+                float2 xp[H], xq[H];
+                F::pairs(vp[i], xp);
+                if (pair) F::pairs(vq[i], xq);
+                const uint32_t id0 = (uint32_t)(col + (vbase + 32 * i) * F::VEC);
+#pragma unroll
+                for (int k = 0; k < H; ++k) {
+                    float2 p = __fmul2_rn(fex2x2(__ffma2_rn(xp[k], c2, np2)), ip2);
+                    if (CUT) {
+                        if (!kept_at(xp[k].x, id0 + 2 * k, lcp, icp)) p.x = 0.0f;
+                        if (!kept_at(xp[k].y, id0 + 2 * k + 1, lcp, icp)) p.y = 0.0f;
+                    }
+                    if (pair) {
+                        float2 q = __fmul2_rn(fex2x2(__ffma2_rn(xq[k], c2, nq2)), iq2);
+                        if (CUT) {
+                            if (!kept_at(xq[k].x, id0 + 2 * k, lcq, icq)) q.x = 0.0f;
+                            if (!kept_at(xq[k].y, id0 + 2 * k + 1, lcq, icq)) q.y = 0.0f;
+                        }
+                        const float2 d = __ffma2_rn(q, m1, p);  // p - q, one rounding
+                        am = __fadd2_rn(am, make_float2(fminf(p.x, q.x), fminf(p.y, q.y)));
+                        ar = __fadd2_rn(ar, make_float2(fmaxf(d.x, 0.0f), fmaxf(d.y, 0.0f)));
+                    }
+                    ap = __fadd2_rn(ap, p);
+                }
+            }
+            tr = ar.x + ar.y;
+            tp = ap.x + ap.y;
+            alpha.add(am.x + am.y);
+        };
+        if (n == TS && !(a.p_out || a.q_out)) {
+            if (nuc)
+                final_fast(std::true_type{});
+            else
+                final_fast(std::false_type{});
+        } else if (nuc) {
             final_tile(std::true_type{});
-        else
+        } else {
             final_tile(std::false_type{});
+        }
         // this warp's block of the tile: sums of r (pairs only) and of p, in the record
         const float wtr = warp_ksum(KSum{tr, 0.0f}), wtp = warp_ksum(KSum{tp, 0.0f});
         if (lane == 0) {
@@ -919,7 +1000,8 @@ __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
         }
         const float Mp = rec->Mp, Mq = rec->Mq, invp2 = rec->invp, invq2 = rec->invq;
         const unsigned long long cutp = rec->cutp, cutq = rec->cutq;
-        const float c = 1.4426950408889634f / si.T;  // the free kernel's expression
+        const float c = 1.4426950408889634f / si.T;  // the free kernel's expressions
+        const float nmcp = row_nmc(Mp, c), nmcq = pair ? row_nmc(Mq, c) : 0.0f;
         const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
         const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
 
@@ -989,9 +1071,9 @@ __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
                     const int e = e0 + j;
                     rv[j] = 0.0f;
                     if (e < e_end) {
-                        const float p = kept_prob<true>(F::load(trow, e), (uint32_t)e, Mp, c, invp2, cutp);
+                        const float p = kept_prob<true>(F::load(trow, e), (uint32_t)e, c, nmcp, invp2, cutp);
                         const float q =
-                            use_p ? 0.0f : kept_prob<true>(F::load(drow, e), (uint32_t)e, Mq, c, invq2, cutq);
+                            use_p ? 0.0f : kept_prob<true>(F::load(drow, e), (uint32_t)e, c, nmcq, invq2, cutq);
                         rv[j] = use_p ? p : resid_f(p, q);
                         own += rv[j];
                         if (rv[j] > 0.0f) mylast = e;
@@ -1028,14 +1110,13 @@ __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
             if (lane == 0) {
                 const int xt = a.draft_tokens[(size_t)b * G + u];
                 const float lpx = F::load(trow, xt), lqx = F::load(drow, xt);
-                const double c2 = 1.4426950408889634 / (double)si.T;
-                const float chi = (float)c2, clo = (float)(c2 - (double)chi);
+                const float clo = (float)(1.4426950408889634 / (double)si.T - (double)c);  // c + clo = log2(e) / T
                 const unsigned long long kx =
                     ((unsigned long long)okey32(__float_as_uint(lpx)) << 32) | (unsigned long long)(~(uint32_t)xt);
                 const unsigned long long kqx =
                     ((unsigned long long)okey32(__float_as_uint(lqx)) << 32) | (unsigned long long)(~(uint32_t)xt);
-                const double px = kx < cutp ? 0.0 : (double)exp2_prod(lpx, Mp, chi, clo) * (double)invp2;
-                const double qx = kqx < cutq ? 0.0 : (double)exp2_prod(lqx, Mq, chi, clo) * (double)invq2;
+                const double px = kx < cutp ? 0.0 : (double)exp2_prod(lpx, Mp, c, clo, nmcp) * (double)invp2;
+                const double qx = kqx < cutq ? 0.0 : (double)exp2_prod(lqx, Mq, c, clo, nmcq) * (double)invq2;
                 const double ua = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 0u);
                 accept = (ua * qx < px) ? 1 : 0;
             }
