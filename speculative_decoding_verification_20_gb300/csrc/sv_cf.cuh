@@ -34,4 +34,23 @@ __device__ __forceinline__ CF warp_cf_scan(CF a, int lane) {  // inclusive, in l
     return a;
 }
 
+// x * a as a compensated pair (FMA two-product of the head)
+__device__ __forceinline__ CF cf_scale(float x, CF a) {
+    const float p = x * a.s;
+    const float e = fmaf(x, a.s, -p);  // x * a.s = p + e exactly
+    return CF{p, fmaf(x, a.c, -e)};
+}
+// a >= b, decided on the compensated difference
+__device__ __forceinline__ bool cf_ge(CF a, CF b) {
+    const CF d = cf_add(a, CF{-b.s, -b.c});
+    return d.s - d.c >= 0.0f;
+}
+// 1 / a to about fp32 rounding: the rounded reciprocal of the head, then one
+// Newton step on the exact residual 1 - r * a.s and the tail
+__device__ __forceinline__ float cf_recip(CF a) {
+    const float r = 1.0f / a.s;
+    const float t = fmaf(-r, a.s, 1.0f) + r * a.c;
+    return fmaf(r, t, r);
+}
+
 }  // namespace sv

@@ -39,7 +39,7 @@ struct CombPair {
 // below the common prefix of the smallest and largest key (warp reductions),
 // ties at it by id (ids < 2^18).  M slots per lane cover m.
 template <int KB, int M>
-__device__ int warp_keep_topk_m(unsigned long long* buf, int m, int k, int lane) {
+__device__ __noinline__ int warp_keep_topk_m(unsigned long long* buf, int m, int k, int lane) {
     const int used = (m + 31) >> 5;
     unsigned long long e[M];
     uint32_t key[M];
@@ -163,50 +163,34 @@ __device__ __forceinline__ float prob_of(const unsigned long long* byid, const f
     return 0.0f;
 }
 
-// 2^x for x <= 0, with the exponent split (Cody-Waite style) into an integer n
-// and a fraction f in [-1/2, 1/2] in fp64: only f goes through the fp32 exp2,
-// and 2^n is applied exactly, so the result keeps the fp32 exp2's relative
-// accuracy whatever the size of x, at the cost of a few fp64 operations
-// (instead of a full fp64 exponential).  Below 2^-1022 the result is 0.
-__device__ __forceinline__ double exp2_split(double x) {
-    const double n = rint(x);
-    if (n < -1022.0) return 0.0;
-    const double f = x - n;
-    const double pw = __longlong_as_double((long long)(n + 1023.0) << 52);
-    return (double)exp2f((float)f) * pw;
+// Unnormalised weight 2^((l - vmax) * c) of a kept logit l, c = log2(e) / T
+// given as a float pair chi + clo, to about fp32 rounding whatever the size
+// of the exponent and without fp64 arithmetic: the difference is formed
+// exactly (two-sum; exact in fp32 anyway for bf16 logits), its product with
+// chi by an FMA two-product, the integer part n is applied exactly and only
+// the fraction in [-1/2, 1/2] goes through exp2f.  Below 2^-126 the weight is 0.
+__device__ __forceinline__ float kept_weight(float l, float vmax, float chi, float clo) {
+    const float d = l - vmax;
+    const float p = d * chi;
+    const float n = rintf(p);
+    if (!(n >= -126.0f)) return 0.0f;
+    const float bb = d - l;
+    const float dlo = (l - (d - bb)) + (-vmax - bb);  // l - vmax = d + dlo exactly
+    const float e = fmaf(d, chi, -p);                  // d * chi = p + e exactly
+    const float f = (p - n) + (e + fmaf(d, clo, dlo * chi));
+    return exp2f(f) * __int_as_float((int)(n + 127.0f) << 23);
 }
-
-// Unnormalised weight 2^((v - vmax) * log2(e) / T) of a kept logit.
-// bf16 logits: v - vmax is exact in fp32; the product with log2(e)/T (given
-// as a float pair chi + clo) is formed exactly by an FMA two-product (Dekker),
-// split into an integer n and a fraction in fp32, and only the fraction goes
-// through exp2f -- no fp64 arithmetic.  fp32 logits: the difference is not
-// always exact in fp32, so the exponent is formed in fp64 (exp2_split).
 template <typename TIn>
-struct KeptWeight;
-template <>
-struct KeptWeight<__nv_bfloat16> {
-    __device__ static float vmax_of(uint32_t k) { return key_value16(k); }
-    __device__ static float w(uint32_t k, float vmax, float chi, float clo, double) {
-        const float d = key_value16(k) - vmax;
-        const float p = d * chi;
-        const float e = fmaf(d, chi, -p);
-        const float n = rintf(p);
-        if (n < -126.0f) return 0.0f;
-        const float f = (p - n) + fmaf(d, clo, e);
-        return exp2f(f) * __int_as_float((int)(n + 127.0f) << 23);
-    }
-};
-template <>
-struct KeptWeight<float> {
-    __device__ static float vmax_of(uint32_t k) { return key_value32(k); }
-    __device__ static float w(uint32_t k, float vmax, float, float, double c2) {
-        return (float)exp2_split(((double)key_value32(k) - (double)vmax) * c2);
-    }
-};
+__device__ __forceinline__ float key_logit(uint32_t k) {
+    return sizeof(TIn) == 2 ? key_value16(k) : key_value32(k);
+}
 
 // Normalisation of one sorted kept list by one warp: softmax over the kept
 // logits at temperature T (one-hot if T == 0), then top-p.  prob[j] for j < k.
+// No fp64: the top-p prefix is found by comparing the running sum of the
+// weights with P * S (S their sum) as compensated pairs, with no division, so
+// k exactly tied weights cross exactly where j >= P * k, as the fp64
+// definition decides for k <= 256 and a float P.
 template <typename TIn>
 __device__ void normalise_kept(const unsigned long long* top, int k, float Tf, float Pf, float* prob) {
     const int lane = threadIdx.x & 31;
@@ -215,48 +199,44 @@ __device__ void normalise_kept(const unsigned long long* top, int k, float Tf, f
         __syncwarp();
         return;
     }
-    const float vmax = KeptWeight<TIn>::vmax_of(comp_key(top[0]));
-    const double c2 = 1.4426950408889634 / (double)Tf;  // log2(e) / T
-    const float chi = (float)c2, clo = (float)(c2 - (double)chi);
+    const float vmax = key_logit<TIn>(comp_key(top[0]));
+    // log2(e) / T = chi + clo: chi rounded, clo from the exact remainder of the division
+    constexpr float kL2eHi = 1.44269502162933349609375f;  // fp32(log2 e)
+    constexpr float kL2eLo = 1.925963033500011e-08f;       // log2 e - kL2eHi
+    const float chi = kL2eHi / Tf;
+    const float clo = (fmaf(-chi, Tf, kL2eHi) + kL2eLo) / Tf;
     CF s{0.0f, 0.0f};
     for (int j = lane; j < k; j += 32) {
-        const float w = KeptWeight<TIn>::w(comp_key(top[j]), vmax, chi, clo, c2);
+        const float w = kept_weight(key_logit<TIn>(comp_key(top[j])), vmax, chi, clo);
         prob[j] = w;
         s = cf_add(s, CF{w, 0.0f});
     }
     s = warp_cf_sum(s);
-    // probabilities and the top-p running mass in fp64 from the fp32 weights, so
-    // that exact ties (equal weights, 1/k each) sum as the fp64 definition does
-    const double inv = 1.0 / ((double)s.s - (double)s.c);
     __syncwarp();
+    int keep = k;
     if (Pf < 1.0f) {  // shortest prefix (prob desc, id asc) whose mass reaches P, crossing token kept
-        const double P = (double)Pf;
-        double carry = 0.0;
-        int keep = k;
+        const CF ps = cf_scale(Pf, s);
+        CF carry{0.0f, 0.0f};
         for (int c0 = 0; c0 < k; c0 += 32) {
             const int j = c0 + lane;
-            double x = j < k ? (double)prob[j] * inv : 0.0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-                if (lane >= o) x += y;
-            }
-            const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < k && carry + x >= P);
+            const CF x = cf_add(carry, warp_cf_scan(CF{j < k ? prob[j] : 0.0f, 0.0f}, lane));
+            const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < k && cf_ge(x, ps));
             if (hit) {
                 keep = c0 + __ffs(hit);
                 break;
             }
-            carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+            carry = CF{__shfl_sync(0xFFFFFFFFu, x.s, 31), __shfl_sync(0xFFFFFFFFu, x.c, 31)};
         }
-        double s2 = 0.0;
-        for (int j = lane; j < keep; j += 32) s2 += (double)prob[j] * inv;
-        s2 = warp_sum(s2);
-        const double inv2 = inv / s2;
-        __syncwarp();
-        for (int j = lane; j < k; j += 32) prob[j] = j < keep ? (float)((double)prob[j] * inv2) : 0.0f;
-    } else {
-        for (int j = lane; j < k; j += 32) prob[j] = (float)((double)prob[j] * inv);
     }
+    CF s2 = s;
+    if (keep < k) {
+        s2 = CF{0.0f, 0.0f};
+        for (int j = lane; j < keep; j += 32) s2 = cf_add(s2, CF{prob[j], 0.0f});
+        s2 = warp_cf_sum(s2);
+    }
+    const float inv = cf_recip(s2);
+    __syncwarp();
+    for (int j = lane; j < k; j += 32) prob[j] = j < keep ? prob[j] * inv : 0.0f;
     __syncwarp();
 }
 
@@ -283,6 +263,9 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
     const int G = a.G;
     const bool pair = unit < si.gamma;
     const int kt = sm.kept[0], kd = pair ? sm.kept[1] : 0;
+    // the unit's two uniforms (acceptance, residual draw), one per lane, in parallel
+    const double uu = lane < 2 ? uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), (uint32_t)lane) : 0.0;
+    const double u_acc = __shfl_sync(0xFFFFFFFFu, uu, 0), u_res = __shfl_sync(0xFFFFFFFFu, uu, 1);
     if (kt < 0 || kd < 0) {
         if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
         unit_finished_warp(a, b, lane);
@@ -295,8 +278,7 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
         const int x = a.draft_tokens[(size_t)b * G + unit];
         const double px = (double)prob_of(sm.byid[0], sm.prob[0], kt, x);
         const double qx = (double)prob_of(sm.byid[1], sm.prob[1], kd, x);
-        const double u = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 0u);
-        accept = (u * qx < px) ? 1 : 0;
+        accept = (u_acc * qx < px) ? 1 : 0;
     }
 
     // alpha_i = sum_x min(p, q) and the residual weights, in ascending token id
@@ -329,7 +311,7 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
         }
     }
     // inverse CDF: the first id whose running sum passes v
-    const double v = uniform01(a.seed, (uint32_t)b, (uint32_t)(unit + 1), 1u) * (double)Zt;
+    const double v = u_res * (double)Zt;
     int token = -1, last_pos = -1;
     CF carry{0.0f, 0.0f};
 #pragma unroll

@@ -78,7 +78,7 @@ __device__ __forceinline__ void unit_finished(const Args& a, int b) {
 // Warp versions of the two functions above, for kernels where one warp owns
 // a unit.  The first rejection is found with a ballot over 32 positions at a
 // time and the lowest set lane.
-__device__ __forceinline__ void finalize_sequence_warp(const Args& a, int b, int lane) {
+static __device__ __noinline__ void finalize_sequence_warp(const Args& a, int b, int lane) {
     const SeqInfo si = a.seq[b];
     const int G = a.G, gamma = si.gamma;
     const uint32_t st = __ldcg(&a.seq_status[b]);

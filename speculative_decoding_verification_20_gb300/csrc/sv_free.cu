@@ -73,6 +73,7 @@ struct FreeSmem {
     uint64_t empty[kFStages];
     uint64_t gsync;
     int4 hdr[kFStages];               // unit index (-1: no more work), pass, tile, elements
+    int4 uhdr[kFStages];              // the unit: list item (b << 8 | u), gamma_b, T and top-p (float bits)
     float red[2][kFWarps][8];         // per warp: row statistics (by the parity of the CTA's unit count)
     unsigned long long h1[2][kNB1];   // per row: coarse mass histogram (2^40 fixed point); then the crossing elements
     unsigned long long h2[2][kNB2];   // per row: fine mass histogram
@@ -588,7 +589,10 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                             ok = false;
                             break;
                         }
-                        if (lane == 0) sm.hdr[stage] = make_int4((int)w, pass, tile, n);
+                        if (lane == 0) {
+                            sm.hdr[stage] = make_int4((int)w, pass, tile, n);
+                            sm.uhdr[stage] = make_int4((int)item, si.gamma, __float_as_int(si.T), __float_as_int(si.P));
+                        }
                         if (TMA) {
                             const uint32_t bytes = (uint32_t)(n * sizeof(TIn));
                             fbar_expect(&sm.full[stage], pair ? 2u * bytes : bytes);
@@ -662,15 +666,15 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
         if (h.x < 0) break;
         const int w = h.x, pass = h.y, tile = h.z, n = h.w;
         const int col = tile * TS;
-        if (pass == 0 && tile == 0) {  // a new unit
-            const uint32_t item = a.free_units[w];
-            b = (int)(item >> 8);
-            u = (int)(item & 0xFFu);
-            const SeqInfo si = a.seq[b];
-            pair = u < si.gamma;
-            c = 1.4426950408889634f / si.T;
-            nuc = si.P < 1.0f;
-            Pf = si.P;
+        if (pass == 0 && tile == 0) {  // a new unit (from the producer's header: no global loads)
+            const int4 uh = sm.uhdr[stage];  // read before the stage is released
+            b = uh.x >> 8;
+            u = uh.x & 0xFF;
+            pair = u < uh.y;
+            const float T = __int_as_float(uh.z);
+            c = 1.4426950408889634f / T;
+            Pf = __int_as_float(uh.w);
+            nuc = Pf < 1.0f;
             fall = false;
             cutp = cutq = 0ull;
             op.init();

@@ -6,45 +6,60 @@
 
 namespace sv {
 
+// One compare-exchange of a bitonic stage between x[m] and its partner value
+// y: keep the larger value where this position's block sorts descending and
+// this position is the lower one of the pair (or ascending and upper).
+__device__ __forceinline__ unsigned long long bitonic_keep(unsigned long long v, unsigned long long y, bool take_max) {
+    return take_max ? (v > y ? v : y) : (v < y ? v : y);
+}
+
 // Bitonic sort across the warp of 32 * P 64-bit keys held P per lane (element
-// m * 32 + lane in x[m]), descending or ascending.
+// m * 32 + lane in x[m]), descending or ascending.  The merge stages (k2, j)
+// run as loops, not unrolled, so the network costs one loop body of code
+// whatever P is: partners at distance j < 32 are in lane ^ j (a shuffle),
+// partners at j >= 32 are in the same lane, at register m ^ (j / 32).
 template <int P>
 __device__ __forceinline__ void warp_bitonic(unsigned long long (&x)[P], int lane, bool descending) {
     constexpr int N = 32 * P;
-#pragma unroll
+#pragma unroll 1
     for (int k2 = 2; k2 <= N; k2 <<= 1) {
-#pragma unroll
+#pragma unroll 1
         for (int j = k2 >> 1; j > 0; j >>= 1) {
-            if (j >= 32) {  // partners in the same lane
-#pragma unroll
-                for (int m = 0; m < P; ++m) {
-                    const int mp = m ^ (j >> 5);
-                    if (mp > m) {
-                        const bool lower_max = (((m * 32 + lane) & k2) == 0) == descending;
-                        const unsigned long long lo = x[m], hi = x[mp];
-                        const bool sw = lower_max ? (lo < hi) : (lo > hi);
-                        x[m] = sw ? hi : lo;
-                        x[mp] = sw ? lo : hi;
-                    }
-                }
-            } else {  // partners in lane ^ j
+            if (j < 32) {
+                const bool lower = (lane & j) == 0;
 #pragma unroll
                 for (int m = 0; m < P; ++m) {
                     const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, x[m], j);
-                    const bool lower = (lane & j) == 0;
                     const bool lower_max = (((m * 32 + lane) & k2) == 0) == descending;
-                    const bool take_max = lower == lower_max;
-                    x[m] = take_max ? (x[m] > y ? x[m] : y) : (x[m] < y ? x[m] : y);
+                    x[m] = bitonic_keep(x[m], y, lower == lower_max);
+                }
+            } else {
+                // in-lane partners m and m ^ s, s = j / 32 in {1, 2, 4, ...} < P
+#pragma unroll
+                for (int s = 1; s < P; s <<= 1) {
+                    if ((j >> 5) != s) continue;
+#pragma unroll
+                    for (int m = 0; m < P; ++m) {
+                        const int mp = m ^ s;
+                        if (mp > m) {
+                            const bool lower_max = (((m * 32 + lane) & k2) == 0) == descending;
+                            const unsigned long long lo = x[m], hi = x[mp];
+                            const bool sw = lower_max ? (lo < hi) : (lo > hi);
+                            x[m] = sw ? hi : lo;
+                            x[mp] = sw ? lo : hi;
+                        }
+                    }
                 }
             }
         }
     }
 }
 
-// Sort n <= 32 * P entries of src (pad: `pad`) into dst across the warp.
+// Sort n <= 32 * P entries of src (pad: `pad`) into dst across the warp.  Kept
+// out of line: one copy per size serves every caller.
 template <int P>
-__device__ __forceinline__ void warp_sort_into(const unsigned long long* src, int n, unsigned long long* dst,
-                                               bool descending, unsigned long long pad, int lane) {
+__device__ __noinline__ void warp_sort_into(const unsigned long long* src, int n, unsigned long long* dst,
+                                            bool descending, unsigned long long pad, int lane) {
     unsigned long long x[P];
 #pragma unroll
     for (int m = 0; m < P; ++m) x[m] = m * 32 + lane < n ? src[m * 32 + lane] : pad;
