@@ -61,8 +61,14 @@ constexpr float kNDmax = 64.0f;  // beyond it a logit's mass is below 2^-64 of t
 constexpr int kNB1 = 512;        // coarse bins of 1/8 log2 unit
 constexpr int kNB2 = 512;        // fine bins inside the coarse bin where the running mass passes P
 constexpr int kNCap = 256;       // elements of the crossing fine bin sorted here (else: cluster kernel)
-constexpr float kMassScale = 1099511627776.0f;  // 2^40: masses are summed in 64-bit fixed point
-static_assert(kNCap <= kNB1, "the crossing elements are collected over the coarse histogram");
+constexpr float kMassScale = 1099511627776.0f;  // 2^40: masses are summed exactly in fixed point
+// A logit's fixed-point mass m <= 2^40 is added to a bin as two 32-bit parts,
+// m >> 10 and m & 1023 (native shared-memory atomics; a 64-bit atomic per
+// logit serialises on the hot bins).  Neither part can overflow: the high
+// parts of a row sum to at most 2^30 (the masses sum to 1), and a bin's low
+// parts to at most 1023 * SV_MAX_VOCAB < 2^28.
+constexpr int kMassLoBits = 10;
+static_assert(1023ull * SV_MAX_VOCAB < (1ull << 32), "low parts of a bin fit 32 bits");
 // passes of a unit through the ring: 0 statistics, 1 coarse histogram, 2 fine
 // histogram, 3 collect the crossing elements, 4 alpha and residual weights
 constexpr int kPassFinal = 4;
@@ -75,14 +81,18 @@ struct FreeSmem {
     int4 hdr[kFStages];               // unit index (-1: no more work), pass, tile, elements
     int4 uhdr[kFStages];              // the unit: list item (b << 8 | u), gamma_b, T and top-p (float bits)
     float red[2][kFWarps][8];         // per warp: row statistics (by the parity of the CTA's unit count)
-    unsigned long long h1[2][kNB1];   // per row: coarse mass histogram (2^40 fixed point); then the crossing elements
-    unsigned long long h2[2][kNB2];   // per row: fine mass histogram
+    uint32_t h1[2][2][kNB1];          // per row: coarse mass histogram (2^40 fixed point) as [high, low] parts
+    uint32_t h2[2][2][kNB2];          // per row: fine mass histogram, the same way
+    unsigned long long list[2][kNCap];  // per row: the elements of the crossing fine bin
     int nb[2][2];                     // per row: crossing coarse bin, crossing fine bin
     unsigned long long nbase[2];      // per row: mass before the crossing fine bin
     int ncnt[2];                      // per row: crossing elements collected
     uint32_t cut_key[2], cut_id[2];   // per row: the last kept element (key, id)
     float kinv[2];                    // per row: 1 / (sum x kept mass); -1: too many ties at the cut
 };
+
+// two CTAs per SM: 228 KB of shared memory less 1 KB reserved per CTA
+static_assert(sizeof(FreeSmem) <= 115712, "the whole-row kernel must fit twice on an SM");
 
 // ---------------------------------------------------------------------------
 // PTX helpers (mbarriers, TMA bulk copies); every wait is bounded
@@ -402,16 +412,29 @@ __device__ __forceinline__ unsigned long long ncomp(float x, uint32_t id) {
     return ((unsigned long long)okey32(__float_as_uint(x)) << 32) | (unsigned long long)(~id);
 }
 __device__ __forceinline__ unsigned long long mass_fix(float p) { return __float2ull_rz(p * kMassScale); }
+// add the mass of probability p to bin `bin` of a split histogram h[2][n]
+template <int N>
+__device__ __forceinline__ void mass_add(uint32_t (&h)[2][N], int bin, float p) {
+    const unsigned long long m = mass_fix(p);
+    if (m == 0ull) return;
+    atomicAdd(&h[0][bin], (uint32_t)(m >> kMassLoBits));
+    const uint32_t lo = (uint32_t)m & ((1u << kMassLoBits) - 1u);
+    if (lo) atomicAdd(&h[1][bin], lo);
+}
+template <int N>
+__device__ __forceinline__ unsigned long long mass_of(const uint32_t (&h)[2][N], int bin) {
+    return ((unsigned long long)h[0][bin] << kMassLoBits) + h[1][bin];
+}
 
 // For the warp: the first bin of h[0..n) (n a multiple of 32) at which the
 // running mass reaches target, and the mass before it; if the total falls
 // short (rounding), the last bin with mass.  -1 when h is empty.
-__device__ int warp_cross(const unsigned long long* h, int n, unsigned long long target, unsigned long long* before,
-                          int lane) {
-    const int per = n / 32;
-    const unsigned long long* mine = h + lane * per;
+template <int N>
+__device__ int warp_cross(const uint32_t (&h)[2][N], unsigned long long target, unsigned long long* before, int lane) {
+    constexpr int per = N / 32;
+    const int b0 = lane * per;
     unsigned long long own = 0;
-    for (int i = 0; i < per; ++i) own += mine[i];
+    for (int i = 0; i < per; ++i) own += mass_of(h, b0 + i);
     unsigned long long x = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -429,12 +452,13 @@ __device__ int warp_cross(const unsigned long long* h, int n, unsigned long long
         if (lane == src) {
             unsigned long long run = excl;
             for (int i = 0; i < per; ++i) {
-                if (mine[i] > 0 && run + mine[i] >= target) {
-                    bin = lane * per + i;
+                const unsigned long long mi = mass_of(h, b0 + i);
+                if (mi > 0 && run + mi >= target) {
+                    bin = b0 + i;
                     bef = run;
                     break;
                 }
-                run += mine[i];
+                run += mi;
             }
         }
     } else if (nz) {
@@ -442,11 +466,12 @@ __device__ int warp_cross(const unsigned long long* h, int n, unsigned long long
         if (lane == src) {
             unsigned long long run = excl;
             for (int i = 0; i < per; ++i) {
-                if (mine[i] > 0) {
-                    bin = lane * per + i;
+                const unsigned long long mi = mass_of(h, b0 + i);
+                if (mi > 0) {
+                    bin = b0 + i;
                     bef = run;
                 }
-                run += mine[i];
+                run += mi;
             }
         }
     }
@@ -522,15 +547,15 @@ __device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVe
             const int bb = min(kNB1 - 1, (int)(d * s1));
             if (pass == 1) {
                 const float p = prob_f(x[j], c, nmc, inv);
-                if (p > 0.0f) atomicAdd(&sm.h1[r][bb], mass_fix(p));
+                mass_add(sm.h1[r], bb, p);
             } else if (bb == b1) {
                 const int sb = min(kNB2 - 1, max(0, (int)((d - d1) * s2)));
                 if (pass == 2) {
                     const float p = prob_f(x[j], c, nmc, inv);
-                    if (p > 0.0f) atomicAdd(&sm.h2[r][sb], mass_fix(p));
+                    mass_add(sm.h2[r], sb, p);
                 } else if (sb == b2) {
                     const int slot = atomicAdd(&sm.ncnt[r], 1);
-                    if (slot < kNCap) sm.h1[r][slot] = ncomp(x[j], (uint32_t)(col + e0 + j));
+                    if (slot < kNCap) sm.list[r][slot] = ncomp(x[j], (uint32_t)(col + e0 + j));
                 }
             }
         }
@@ -757,7 +782,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 // the coarse histograms start empty (nothing reads them between
                 // the previous unit's cut and this barrier)
                 if (nuc)
-                    for (int i = t; i < 2 * kNB1; i += kFConsumers) (&sm.h1[0][0])[i] = 0ull;
+                    for (int i = t; i < 4 * kNB1; i += kFConsumers) (&sm.h1[0][0][0])[i] = 0u;
                 if (!fsync(sm, g)) break;
                 // every warp combines the seven warps' statistics itself; red is
                 // double-buffered by unit, so no second barrier is needed
@@ -789,7 +814,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 const int r = warp;
                 unsigned long long bef = 0ull;
                 if (pass == 1) {
-                    const int bin = warp_cross(sm.h1[r], kNB1, target, &bef, lane);
+                    const int bin = warp_cross(sm.h1[r], target, &bef, lane);
                     if (lane == 0) {
                         sm.nb[r][0] = bin;
                         sm.nbase[r] = bef;
@@ -797,7 +822,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 } else if (pass == 2) {
                     const unsigned long long base = sm.nbase[r];
                     const int bin = sm.nb[r][0] < 0 ? -1
-                                                    : warp_cross(sm.h2[r], kNB2, target > base ? target - base : 0ull,
+                                                    : warp_cross(sm.h2[r], target > base ? target - base : 0ull,
                                                                  &bef, lane);
                     if (lane == 0) {
                         sm.nb[r][1] = bin;
@@ -808,7 +833,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                     double K = 0.0;
                     const int cnt = sm.ncnt[r];
                     const bool ok = sm.nb[r][1] >= 0 &&
-                                    warp_cut(sm.h1[r], min(cnt, kNCap + 1), sm.nbase[r], (double)Pf,
+                                    warp_cut(sm.list[r], min(cnt, kNCap + 1), sm.nbase[r], (double)Pf,
                                              c, r == 0 ? nmcp : nmcq, r == 0 ? invp : invq, &ck, &ci, &K, lane);
                     if (lane == 0) {
                         sm.cut_key[r] = ck;
@@ -818,7 +843,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 }
             }
             if (pass == 1)  // the fine histograms start empty
-                for (int i = t; i < 2 * kNB2; i += kFConsumers) (&sm.h2[0][0])[i] = 0ull;
+                for (int i = t; i < 4 * kNB2; i += kFConsumers) (&sm.h2[0][0][0])[i] = 0u;
             if (pass == 2 && t < 2) sm.ncnt[t] = 0;
             if (!fsync(sm, g)) break;
             if (pass == 3) {
