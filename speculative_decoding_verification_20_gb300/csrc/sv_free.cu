@@ -518,41 +518,48 @@ __device__ bool warp_cut(unsigned long long* list, int n, unsigned long long bas
     return true;
 }
 
-// One tile of a nucleus pass for row r (max M, nmc = row_nmc(M, c), 1/sum inv);
-// the thread holds the
-// vectors vbase + 32 i of the segment.  Pass 1 adds the
-// masses to the coarse histogram, pass 2 those of the crossing coarse bin to
-// the fine histogram, pass 3 collects the elements of the crossing fine bin.
-template <typename TIn>
+// Bin coordinate of a logit: t = -8 * (l * c + nmc), the distance below the row
+// maximum in 1/8 log2 units, from the weight's own exponent (the scaling by 8
+// is exact).  It is the same number in every pass, and monotone in l, so the
+// bins partition the row in (logit desc) order consistently.  Coarse bin
+// (int)t for t < 512 (t may be a rounding below 0 at the maximum: bin 0);
+// fine bin (int)((t - b1) * 512) inside coarse bin b1.
+//
+// One tile of a nucleus pass for row r (c, nmc = row_nmc(M, c), 1/sum inv);
+// the thread holds the vectors vbase + 32 i of the segment (FULL: all whole).
+// Pass 1 adds the masses to the coarse histogram, pass 2 those of the
+// crossing coarse bin to the fine histogram, pass 3 collects the elements of
+// the crossing fine bin.  Passes 2 and 3 test a bin by two compares on t and
+// convert only the few logits inside it.
+template <typename TIn, bool FULL>
 __device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVec], int n, int vbase, int col,
-                                             int pass, int r, float M, float c, float nmc, float inv) {
+                                             int pass, int r, float c, float nmc, float inv) {
     using F = FE<TIn>;
-    const float s1 = (float)kNB1 / kNDmax;
-    const float s2 = (float)kNB2 * (float)kNB1 / kNDmax;
+    constexpr float kTMax = (float)kNB1;  // t >= 512: more than kNDmax below the maximum
+    static_assert(kNB1 * 8 == (int)(kNDmax * 64), "coarse bins are 1/8 log2 unit");
     const int b1 = pass >= 2 ? sm.nb[r][0] : -1;
     const int b2 = pass >= 3 ? sm.nb[r][1] : -1;
-    const float d1 = (float)b1 * (kNDmax / (float)kNB1);
+    const float lo1 = b1 <= 0 ? -INFINITY : (float)b1;            // coarse bin b1 is [lo1, hi1)
+    const float hi1 = b1 >= kNB1 - 1 ? kTMax : (float)(b1 + 1);
+    const float base1 = (float)max(b1, 0);
 #pragma unroll
     for (int i = 0; i < kFVec; ++i) {
         const int e0 = (vbase + 32 * i) * F::VEC;
-        const int valid = min(F::VEC, n - e0);
-        if (valid <= 0) continue;
+        const int valid = FULL ? F::VEC : min(F::VEC, n - e0);
+        if (!FULL && valid <= 0) continue;
         float x[F::VEC];
         F::unpack(v[i], x);
 #pragma unroll
         for (int j = 0; j < F::VEC; ++j) {
-            if (j >= valid) continue;
-            const float d = (M - x[j]) * c;
-            if (!(d < kNDmax)) continue;
-            const int bb = min(kNB1 - 1, (int)(d * s1));
+            if (!FULL && j >= valid) continue;
+            const float e = fmaf(x[j], c, nmc);  // the weight's exponent
+            const float t = -8.0f * e;
             if (pass == 1) {
-                const float p = prob_f(x[j], c, nmc, inv);
-                mass_add(sm.h1[r], bb, p);
-            } else if (bb == b1) {
-                const int sb = min(kNB2 - 1, max(0, (int)((d - d1) * s2)));
+                if (t < kTMax) mass_add(sm.h1[r], (int)t, fex2(e) * inv);
+            } else if (t >= lo1 && t < hi1) {
+                const int sb = min(kNB2 - 1, max(0, (int)((t - base1) * (float)kNB2)));
                 if (pass == 2) {
-                    const float p = prob_f(x[j], c, nmc, inv);
-                    mass_add(sm.h2[r], sb, p);
+                    mass_add(sm.h2[r], sb, fex2(e) * inv);
                 } else if (sb == b2) {
                     const int slot = atomicAdd(&sm.ncnt[r], 1);
                     if (slot < kNCap) sm.list[r][slot] = ncomp(x[j], (uint32_t)(col + e0 + j));
@@ -805,8 +812,13 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
         if (pass < kPassFinal) {
             // ---- nucleus passes: the last kept token of each row (top-p < 1)
             if (dead) continue;
-            nucleus_tile<TIn>(sm, vp, n, vbase, col, pass, 0, Mp, c, nmcp, invp);
-            if (pair) nucleus_tile<TIn>(sm, vq, n, vbase, col, pass, 1, Mq, c, nmcq, invq);
+            if (n == TS) {
+                nucleus_tile<TIn, true>(sm, vp, n, vbase, col, pass, 0, c, nmcp, invp);
+                if (pair) nucleus_tile<TIn, true>(sm, vq, n, vbase, col, pass, 1, c, nmcq, invq);
+            } else {
+                nucleus_tile<TIn, false>(sm, vp, n, vbase, col, pass, 0, c, nmcp, invp);
+                if (pair) nucleus_tile<TIn, false>(sm, vq, n, vbase, col, pass, 1, c, nmcq, invq);
+            }
             if (tile != ntiles - 1) continue;
             if (!fsync(sm, g)) break;
             const unsigned long long target = (unsigned long long)((double)Pf * (double)kMassScale);
