@@ -46,13 +46,19 @@ namespace sv {
 namespace {
 
 constexpr int kFStages = 3;
-constexpr int kFWarps = kFreeWarps;  // with the producer, 8 warps: 2 CTAs per SM at up to 128 registers
-constexpr int kFConsumers = 32 * kFWarps;
-constexpr int kFThreads = kFConsumers + 32;
-constexpr int kFSegBytes = kFreeSegBytes;
 constexpr int kFVec = kFreeBlockBytes / 16 / 32;  // 16-byte vectors per lane per segment (4)
 constexpr unsigned long long kFWaitNs = 2000000000ull;
-static_assert(kFVec * 16 * kFConsumers == kFSegBytes, "segment geometry");
+// W consumer warps and a producer warp; up to 128 registers a thread either way
+// (7: 2 CTAs per SM, 15: 1 CTA per SM)
+template <int W>
+struct FGeo {
+    static constexpr int kWarps = W;
+    static constexpr int kConsumers = 32 * W;
+    static constexpr int kThreads = kConsumers + 32;
+    static constexpr int kSegBytes = W * kFreeBlockBytes;
+    static constexpr int kCtasPerSm = W == kFreeWarpsNarrow ? 2 : 1;
+    static_assert(W < 32 && kFVec * 16 * kConsumers == kSegBytes, "segment geometry");
+};
 constexpr int kTailWarps = 8;
 
 // nucleus (top-p) cut of a row: probability mass histograms over the distance
@@ -73,14 +79,15 @@ static_assert(1023ull * SV_MAX_VOCAB < (1ull << 32), "low parts of a bin fit 32 
 // histogram, 3 collect the crossing elements, 4 alpha and residual weights
 constexpr int kPassFinal = 4;
 
+template <int W>
 struct FreeSmem {
-    alignas(128) uint8_t buf[kFStages][2][kFSegBytes];  // [stage][target, draft segment]
+    alignas(128) uint8_t buf[kFStages][2][FGeo<W>::kSegBytes];  // [stage][target, draft segment]
     uint64_t full[kFStages];
     uint64_t empty[kFStages];
     uint64_t gsync;
     int4 hdr[kFStages];               // unit index (-1: no more work), pass, tile, elements
     int4 uhdr[kFStages];              // the unit: list item (b << 8 | u), gamma_b, T and top-p (float bits)
-    float red[2][kFWarps][8];         // per warp: row statistics (by the parity of the CTA's unit count)
+    float red[2][W][8];               // per warp: row statistics (by the parity of the CTA's unit count)
     uint32_t h1[2][2][kNB1];          // per row: coarse mass histogram (2^40 fixed point) as [high, low] parts
     uint32_t h2[2][2][kNB2];          // per row: fine mass histogram, the same way
     unsigned long long list[2][kNCap];  // per row: the elements of the crossing fine bin
@@ -91,8 +98,9 @@ struct FreeSmem {
     float kinv[2];                    // per row: 1 / (sum x kept mass); -1: too many ties at the cut
 };
 
-// two CTAs per SM: 228 KB of shared memory less 1 KB reserved per CTA
-static_assert(sizeof(FreeSmem) <= 115712, "the whole-row kernel must fit twice on an SM");
+// 228 KB of shared memory per SM, less 1 KB reserved per CTA
+static_assert(sizeof(FreeSmem<kFreeWarpsNarrow>) <= 115712, "the narrow whole-row kernel must fit twice on an SM");
+static_assert(sizeof(FreeSmem<kFreeWarpsWide>) <= 232448, "the wide whole-row kernel must fit on an SM");
 
 // ---------------------------------------------------------------------------
 // PTX helpers (mbarriers, TMA bulk copies); every wait is bounded
@@ -139,7 +147,8 @@ struct FSync {
     uint32_t ph;
     bool ok;
 };
-__device__ __forceinline__ bool fsync(FreeSmem& sm, FSync& g) {
+template <int W>
+__device__ __forceinline__ bool fsync(FreeSmem<W>& sm, FSync& g) {
     __syncwarp();
     if (!g.ok) return false;
     if ((threadIdx.x & 31) == 0) fbar_arrive(&sm.gsync);
@@ -374,8 +383,9 @@ __device__ __forceinline__ void warp_online(const Online& o, float c, float* wm,
 // the seven warps' (maximum, rescaled sum) pairs in red[w][col], [col + 1]:
 // lane w rescales warp w's sum to the common maximum, and the warp adds them
 // with a compensated sum.  M = -inf when the row has no finite logit.
+template <int W>
 __device__ __forceinline__ void combine_stats(const float (*red)[8], int col, float c, int lane, float* M, float* S) {
-    const float wm = lane < kFWarps ? red[lane][col] : -INFINITY;
+    const float wm = lane < W ? red[lane][col] : -INFINITY;
     const float m = warp_maxf(wm);
     float x = 0.0f;
     if (m > -INFINITY && wm > -INFINITY) x = red[lane][col + 1] * fex2(row_nmc(m, c) - row_nmc(wm, c));
@@ -531,8 +541,8 @@ __device__ bool warp_cut(unsigned long long* list, int n, unsigned long long bas
 // crossing coarse bin to the fine histogram, pass 3 collects the elements of
 // the crossing fine bin.  Passes 2 and 3 test a bin by two compares on t and
 // convert only the few logits inside it.
-template <typename TIn, bool FULL>
-__device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVec], int n, int vbase, int col,
+template <typename TIn, bool FULL, int W>
+__device__ __forceinline__ void nucleus_tile(FreeSmem<W>& sm, const uint4 (&v)[kFVec], int n, int vbase, int col,
                                              int pass, int r, float c, float nmc, float inv) {
     using F = FE<TIn>;
     constexpr float kTMax = (float)kNB1;  // t >= 512: more than kNDmax below the maximum
@@ -569,12 +579,14 @@ __device__ __forceinline__ void nucleus_tile(FreeSmem& sm, const uint4 (&v)[kFVe
     }
 }
 
-template <typename TIn, bool TMA>
-__global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
+template <typename TIn, bool TMA, int W>
+__global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_kernel(Args a) {
     using F = FE<TIn>;
-    constexpr int TS = kFSegBytes / (int)sizeof(TIn);  // elements per segment (tile)
+    constexpr int kFWarps = W;
+    constexpr int kFConsumers = FGeo<W>::kConsumers;
+    constexpr int TS = FGeo<W>::kSegBytes / (int)sizeof(TIn);  // elements per segment (tile)
     extern __shared__ __align__(128) uint8_t fsm_raw[];
-    FreeSmem& sm = *reinterpret_cast<FreeSmem*>(fsm_raw);
+    FreeSmem<W>& sm = *reinterpret_cast<FreeSmem<W>*>(fsm_raw);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int V = a.V, G = a.G;
     const int ntiles = (V + TS - 1) / TS;
@@ -688,6 +700,7 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
         R.cutp = cutp;
         R.cutq = cutq;
         R.flags = flags;
+        for (int i = kFWarps; i < kFreeWarpsWide; ++i) R.alpha[i] = 0.0f;
     };
     while (true) {
         if (!__all_sync(0xFFFFFFFFu, fbar_wait(&sm.full[stage], ph))) {
@@ -793,8 +806,8 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
                 if (!fsync(sm, g)) break;
                 // every warp combines the seven warps' statistics itself; red is
                 // double-buffered by unit, so no second barrier is needed
-                combine_stats(red, 0, c, lane, &Mp, &Sp);
-                combine_stats(red, 2, c, lane, &Mq, &Sq);
+                combine_stats<W>(red, 0, c, lane, &Mp, &Sp);
+                combine_stats<W>(red, 2, c, lane, &Mq, &Sq);
                 const bool anynf = __any_sync(0xFFFFFFFFu, lane < kFWarps && red[lane][4] != 0.0f);
                 // a row with a NaN or +inf logit, or without any finite one
                 dead = anynf || !(Mp > -INFINITY) || (pair && !(Mq > -INFINITY));
@@ -813,11 +826,11 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
             // ---- nucleus passes: the last kept token of each row (top-p < 1)
             if (dead) continue;
             if (n == TS) {
-                nucleus_tile<TIn, true>(sm, vp, n, vbase, col, pass, 0, c, nmcp, invp);
-                if (pair) nucleus_tile<TIn, true>(sm, vq, n, vbase, col, pass, 1, c, nmcq, invq);
+                nucleus_tile<TIn, true, W>(sm, vp, n, vbase, col, pass, 0, c, nmcp, invp);
+                if (pair) nucleus_tile<TIn, true, W>(sm, vq, n, vbase, col, pass, 1, c, nmcq, invq);
             } else {
-                nucleus_tile<TIn, false>(sm, vp, n, vbase, col, pass, 0, c, nmcp, invp);
-                if (pair) nucleus_tile<TIn, false>(sm, vq, n, vbase, col, pass, 1, c, nmcq, invq);
+                nucleus_tile<TIn, false, W>(sm, vp, n, vbase, col, pass, 0, c, nmcp, invp);
+                if (pair) nucleus_tile<TIn, false, W>(sm, vq, n, vbase, col, pass, 1, c, nmcq, invq);
             }
             if (tile != ntiles - 1) continue;
             if (!fsync(sm, g)) break;
@@ -1009,11 +1022,10 @@ __global__ void __launch_bounds__(kFThreads, 2) free_kernel(Args a) {
 template <typename TIn>
 __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
     using F = FE<TIn>;
-    constexpr int TS = kFSegBytes / (int)sizeof(TIn);       // elements per segment
     constexpr int BS = kFreeBlockBytes / (int)sizeof(TIn);  // elements per block
     constexpr int CH = 32 * F::VEC;                         // a block is read in chunks of VEC per lane
     constexpr int NCH = BS / CH;
-    static_assert(NCH * CH == BS && BS * kFWarps == TS, "block geometry");
+    static_assert(NCH * CH == BS, "block geometry");
     const int lane = threadIdx.x & 31;
     grid_dependency_wait();  // the free kernel's records
     grid_dependents_go();
@@ -1098,7 +1110,7 @@ __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
         int token = -1;
         if (blk >= 0) {
             const double vrel = v - bef;
-            const int e_start = (blk / kFWarps) * TS + (blk % kFWarps) * BS;
+            const int e_start = blk * BS;  // blocks are consecutive in the row whatever the warp count
             const int e_end = min(V, e_start + BS);
             CF run{0.0f, 0.0f};
             int lastel = -1;
@@ -1147,7 +1159,7 @@ __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
         int accept = 0;
         float alpha_v = 0.0f;
         if (pair) {
-            alpha_v = cf_val(warp_cf_sum(CF{lane < kFWarps ? rec->alpha[lane] : 0.0f, 0.0f}));
+            alpha_v = cf_val(warp_cf_sum(CF{lane < kFreeWarpsWide ? rec->alpha[lane] : 0.0f, 0.0f}));
             if (lane == 0) {
                 const int xt = a.draft_tokens[(size_t)b * G + u];
                 const float lpx = F::load(trow, xt), lqx = F::load(drow, xt);
@@ -1175,24 +1187,26 @@ __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
     }
 }
 
-template <typename TIn, bool TMA>
-cudaError_t launch_free_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) {
-    auto k = free_kernel<TIn, TMA>;
-    const int smem = (int)sizeof(FreeSmem);
+template <typename TIn, bool TMA, int W>
+cudaError_t launch_free_w(const Args& a0, int sms, cudaStream_t s, void* const ev[2]) {
+    auto k = free_kernel<TIn, TMA, W>;
+    const int smem = (int)sizeof(FreeSmem<W>);
     static const bool attr_ok = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
                                 cudaSuccess;
     if (!attr_ok) return cudaErrorInvalidValue;
     static const int occ = [&] {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kFThreads, smem) != cudaSuccess) n = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, FGeo<W>::kThreads, smem) != cudaSuccess) n = 1;
         return n > 0 ? n : 1;
     }();
+    Args a = a0;
+    a.free_nblk = free_blocks(a.V, sizeof(TIn) == 2 ? SV_BF16 : SV_F32, W);  // the record stride of this variant
     const long long units = (long long)a.B * (a.G + 1);
     long long grid = (long long)occ * sms;
     if (grid > units) grid = units;
     if (grid < 1) grid = 1;
     if (ev && ev[0]) cudaEventRecord((cudaEvent_t)ev[0], s);
-    cudaError_t e = launch_pdl(k, dim3((unsigned)grid), dim3(kFThreads), (size_t)smem, s, a);
+    cudaError_t e = launch_pdl(k, dim3((unsigned)grid), dim3(FGeo<W>::kThreads), (size_t)smem, s, a);
     if (e != cudaSuccess) return e;
     if (ev && ev[1]) cudaEventRecord((cudaEvent_t)ev[1], s);
     // the tail: a warp per unit, up to 4 CTAs of 8 warps per SM in flight
@@ -1200,6 +1214,15 @@ cudaError_t launch_free_t(const Args& a, int sms, cudaStream_t s, void* const ev
     if (tgrid > 4LL * sms) tgrid = 4LL * sms;
     if (tgrid < 1) tgrid = 1;
     return launch_pdl(free_tail_kernel<TIn>, dim3((unsigned)tgrid), dim3(32 * kTailWarps), 0, s, a);
+}
+
+// The narrow variant (7 consumer warps, 2 CTAs per SM) unless the batch has
+// fewer units than its CTA slots: then each unit gets a whole SM's 15 warps.
+template <typename TIn, bool TMA>
+cudaError_t launch_free_t(const Args& a, int sms, cudaStream_t s, void* const ev[2]) {
+    const long long units = (long long)a.B * (a.G + 1);
+    if (units < 2LL * sms) return launch_free_w<TIn, TMA, kFreeWarpsWide>(a, sms, s, ev);
+    return launch_free_w<TIn, TMA, kFreeWarpsNarrow>(a, sms, s, ev);
 }
 
 }  // namespace

@@ -47,12 +47,14 @@ constexpr int kStreamMaxK = SV_STREAM_MAX_TOP_K;
 constexpr int kListCap = 512;   // candidates one piece hands to the combine kernel
 constexpr int kSortCap = 2048;  // candidates per row sorted in shared memory by the combine kernel
 constexpr int kDenseThreads = 256;
-// free kernel geometry: a ring stage holds one 14 KB segment of each row of a
-// unit; each of the 7 consumer warps owns a contiguous 2 KB block of it
-constexpr int kFreeWarps = 7;
-constexpr int kFreeSegBytes = 14336;
-constexpr int kFreeBlockBytes = kFreeSegBytes / kFreeWarps;
-static_assert(kFreeBlockBytes * kFreeWarps == kFreeSegBytes && kFreeBlockBytes % 512 == 0, "free block geometry");
+// free kernel geometry: each consumer warp owns a contiguous 2 KB block of a
+// ring segment, so block j of a row always starts at token j * block_elems.
+// The kernel runs with 7 consumer warps (a 14 KB segment, 2 CTAs per SM) or,
+// for batches with fewer units than those CTA slots, with 15 (30 KB, 1 CTA per
+// SM, twice the warps per unit).
+constexpr int kFreeBlockBytes = 2048;
+constexpr int kFreeWarpsNarrow = 7;
+constexpr int kFreeWarpsWide = 15;
 
 // counters at the head of the workspace list area
 enum : int {
@@ -78,10 +80,9 @@ struct FreeRec {
     float invp, invq;               // 1 / (sum x kept mass) of each row
     unsigned long long cutp, cutq;  // last kept element (okey << 32 | ~id); 0: the row is not cut
     uint32_t flags;
-    float alpha[kFreeWarps];        // per-warp partial sums of min(p, q)
-    uint32_t pad[4];
+    float alpha[kFreeWarpsWide];    // per-warp partial sums of min(p, q) (0 past the kernel's warps)
 };
-static_assert(sizeof(FreeRec) == 80, "free record size");
+static_assert(sizeof(FreeRec) == 96, "free record size");
 
 // per-sequence plan (32 bytes)
 struct SeqInfo {
@@ -132,7 +133,7 @@ struct Args {
     uint32_t* cand_cnt;       // [stream rows * ppr]
     FreeRec* free_rec;        // [units] by free list index
     float* free_blk;          // [units][2][free_nblk]: per block sums of r (residual weights) and p
-    int free_nblk;            // blocks per row
+    int free_nblk;            // blocks per row of the free kernel's variant (set by its launcher)
 };
 
 struct WsLayout {
@@ -149,9 +150,10 @@ static_assert(((SV_MAX_VOCAB + kTilesPerPiece * (kTileBytes / 4) - 1) / (kTilesP
                   kSortCap,
               "pieces per row times the list cap must fit the combine sort");
 
-__host__ __device__ inline int free_seg_elems(int dtype) { return kFreeSegBytes / (dtype == SV_BF16 ? 2 : 4); }
-__host__ __device__ inline int free_blocks(int V, int dtype) {
-    return (V + free_seg_elems(dtype) - 1) / free_seg_elems(dtype) * kFreeWarps;
+// blocks per row written by the free kernel with `warps` consumer warps (whole segments)
+__host__ __device__ inline int free_blocks(int V, int dtype, int warps) {
+    const int seg = warps * (kFreeBlockBytes / (dtype == SV_BF16 ? 2 : 4));
+    return (V + seg - 1) / seg * warps;
 }
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -175,7 +177,9 @@ __host__ __device__ inline WsLayout ws_layout(int B, int G, int V, int dtype) {
     L.counts = o;      o = align_up(o + 64, 256);
     L.cand_cnt = o;    o = align_up(o + 4 * rows * L.ppr, 256);
     L.cand = o;        o = align_up(o + 8 * rows * L.ppr * kListCap, 256);
-    L.free_nblk = free_blocks(V, dtype);
+    L.free_nblk = free_blocks(V, dtype, kFreeWarpsNarrow) > free_blocks(V, dtype, kFreeWarpsWide)
+                      ? free_blocks(V, dtype, kFreeWarpsNarrow)
+                      : free_blocks(V, dtype, kFreeWarpsWide);  // room for either variant
     L.free_rec = o;    o = align_up(o + sizeof(FreeRec) * units, 256);
     L.free_blk = o;    o = align_up(o + 4 * units * 2 * (size_t)L.free_nblk, 256);
     L.total = o;
