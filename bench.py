@@ -36,11 +36,14 @@ FALLBACK_HBM_GBS = 6800.0
 # the whole-row kernel of rows without top-k and its per-unit tail, and the
 # dense cluster kernel (a kernel whose path no row takes exits at once)
 LAUNCHES_PER_STEP = 6
-# sources of the select kernel, whose DRAM traffic profiles/traffic.json records
-KERNEL_SOURCES = ("speculative_decoding_verification_20_gb300/csrc/sv_stream.cu",
-                  "speculative_decoding_verification_20_gb300/csrc/sv_keys.cuh",
-                  "speculative_decoding_verification_20_gb300/csrc/sv_internal.cuh",
-                  "speculative_decoding_verification_20_gb300/csrc/sv_finalize.cuh")
+# sources of each kernel whose DRAM traffic profiles/traffic.json records: a
+# record counts only while these files are unchanged since its capture
+_CSRC = "speculative_decoding_verification_20_gb300/csrc/"
+KERNEL_SOURCES = {
+    "stream": tuple(_CSRC + f for f in ("sv_stream.cu", "sv_keys.cuh", "sv_internal.cuh", "sv_finalize.cuh")),
+    "free": tuple(_CSRC + f for f in ("sv_free.cu", "sv_cf.cuh", "sv_warp_sort.cuh", "sv_internal.cuh",
+                                      "sv_finalize.cuh")),
+}
 
 
 def measured_peak():
@@ -52,24 +55,27 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(path: str = "stream") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[path]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
-    valid only while the kernel sources are unchanged since that capture."""
+def recorded_traffic(workload: str, path: str, default_batch: bool):
+    """DRAM bytes per launch of the dominant kernel at the workload's full size,
+    from the committed ncu summary; None for another batch size, another
+    kernel, or once that kernel's sources changed since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f).get(workload)
     except Exception:
         return None
-    if not rec or rec.get("kernel_hash") != kernel_hash():
+    if not default_batch or not rec or path not in KERNEL_SOURCES or rec.get("path") != path:
+        return None
+    if rec.get("kernel_hash") != kernel_hash(path):
         return None
     return rec.get("bytes_per_launch")
 
@@ -346,7 +352,7 @@ def main():
             dist.destroy_process_group()
         return 0
     clocks = clk.summary(wall0, wall1)
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload, main, args.batch is None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -360,7 +366,7 @@ def main():
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "kernel": {"stream": "select_kernel (streaming top-k path)",
-                                "free": "free_kernel (whole-row path of unfiltered rows)",
+                                "free": "free_kernel (whole-row path: rows without top-k)",
                                 "dense": "dense_kernel (cluster path)"}[main],
                      "kernel_ms": kernel_ms_avg, "algorithmic_bytes_per_launch": main_bytes,
                      "traffic": traffic},

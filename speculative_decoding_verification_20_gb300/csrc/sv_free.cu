@@ -421,14 +421,19 @@ __device__ __forceinline__ float exp2_prod(float l, float M, float chi, float cl
 __device__ __forceinline__ unsigned long long ncomp(float x, uint32_t id) {
     return ((unsigned long long)okey32(__float_as_uint(x)) << 32) | (unsigned long long)(~id);
 }
-__device__ __forceinline__ unsigned long long mass_fix(float p) { return __float2ull_rz(p * kMassScale); }
-// add the mass of probability p to bin `bin` of a split histogram h[2][n]
+// Add the mass of probability p (0 <= p <= 1) to bin `bin` of a split
+// histogram h[2][n].  The parts of m = floor(p * 2^40) come from fp32 alone:
+// with t = p * 2^30 (exact), hi = trunc(t) and lo = floor((t - hi) * 2^10), where
+// t - hi is exact, so hi * 2^10 + lo = m exactly (the same integers as a 64-bit
+// conversion, which would run on this GPU's narrow fp64 pipe).
 template <int N>
 __device__ __forceinline__ void mass_add(uint32_t (&h)[2][N], int bin, float p) {
-    const unsigned long long m = mass_fix(p);
-    if (m == 0ull) return;
-    atomicAdd(&h[0][bin], (uint32_t)(m >> kMassLoBits));
-    const uint32_t lo = (uint32_t)m & ((1u << kMassLoBits) - 1u);
+    static_assert(kMassLoBits == 10, "the split below is for 2^40 = 2^30 * 2^10");
+    const float t = p * 1073741824.0f;  // 2^30
+    const float hf = truncf(t);
+    const uint32_t hi = (uint32_t)hf;
+    const uint32_t lo = (uint32_t)((t - hf) * 1024.0f);
+    if (hi) atomicAdd(&h[0][bin], hi);
     if (lo) atomicAdd(&h[1][bin], lo);
 }
 template <int N>
