@@ -15,7 +15,7 @@ namespace sv {
 
 
 // ---------------------------------------------------------------------------
-// plan kernel: one CTA walks the batch in chunks of kPlanThreads sequences.
+// plan kernel: one CTA walks the batch in chunks of blockDim.x (<= 1024) sequences.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t block_excl_scan_1024(uint32_t v, uint32_t* s_warp, uint32_t* total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -280,7 +280,10 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
         return SV_ECUDA;
     if (q_out && cudaMemsetAsync(q_out, 0, sizeof(float) * (size_t)B * gamma_max * V, s) != cudaSuccess)
         return SV_ECUDA;
-    plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
+    // one CTA of min(1024, B rounded up to a warp) threads: a small batch pays
+    // for no idle warps at the plan's block-wide scans
+    const int plan_threads = B >= kPlanThreads ? kPlanThreads : (B + 31) / 32 * 32;
+    plan_kernel<<<1, plan_threads, 0, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
 
     const bool vector = ((size_t)V * es) % 16 == 0;
