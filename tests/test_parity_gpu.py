@@ -172,6 +172,25 @@ def test_exact_ties(dtype):
         assert_ok(rep)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_whole_row_top_p_both_variants(dtype):
+    """Rows with top-p and no top-k take the whole-row kernel's nucleus cut.  A batch
+    with at least two units per SM runs its 7-warp variant, a smaller one its 15-warp
+    variant; both against the oracle, with the probability outputs (the kernel's
+    generic per-element path) and without them (its packed full-tile path).  V spans
+    one full segment and a ragged one in either variant."""
+    from dataclasses import replace
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    G, V = 4, 9000
+    for B in ((2 * sms) // (G + 1) + 8, 16):
+        wl = _rand_batch(B, G, V, dtype, seed=40 + B, T=np.linspace(0.5, 1.5, B))
+        wl = replace(wl, top_p=torch.as_tensor(np.linspace(0.5, 0.999, B), dtype=torch.float32),
+                     num_draft=torch.as_tensor(1 + np.arange(B) % G, dtype=torch.int32))
+        for probs in (False, True):
+            rep, _, _ = run(wl, probs=probs)
+            assert_ok(rep)
+
+
 def test_mixed_parameters_per_row():
     B, G, V = 40, 5, 3000
     gen = torch.Generator().manual_seed(3)
