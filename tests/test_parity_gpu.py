@@ -303,3 +303,47 @@ def test_streaming_threshold_redo_and_overflow(dtype):
                                 torch.full((B,), 0.95, dtype=torch.float32), 40 + k)
         rep, _, _ = run(wl, probs=True)
         assert_ok(rep)
+
+
+# ---------------------------------------------------------------------------
+# The output law on the GPU: the first emitted token follows the (filtered)
+# target distribution p whatever the draft q ("Fast Inference from
+# Transformers via Speculative Decoding" review page, Algorithm 1 and its
+# correctness argument)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("k,p_top", [(None, None), (3, None), (None, 0.9)])
+def test_chisquare_first_token_law_million_sequences(k, p_top):
+    """10^6 sequences (5 calls of 2 * 10^5 with different seeds; one call of 10^6
+    would need a 12 GB workspace for the select kernel's candidate lists, sized
+    for 512 per row whatever V), V = 8, gamma = 1, one (p, q) pair for all, x drawn
+    from the filtered q: the first emitted token (the accepted draft or the
+    residual draw) must follow the filtered p.  No filter runs the whole-row
+    kernel, top-k 3 the select and combine kernels, top-p 0.9 the nucleus cut.
+    The filtered laws come from the oracle (one row, probability outputs)."""
+    stats = pytest.importorskip("scipy.stats")
+    rng = np.random.default_rng(2024 + (k or 0) + int(100 * (p_top or 0)))
+    V, B, calls = 8, 200_000, 5
+    lp = np.log(rng.dirichlet(np.ones(V))).astype(np.float32)
+    lq = np.log(rng.dirichlet(np.ones(V))).astype(np.float32)
+    kk = None if k is None else np.array([k], dtype=np.int32)
+    pp = None if p_top is None else np.array([p_top], dtype=np.float32)
+    one = oracle.verify(np.stack([lp, lp])[None], lq[None, None], np.zeros((1, 1), dtype=np.int32),
+                        np.ones(1, dtype=np.float32), None, kk, pp, seed=0, probs=True)
+    p_law, q_law = one.p_out[0, 0], one.q_out[0, 0]
+    dev = torch.device("cuda")
+    tgt = torch.as_tensor(np.broadcast_to(np.stack([lp, lp])[None], (B, 2, V)).copy(), device=dev)
+    drf = torch.as_tensor(np.broadcast_to(lq[None, None], (B, 1, V)).copy(), device=dev)
+    counts = np.zeros(V, dtype=np.int64)
+    for c in range(calls):
+        x = rng.choice(V, size=(B, 1), p=q_law / q_law.sum()).astype(np.int32)
+        res = sv.spec_verify(tgt, drf, torch.as_tensor(x, device=dev), 1.0, None,
+                             None if k is None else k, None if p_top is None else p_top, seed=77 + c)
+        torch.cuda.synchronize()
+        assert (to_np(res["row_status"]) == 0).all()
+        counts += np.bincount(to_np(res["out_tokens"])[:, 0], minlength=V)
+    n = B * calls
+    support = p_law > 0
+    assert counts[~support].sum() == 0, (counts, p_law)
+    _, pval = stats.chisquare(counts[support], p_law[support] / p_law[support].sum() * n)
+    assert pval > 1e-3, (counts / n, p_law, pval)
