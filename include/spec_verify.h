@@ -116,7 +116,9 @@ int spec_verify(const void* target_logits, const void* draft_logits, int dtype, 
 /* Path selection for spec_verify_ex (testing and measurement). */
 typedef enum {
     SV_PATH_AUTO = 0,  /* greedy and top_k <= SV_STREAM_MAX_TOP_K rows: streaming top-k path; rows with no
-                          top-k and no top-p: whole-row path; others: dense cluster path */
+                          top-k (with or without top-p): whole-row path; top_k > SV_STREAM_MAX_TOP_K: dense
+                          cluster path (which also finishes whole-row units whose nucleus cut holds more
+                          than 256 tied logits) */
     SV_PATH_DENSE = 1  /* every row through the dense (whole-row, cluster) path */
 } sv_path;
 
@@ -132,9 +134,9 @@ typedef enum {
  *   path       sv_path
  *   ev_stream  two cudaEvent_t (or NULL) recorded on `stream` immediately
  *              before and after the streaming top-k kernel
- *   ev_dense   the same around the dense cluster kernel (top-p, top-k > 256)
- *   ev_free    the same around the whole-row kernel of unfiltered rows
- *              (no top-k, no top-p)
+ *   ev_dense   the same around the dense cluster kernel (top-k > 256)
+ *   ev_free    the same around the whole-row kernel of rows with no top-k
+ *              (its per-unit tail kernel follows, outside the events)
  */
 typedef struct {
     uint32_t struct_size;

@@ -153,7 +153,7 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.T
     request, p_out / q_out (probs=True) and pos_accept / pos_token (positions=True).
     events: {"stream": (begin, end), "dense": (begin, end), "free": (begin, end)} torch.cuda.Event
     pairs that the library records on the launching stream around its streaming top-k, dense
-    cluster and unfiltered whole-row kernels.
+    cluster and whole-row (no top-k) kernels.
     """
     lib = load_library()
     if not (target.is_cuda and draft.is_cuda):

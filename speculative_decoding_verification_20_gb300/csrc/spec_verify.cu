@@ -1,8 +1,10 @@
 // spec_verify.cu -- host side of the C ABI declared in include/spec_verify.h.
 //
 // Validates arguments on the host (nothing is enqueued on an error), then
-// enqueues on the caller's stream: plan kernel -> streaming top-k kernel ->
-// dense cluster kernel.  No host synchronisation (spec_verify_host excepted).
+// enqueues on the caller's stream: plan kernel -> select (streaming top-k) ->
+// combine -> whole-row kernel -> its per-unit tail -> dense cluster kernel,
+// each after the plan as a programmatic dependent launch.  No host
+// synchronisation (spec_verify_host excepted).
 #include <cuda_runtime.h>
 
 #include <cstdio>

@@ -67,8 +67,8 @@ enum : int {
     kCntFreeNext = 6
 };
 
-// streaming top-k path; whole-row cluster path (top-p, large top-k); whole-row
-// path of unfiltered rows (no top-k, no top-p)
+// streaming top-k path; cluster path (top-k > 256, and handed-over units);
+// whole-row path of rows with no top-k (with or without top-p)
 enum : uint32_t { kModeErr = 0, kModeStream = 1, kModeDense = 2, kModeFree = 3 };
 
 // Per-unit record of the free kernel for its tail kernel (one per entry of the
