@@ -11,6 +11,8 @@ gcc and marshals numpy arrays through ctypes.
 
 Parity status per function (also recorded in the design doc):
   * normalise / alpha / acceptance / residual -- pinned (tests/test_oracle_pins.py)
+  * gumbel_verify / gumbel_draft (shared-noise verification) -- pinned
+    (tests/test_gumbel_oracle.py)
   * philox4x32_10 -- parity unpinned against a published vector; pinned only by
     statistical tests and agreement with the separately written device copy.
 """
@@ -76,6 +78,14 @@ def _load():
         lib.svr_verify.restype = ctypes.c_int
         lib.svr_verify_seeded.argtypes = common + [ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_int] + outs
         lib.svr_verify_seeded.restype = ctypes.c_int
+        lib.svr_gumbel_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
+        lib.svr_gumbel_uniform.restype = ctypes.c_double
+        lib.svr_gumbel_verify.argtypes = [P, ctypes.c_int, P, P, P, P, P, ctypes.c_uint64, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, P, P, P, P, P]
+        lib.svr_gumbel_verify.restype = ctypes.c_int
+        lib.svr_gumbel_draft.argtypes = [P, ctypes.c_int, P, P, P, P, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, P]
+        lib.svr_gumbel_draft.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -191,3 +201,61 @@ def verify(target, draft, draft_tokens, temperature, num_draft=None, top_k=None,
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return OracleResult(acc, out, alpha, status, pa, pt, am, rm, fm, po, qo)
+
+
+# ---------------------------------------------------------------------------
+# Gumbel-coupled (shared-noise) verification
+# ---------------------------------------------------------------------------
+
+@dataclass
+class GumbelResult:
+    accepted_len: np.ndarray   # [B] int32
+    out_tokens: np.ndarray     # [B, G+1] int32: draft_1..draft_n, t_{n+1}, then -1
+    target_tokens: np.ndarray  # [B, G+1] int32: the target's own token t_k at every k <= gamma_b + 1
+    margin: np.ndarray         # [B, G+1] float64: best minus second-best score at each position
+    status: np.ndarray         # [B] uint32
+
+
+def gumbel_uniform(seed: int, b: int, pos: int, token: int) -> float:
+    return _load().svr_gumbel_uniform(seed, b, pos, token)
+
+
+def _gumbel_params(B, temperature, num_draft, top_k, top_p):
+    T = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+    nd = None if num_draft is None else np.ascontiguousarray(num_draft, dtype=np.int32).reshape(B)
+    tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32).reshape(B)
+    tpp = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32).reshape(B)
+    return T, nd, tk, tpp
+
+
+def gumbel_verify(target, draft_tokens, temperature, num_draft=None, top_k=None, top_p=None, *,
+                  seed: int) -> GumbelResult:
+    """Shared-noise verification of one batch: target [B, G+1, V] logits (float32 or
+    bf16 bit patterns), the drafter's tokens [B, G]."""
+    tgt, dt = _as_logits(target)
+    B, G1, V = tgt.shape
+    G = G1 - 1
+    xt = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, G)
+    T, nd, tk, tpp = _gumbel_params(B, temperature, num_draft, top_k, top_p)
+    acc = np.zeros(B, dtype=np.int32)
+    out = np.zeros((B, G + 1), dtype=np.int32)
+    tt = np.zeros((B, G + 1), dtype=np.int32)
+    mg = np.zeros((B, G + 1), dtype=np.float64)
+    st = np.zeros(B, dtype=np.uint32)
+    rc = _load().svr_gumbel_verify(_ptr(tgt), dt, _ptr(xt), _ptr(nd), _ptr(T), _ptr(tk), _ptr(tpp), int(seed), B,
+                                   G, V, _ptr(acc), _ptr(out), _ptr(tt), _ptr(mg), _ptr(st))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return GumbelResult(acc, out, tt, mg, st)
+
+
+def gumbel_draft(draft, temperature, num_draft=None, top_k=None, top_p=None, *, seed: int) -> np.ndarray:
+    """The coupled drafter's tokens [B, G] for draft logits [B, G, V] and the same noise."""
+    drf, dt = _as_logits(draft)
+    B, G, V = drf.shape
+    T, nd, tk, tpp = _gumbel_params(B, temperature, num_draft, top_k, top_p)
+    x = np.zeros((B, G), dtype=np.int32)
+    rc = _load().svr_gumbel_draft(_ptr(drf), dt, _ptr(nd), _ptr(T), _ptr(tk), _ptr(tpp), int(seed), B, G, V, _ptr(x))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return x

@@ -394,3 +394,158 @@ int svr_verify_seeded(const void* target, const void* draft, int dtype, const in
     free(ur);
     return rc;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Gumbel-coupled (shared-noise) verification [AGW, section 共享噪声的采样].    */
+/*                                                                           */
+/* Sampling from softmax(l) is argmax_i(l_i + g_i) with g_i = -log(-log u_i)  */
+/* (the Gumbel-max trick).  The drafter and the target share the noise g_k of */
+/* each position k: the drafter proposes argmax_i(log q_k(i) + g_k,i), the    */
+/* target takes argmax_i(log p_k(i) + g_k,i), and the round keeps the longest */
+/* prefix where the two agree plus the target's token at the first            */
+/* disagreement (all gamma agree: the target's token at gamma + 1).  p and q  */
+/* are the rows normalised as in svr_normalise (temperature, top-k, top-p);   */
+/* tokens outside the kept set have log p = -inf and are never chosen.        */
+/*                                                                           */
+/* Readings (also in the design doc): the noise of token i at position k of        */
+/* sequence b is u = Philox4x32-10(counter (b, k, 2, i >> 2), key seed), word */
+/* i & 3, on the same 24-bit grid as svr_uniform (draw 2: disjoint from the   */
+/* acceptance and residual draws 0 and 1); argmax ties go to the lower id;    */
+/* T = 0 is the plain argmax of the logits (no noise).                        */
+/* Parity: pinned by the Gumbel-max law, drafter invariance, the page's       */
+/* closed form for the match probability and its lower bound, and the greedy  */
+/* special case (tests/test_gumbel_oracle.py).                                */
+/* ------------------------------------------------------------------------- */
+
+double svr_gumbel_uniform(uint64_t seed, uint32_t b, uint32_t pos, uint32_t token) {
+    uint32_t ctr[4] = {b, pos, 2u, token >> 2};
+    uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    svr_philox4x32_10(ctr, key, out);
+    return ((double)(out[token & 3u] >> 8) + 0.5) / 16777216.0;
+}
+
+/* argmax_i(log probs[i] + g_i) over probs[i] > 0, ties to the lower id;
+ * *gap = best score - second best score (INFINITY if one candidate). */
+static int gumbel_argmax(const double* probs, int V, int noisy, uint64_t seed, uint32_t b, uint32_t pos,
+                         double* gap) {
+    int best = -1;
+    double s1 = -INFINITY, s2 = -INFINITY;
+    for (int i = 0; i < V; ++i) {
+        if (!(probs[i] > 0.0)) continue;
+        double s = log(probs[i]);
+        if (noisy) s += -log(-log(svr_gumbel_uniform(seed, b, pos, (uint32_t)i)));
+        if (best < 0 || s > s1) {
+            s2 = s1;
+            s1 = s;
+            best = i;
+        } else if (s > s2) {
+            s2 = s;
+        }
+    }
+    *gap = s1 - s2;
+    return best;
+}
+
+/* validation and normalisation of one row (the rules of svr_verify); returns the status bits */
+static uint32_t gumbel_row(const void* logits_base, int dtype, size_t base, int V, double T, int k, double tp,
+                           double* logits, double* probs) {
+    for (int x = 0; x < V; ++x) {
+        logits[x] = logit_value(logits_base, dtype, base + x);
+        if (isnan(logits[x]) || logits[x] == INFINITY) return SVR_ST_NONFINITE;
+    }
+    return svr_normalise(logits, V, T, k, tp, probs, NULL) != 0 ? SVR_ST_NONFINITE : 0u;
+}
+
+static uint32_t gumbel_params(int gamma, int G, double T, int k, double tp) {
+    uint32_t st = 0;
+    if (!(T >= 0.0) || isinf(T)) st |= SVR_ST_BAD_TEMPERATURE;
+    if (k < 0) st |= SVR_ST_BAD_TOP_K;
+    if (!(tp > 0.0 && tp <= 1.0)) st |= SVR_ST_BAD_TOP_P;
+    if (gamma < 1 || gamma > G) st |= SVR_ST_BAD_NUM_DRAFT;
+    return st;
+}
+
+int svr_gumbel_verify(const void* target, int dtype, const int32_t* draft_tokens, const int32_t* num_draft,
+                      const float* temperature, const int32_t* top_k, const float* top_p, uint64_t seed, int B,
+                      int G, int V, int32_t* accepted_len, int32_t* out_tokens, int32_t* target_tokens,
+                      double* margin, uint32_t* status) {
+    if (B < 0 || G < 1 || G > SVR_MAX_G || V < 1) return -1;
+    if (dtype != SVR_DTYPE_F32 && dtype != SVR_DTYPE_BF16) return -1;
+    if (B > 0 && (!target || !draft_tokens || !temperature || !accepted_len || !out_tokens)) return -1;
+    double* logits = (double*)malloc(sizeof(double) * (size_t)V);
+    double* probs = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int b = 0; b < B; ++b) {
+        int gamma = num_draft ? num_draft[b] : G;
+        double T = (double)temperature[b];
+        int k = top_k ? top_k[b] : 0;
+        double tp = top_p ? (double)top_p[b] : 1.0;
+        uint32_t st = gumbel_params(gamma, G, T, k, tp);
+        if (!(st & SVR_ST_BAD_NUM_DRAFT))
+            for (int i = 0; i < gamma; ++i) {
+                int32_t x = draft_tokens[(size_t)b * G + i];
+                if (x < 0 || x >= V) st |= SVR_ST_BAD_DRAFT_TOKEN;
+            }
+        accepted_len[b] = 0;
+        for (int j = 0; j <= G; ++j) {
+            out_tokens[(size_t)b * (G + 1) + j] = -1;
+            if (target_tokens) target_tokens[(size_t)b * (G + 1) + j] = -1;
+            if (margin) margin[(size_t)b * (G + 1) + j] = NAN;
+        }
+        /* the target's own noise-driven token at every position 1..gamma+1 */
+        int32_t tt[SVR_MAX_G + 1];
+        for (int j = 0; j <= gamma && !st; ++j) {
+            st |= gumbel_row(target, dtype, ((size_t)b * (G + 1) + j) * (size_t)V, V, T, k, tp, logits, probs);
+            if (st) break;
+            double gap = INFINITY;
+            tt[j] = gumbel_argmax(probs, V, T > 0.0, seed, (uint32_t)b, (uint32_t)(j + 1), &gap);
+            if (target_tokens) target_tokens[(size_t)b * (G + 1) + j] = tt[j];
+            if (margin) margin[(size_t)b * (G + 1) + j] = gap;
+        }
+        if (status) status[b] = st;
+        if (st) {
+            if (target_tokens)
+                for (int j = 0; j <= G; ++j) target_tokens[(size_t)b * (G + 1) + j] = -1;
+            continue;
+        }
+        /* the longest prefix where the draft equals the target's choice, then the target's token */
+        int n = 0;
+        while (n < gamma && draft_tokens[(size_t)b * G + n] == tt[n]) ++n;
+        accepted_len[b] = n;
+        for (int i = 0; i < n; ++i) out_tokens[(size_t)b * (G + 1) + i] = draft_tokens[(size_t)b * G + i];
+        out_tokens[(size_t)b * (G + 1) + n] = tt[n];
+    }
+    free(logits);
+    free(probs);
+    return 0;
+}
+
+int svr_gumbel_draft(const void* draft, int dtype, const int32_t* num_draft, const float* temperature,
+                     const int32_t* top_k, const float* top_p, uint64_t seed, int B, int G, int V,
+                     int32_t* draft_tokens) {
+    if (B < 0 || G < 1 || V < 1) return -1;
+    if (dtype != SVR_DTYPE_F32 && dtype != SVR_DTYPE_BF16) return -1;
+    if (B > 0 && (!draft || !temperature || !draft_tokens)) return -1;
+    double* logits = (double*)malloc(sizeof(double) * (size_t)V);
+    double* probs = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int b = 0; b < B; ++b) {
+        int gamma = num_draft ? num_draft[b] : G;
+        double T = (double)temperature[b];
+        int k = top_k ? top_k[b] : 0;
+        double tp = top_p ? (double)top_p[b] : 1.0;
+        uint32_t st = gumbel_params(gamma, G, T, k, tp);
+        for (int i = 0; i < G; ++i) {
+            int32_t x = 0; /* padding and invalid rows: token 0 */
+            if (!st && i < gamma) {
+                if (gumbel_row(draft, dtype, ((size_t)b * G + i) * (size_t)V, V, T, k, tp, logits, probs) == 0u) {
+                    double gap;
+                    x = gumbel_argmax(probs, V, T > 0.0, seed, (uint32_t)b, (uint32_t)(i + 1), &gap);
+                }
+            }
+            draft_tokens[(size_t)b * G + i] = x;
+        }
+    }
+    free(logits);
+    free(probs);
+    return 0;
+}

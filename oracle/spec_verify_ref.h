@@ -90,6 +90,32 @@ int svr_verify_seeded(const void* target, const void* draft, int dtype, const in
                       double* p_out, double* q_out, uint32_t* status, double* accept_margin,
                       double* resid_margin, double* filter_margin);
 
+/* Gumbel-coupled (shared-noise) verification ("Speculative decoding: the art
+ * of guessing well", section 共享噪声的采样).  The noise of token i at 1-based
+ * position k of sequence b is g = -log(-log u), u = svr_gumbel_uniform(seed, b,
+ * k, i): Philox4x32-10 with counter (b, k, 2, i >> 2) and key seed, word i & 3,
+ * on the 24-bit grid.  Rows are normalised as in svr_normalise. */
+#define SVR_MAX_G 32
+double svr_gumbel_uniform(uint64_t seed, uint32_t b, uint32_t pos, uint32_t token);
+
+/* Verification: target [B, G+1, V] logits, the drafter's tokens [B, G].  For each
+ * sequence the target's token t_k = argmax_i(log p_k(i) + g_k,i) at k = 1..gamma_b+1
+ * (T = 0: argmax of the logits), n = the first k with draft_k != t_k (gamma_b if
+ * none), out = draft_1..draft_n, t_{n+1}, then -1.  target_tokens [B, G+1] (or
+ * NULL) receives every t_k (-1 beyond gamma_b + 1), margin [B, G+1] (or NULL) the
+ * gap between the best and the second-best score at each position.  status as
+ * in svr_verify.  Returns 0, or -1 on bad sizes / pointers (G <= SVR_MAX_G). */
+int svr_gumbel_verify(const void* target, int dtype, const int32_t* draft_tokens, const int32_t* num_draft,
+                      const float* temperature, const int32_t* top_k, const float* top_p, uint64_t seed, int B,
+                      int G, int V, int32_t* accepted_len, int32_t* out_tokens, int32_t* target_tokens,
+                      double* margin, uint32_t* status);
+
+/* The coupled drafter: draft_tokens[b, k-1] = argmax_i(log q_k(i) + g_k,i) for
+ * k = 1..gamma_b with the same noise (0 for padding and invalid rows). */
+int svr_gumbel_draft(const void* draft, int dtype, const int32_t* num_draft, const float* temperature,
+                     const int32_t* top_k, const float* top_p, uint64_t seed, int B, int G, int V,
+                     int32_t* draft_tokens);
+
 #ifdef __cplusplus
 }
 #endif
