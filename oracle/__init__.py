@@ -13,6 +13,8 @@ Parity status per function (also recorded in the design doc):
   * normalise / alpha / acceptance / residual -- pinned (tests/test_oracle_pins.py)
   * gumbel_verify / gumbel_draft (shared-noise verification) -- pinned
     (tests/test_gumbel_oracle.py)
+  * kseq_* (K-SEQ multi-candidate verification, one position) -- pinned
+    (tests/test_kseq_oracle.py)
   * philox4x32_10 -- parity unpinned against a published vector; pinned only by
     statistical tests and agreement with the separately written device copy.
 """
@@ -86,6 +88,15 @@ def _load():
         lib.svr_gumbel_draft.argtypes = [P, ctypes.c_int, P, P, P, P, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, P]
         lib.svr_gumbel_draft.restype = ctypes.c_int
+        D, I = ctypes.c_double, ctypes.c_int
+        lib.svr_kseq_beta.argtypes = [P, P, I, D]
+        lib.svr_kseq_beta.restype = D
+        lib.svr_kseq_rho.argtypes = [P, P, I, I]
+        lib.svr_kseq_rho.restype = D
+        lib.svr_kseq_direct.argtypes = [P, P, I, I, P, P]
+        lib.svr_kseq_direct.restype = D
+        lib.svr_kseq_step.argtypes = [P, P, I, I, P, P, D, P]
+        lib.svr_kseq_step.restype = I
         _lib = lib
     return _lib
 
@@ -259,3 +270,40 @@ def gumbel_draft(draft, temperature, num_draft=None, top_k=None, top_p=None, *, 
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return x
+
+
+# ---------------------------------------------------------------------------
+# K-SEQ multi-candidate verification (one position; p = target, q = draft)
+# ---------------------------------------------------------------------------
+
+def _prob_row(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def kseq_beta(p, q, rho: float) -> float:
+    p, q = _prob_row(p), _prob_row(q)
+    return _load().svr_kseq_beta(_ptr(p), _ptr(q), p.size, float(rho))
+
+
+def kseq_rho(p, q, k: int) -> float:
+    p, q = _prob_row(p), _prob_row(q)
+    return _load().svr_kseq_rho(_ptr(p), _ptr(q), p.size, int(k))
+
+
+def kseq_direct(p, q, k: int):
+    """(A_rho*[V], P_A, rho*): the direct acceptance mass of each token."""
+    p, q = _prob_row(p), _prob_row(q)
+    A = np.zeros(p.size)
+    rho = np.zeros(1)
+    pa = _load().svr_kseq_direct(_ptr(p), _ptr(q), p.size, int(k), _ptr(A), _ptr(rho))
+    return A, pa, float(rho[0])
+
+
+def kseq_step(p, q, cand, u, u_res: float):
+    """(emitted token, index of the accepted candidate or -1)."""
+    p, q = _prob_row(p), _prob_row(q)
+    c = np.ascontiguousarray(cand, dtype=np.int32)
+    uu = np.ascontiguousarray(u, dtype=np.float64)
+    idx = np.zeros(1, dtype=np.int32)
+    tok = _load().svr_kseq_step(_ptr(p), _ptr(q), p.size, c.size, _ptr(c), _ptr(uu), float(u_res), _ptr(idx))
+    return int(tok), int(idx[0])

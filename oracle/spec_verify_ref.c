@@ -549,3 +549,104 @@ int svr_gumbel_draft(const void* draft, int dtype, const int32_t* num_draft, con
     free(probs);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* K-SEQ multi-candidate verification, one position ["SpecTr: Fast           */
+/* Speculative Decoding via Optimal Transport" page, section K-SEQ, eqs.      */
+/* (4)-(7) and the residual distribution].  The page names the draft p and    */
+/* the target q; here, as everywhere in this oracle, p is the TARGET and q the */
+/* DRAFT.  With k candidates X_1..X_k drawn independently from q:             */
+/*   m_rho(x) = min(q(x), p(x) / rho)         (the mass one try gives to x)    */
+/*   beta(rho) = sum_x m_rho(x)                                              */
+/*   candidate i is accepted iff u_i * rho * q(X_i) < p(X_i), i.e. with       */
+/*   probability min(1, p / (rho q)), tried in order, the first accepted wins */
+/*   P_A = 1 - (1 - beta)^k, A_rho(x) = (P_A / beta) m_rho(x)                 */
+/*   all rejected: draw from the residual p - A_rho (normalised by 1 - P_A),  */
+/*   by inverse CDF in ascending token id with v = u_res * sum(p - A_rho).    */
+/* rho* is the root in [1, k] of 1 - (1 - beta(rho))^k = rho beta(rho) (the   */
+/* left side minus the right is non-increasing in rho); bisection, keeping    */
+/* the end where the left side <= the right, so the residual is nonnegative.  */
+/* Special cases from the page: beta = 0 -> nothing is accepted (A = 0) and   */
+/* the residual is p itself; P_A = 1 -> the residual branch is never reached   */
+/* (numerically: a residual with no mass falls back to p).                    */
+/* Readings (also in the design doc): strict acceptance u * rho * q < p as in the  */
+/* single-candidate rule; residual order and uniform as in residual_draw.     */
+/* Parity: pinned by the output law (exact enumeration and chi-square), k = 1 */
+/* equal to the single-candidate rule, the page's counterexample to the naive */
+/* rule, A_rho* = min(rho* q, p) >= min(q, p), and the page's fixed-rho closed */
+/* form (tests/test_kseq_oracle.py).                                          */
+/* ------------------------------------------------------------------------- */
+
+double svr_kseq_beta(const double* p, const double* q, int V, double rho) {
+    double s = 0.0;
+    for (int x = 0; x < V; ++x) s += fmin(q[x], p[x] / rho);
+    return s;
+}
+
+double svr_kseq_rho(const double* p, const double* q, int V, int k) {
+    double lo = 1.0, hi = (double)k;
+    /* f(rho) = 1 - (1 - beta)^k - rho * beta; f(1) >= 0 >= f(k) */
+    for (int it = 0; it < 200 && hi - lo > 1e-15 * hi; ++it) {
+        double mid = 0.5 * (lo + hi);
+        double be = svr_kseq_beta(p, q, V, mid);
+        double f = 1.0 - pow(1.0 - be, (double)k) - mid * be;
+        if (f > 0.0)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return hi;
+}
+
+/* direct acceptance mass A_rho(x) for rho = rho*(p, q, k); returns P_A */
+double svr_kseq_direct(const double* p, const double* q, int V, int k, double* A, double* rho_out) {
+    double rho = svr_kseq_rho(p, q, V, k);
+    double be = svr_kseq_beta(p, q, V, rho);
+    double pa = be > 0.0 ? 1.0 - pow(1.0 - be, (double)k) : 0.0;
+    for (int x = 0; x < V; ++x) A[x] = be > 0.0 ? pa / be * fmin(q[x], p[x] / rho) : 0.0;
+    if (rho_out) *rho_out = rho;
+    return pa;
+}
+
+int svr_kseq_step(const double* p, const double* q, int V, int k, const int32_t* cand, const double* u,
+                  double u_res, int32_t* accepted_index) {
+    double rho = svr_kseq_rho(p, q, V, k);
+    *accepted_index = -1;
+    for (int i = 0; i < k; ++i) {
+        int32_t x = cand[i];
+        if (u[i] * rho * q[x] < p[x]) {
+            *accepted_index = i;
+            return x;
+        }
+    }
+    /* all rejected: residual p - A_rho*, in ascending token id */
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    double* A = (double*)malloc(sizeof(double) * (size_t)V);
+    svr_kseq_direct(p, q, V, k, A, NULL);
+    double Z = 0.0;
+    for (int x = 0; x < V; ++x) {
+        r[x] = fmax(p[x] - A[x], 0.0);
+        Z += r[x];
+    }
+    if (!(Z > 0.0)) { /* no residual mass (P_A = 1 up to rounding): fall back to p */
+        Z = 0.0;
+        for (int x = 0; x < V; ++x) {
+            r[x] = p[x];
+            Z += r[x];
+        }
+    }
+    double v = u_res * Z, cum = 0.0;
+    int token = -1, last = -1;
+    for (int x = 0; x < V; ++x) {
+        if (!(r[x] > 0.0)) continue;
+        last = x;
+        cum += r[x];
+        if (cum > v) {
+            token = x;
+            break;
+        }
+    }
+    free(r);
+    free(A);
+    return token >= 0 ? token : last;
+}

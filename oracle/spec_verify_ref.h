@@ -116,6 +116,23 @@ int svr_gumbel_draft(const void* draft, int dtype, const int32_t* num_draft, con
                      const int32_t* top_k, const float* top_p, uint64_t seed, int B, int G, int V,
                      int32_t* draft_tokens);
 
+/* K-SEQ multi-candidate verification at one position ("SpecTr: Fast Speculative
+ * Decoding via Optimal Transport", section K-SEQ).  p: target probabilities [V],
+ * q: draft probabilities [V] (normalised rows), k candidates drawn from q.
+ *   svr_kseq_beta    beta(rho) = sum_x min(q(x), p(x) / rho)
+ *   svr_kseq_rho     rho* in [1, k]: 1 - (1 - beta)^k = rho beta (bisection)
+ *   svr_kseq_direct  A_rho*(x) = (P_A / beta) min(q(x), p(x) / rho*) into A[V];
+ *                    returns P_A = 1 - (1 - beta)^k (0 if beta = 0)
+ *   svr_kseq_step    the emitted token: the first candidate i with
+ *                    u[i] * rho* * q(cand[i]) < p(cand[i]) (its index in
+ *                    *accepted_index), else the residual p - A_rho* drawn by
+ *                    inverse CDF in ascending id with v = u_res * sum (index -1). */
+double svr_kseq_beta(const double* p, const double* q, int V, double rho);
+double svr_kseq_rho(const double* p, const double* q, int V, int k);
+double svr_kseq_direct(const double* p, const double* q, int V, int k, double* A, double* rho_out);
+int svr_kseq_step(const double* p, const double* q, int V, int k, const int32_t* cand, const double* u,
+                  double u_res, int32_t* accepted_index);
+
 #ifdef __cplusplus
 }
 #endif
