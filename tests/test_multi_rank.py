@@ -37,7 +37,8 @@ def _rank_main(rank: int, world: int, port: int, times, out):
 def test_two_gloo_ranks_reduce_to_the_slowest_time():
     world, port = 2, _free_port()
     times = [0.125, 0.5]
-    with mp.Manager() as m:
+    # spawn, not fork: earlier tests may have started threads in this process
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(world, port, times, out), nprocs=world, join=True)
         res = dict(out)
