@@ -52,7 +52,6 @@ constexpr unsigned long long kFWaitNs = 2000000000ull;
 // (7: 2 CTAs per SM, 15: 1 CTA per SM)
 template <int W>
 struct FGeo {
-    static constexpr int kWarps = W;
     static constexpr int kConsumers = 32 * W;
     static constexpr int kThreads = kConsumers + 32;
     static constexpr int kSegBytes = W * kFreeBlockBytes;
