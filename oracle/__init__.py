@@ -97,6 +97,8 @@ def _load():
         lib.svr_kseq_direct.restype = D
         lib.svr_kseq_step.argtypes = [P, P, I, I, P, P, D, P]
         lib.svr_kseq_step.restype = I
+        lib.svr_kseq_verify.argtypes = [P, P, I, P, P, P, P, P, ctypes.c_uint64, I, I, I, P, P, P]
+        lib.svr_kseq_verify.restype = I
         _lib = lib
     return _lib
 
@@ -307,3 +309,24 @@ def kseq_step(p, q, cand, u, u_res: float):
     idx = np.zeros(1, dtype=np.int32)
     tok = _load().svr_kseq_step(_ptr(p), _ptr(q), p.size, c.size, _ptr(c), _ptr(uu), float(u_res), _ptr(idx))
     return int(tok), int(idx[0])
+
+
+def kseq_verify(target, draft, cand, temperature, num_cand=None, top_k=None, top_p=None, *, seed: int):
+    """Batched K-SEQ at one position per row: target / draft logits [B, V] (float32 or
+    bf16 bits), candidates [B, K].  Returns (out_token [B], accepted [B], status [B])."""
+    tgt, dt = _as_logits(target)
+    drf, dt2 = _as_logits(draft)
+    if dt != dt2 or tgt.shape != drf.shape or tgt.ndim != 2:
+        raise ValueError("target and draft must be [B, V] of one dtype")
+    B, V = tgt.shape
+    c = np.ascontiguousarray(cand, dtype=np.int32)
+    K = c.shape[1]
+    T, nc, tk, tpp = _gumbel_params(B, temperature, num_cand, top_k, top_p)
+    tok = np.zeros(B, dtype=np.int32)
+    acc = np.zeros(B, dtype=np.int32)
+    st = np.zeros(B, dtype=np.uint32)
+    rc = _load().svr_kseq_verify(_ptr(tgt), _ptr(drf), dt, _ptr(c), _ptr(nc), _ptr(T), _ptr(tk), _ptr(tpp),
+                                 int(seed), B, K, V, _ptr(tok), _ptr(acc), _ptr(st))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return tok, acc, st

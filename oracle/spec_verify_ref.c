@@ -650,3 +650,50 @@ int svr_kseq_step(const double* p, const double* q, int V, int k, const int32_t*
     free(A);
     return token >= 0 ? token : last;
 }
+
+/* Batched K-SEQ verification of one position per row [SpecTr page, K-SEQ].  Row b:
+ * target logits [V] and draft logits [V] normalised as in svr_normalise, k_b =
+ * num_cand[b] candidates cand[b, 0..k_b-1] (tried in that order), uniforms
+ * u_i = svr_uniform(seed, b, 1, 3 + i) for candidate i (draws 3..3+K-1, below the
+ * input-generation domain 16+) and u_res = svr_uniform(seed, b, 1, 1).  out_token[b]
+ * is the emitted token, accepted[b] the index of the accepted candidate or -1
+ * (residual), status[b] the usual bits (a candidate outside [0, V) is
+ * SVR_ST_BAD_DRAFT_TOKEN, k_b outside [1, K] SVR_ST_BAD_NUM_DRAFT). */
+int svr_kseq_verify(const void* target, const void* draft, int dtype, const int32_t* cand, const int32_t* num_cand,
+                    const float* temperature, const int32_t* top_k, const float* top_p, uint64_t seed, int B, int K,
+                    int V, int32_t* out_token, int32_t* accepted, uint32_t* status) {
+    if (B < 0 || K < 1 || K > 13 || V < 1) return -1;
+    if (dtype != SVR_DTYPE_F32 && dtype != SVR_DTYPE_BF16) return -1;
+    if (B > 0 && (!target || !draft || !cand || !temperature || !out_token || !accepted)) return -1;
+    double* logits = (double*)malloc(sizeof(double) * (size_t)V);
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    double* q = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int b = 0; b < B; ++b) {
+        int k = num_cand ? num_cand[b] : K;
+        double T = (double)temperature[b];
+        int tk = top_k ? top_k[b] : 0;
+        double tp = top_p ? (double)top_p[b] : 1.0;
+        uint32_t st = gumbel_params(k, K, T, tk, tp); /* the same parameter rules (k plays gamma's part) */
+        if (!(st & SVR_ST_BAD_NUM_DRAFT))
+            for (int i = 0; i < k; ++i) {
+                int32_t x = cand[(size_t)b * K + i];
+                if (x < 0 || x >= V) st |= SVR_ST_BAD_DRAFT_TOKEN;
+            }
+        if (!st) st |= gumbel_row(target, dtype, (size_t)b * V, V, T, tk, tp, logits, p);
+        if (!st) st |= gumbel_row(draft, dtype, (size_t)b * V, V, T, tk, tp, logits, q);
+        if (status) status[b] = st;
+        out_token[b] = -1;
+        accepted[b] = -1;
+        if (st) continue;
+        double u[13];
+        for (int i = 0; i < k; ++i) u[i] = svr_uniform(seed, (uint32_t)b, 1u, 3u + (uint32_t)i);
+        int32_t idx = -1;
+        out_token[b] = svr_kseq_step(p, q, V, k, cand + (size_t)b * K, u, svr_uniform(seed, (uint32_t)b, 1u, 1u),
+                                     &idx);
+        accepted[b] = idx;
+    }
+    free(logits);
+    free(p);
+    free(q);
+    return 0;
+}

@@ -133,6 +133,14 @@ double svr_kseq_direct(const double* p, const double* q, int V, int k, double* A
 int svr_kseq_step(const double* p, const double* q, int V, int k, const int32_t* cand, const double* u,
                   double u_res, int32_t* accepted_index);
 
+/* Batched K-SEQ at one position per row: target / draft logits [B, V], candidates
+ * [B, K] (K <= 13), num_cand [B] or NULL (all K); uniforms svr_uniform(seed, b, 1,
+ * 3 + i) per candidate and svr_uniform(seed, b, 1, 1) for the residual.  Outputs:
+ * out_token [B], accepted [B] (candidate index or -1), status [B] (or NULL). */
+int svr_kseq_verify(const void* target, const void* draft, int dtype, const int32_t* cand, const int32_t* num_cand,
+                    const float* temperature, const int32_t* top_k, const float* top_p, uint64_t seed, int B, int K,
+                    int V, int32_t* out_token, int32_t* accepted, uint32_t* status);
+
 #ifdef __cplusplus
 }
 #endif

@@ -140,3 +140,67 @@ def test_disjoint_supports_accept_nothing(oracle_mod):
     assert pa == 0.0 and (A == 0).all()
     tok, idx = oracle_mod.kseq_step(p, q, [0, 1, 0], [0.0, 0.0, 0.0], 0.5)
     assert idx == -1 and tok == 3  # v = 0.5: past the 0.3 of token 2
+
+
+# ---------------------------------------------------------------------------
+# the batched entry: one position per row, Philox uniforms
+# ---------------------------------------------------------------------------
+
+def test_batched_equals_the_step_with_its_documented_uniforms(oracle_mod):
+    rng = np.random.default_rng(31)
+    B, K, V, seed = 64, 4, 20, 123
+    tgt = (rng.normal(size=(B, V)) * 1.5).astype(np.float32)
+    drf = (tgt + rng.normal(size=(B, V))).astype(np.float32)
+    T = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    nc = rng.integers(1, K + 1, B).astype(np.int32)
+    cand = rng.integers(0, V, (B, K)).astype(np.int32)
+    tok, acc, st = oracle_mod.kseq_verify(tgt, drf, cand, T, nc, seed=seed)
+    assert (st == 0).all()
+    for b in range(B):
+        pn = oracle_mod.normalise(tgt[b].astype(np.float64), float(T[b]))
+        qn = oracle_mod.normalise(drf[b].astype(np.float64), float(T[b]))
+        u = [oracle_mod.uniform(seed, b, 1, 3 + i) for i in range(nc[b])]
+        assert (tok[b], acc[b]) == oracle_mod.kseq_step(pn, qn, cand[b, : nc[b]], u, oracle_mod.uniform(seed, b, 1, 1))
+
+
+def test_batched_one_candidate_is_the_sampling_verify(oracle_mod):
+    """k = 1 with the same uniforms as the sampling oracle's position 1."""
+    rng = np.random.default_rng(32)
+    B, V, seed = 200, 15, 9
+    tgt = rng.normal(size=(B, V)).astype(np.float32)
+    drf = (tgt + rng.normal(size=(B, V)) * 0.8).astype(np.float32)
+    T = np.ones(B, dtype=np.float32)
+    x = rng.integers(0, V, (B, 1)).astype(np.int32)
+    tok, acc, _ = oracle_mod.kseq_verify(tgt, drf, x, T, seed=seed)
+    ua = np.array([[oracle_mod.uniform(seed, b, 1, 3)] for b in range(B)])
+    ur = np.array([[oracle_mod.uniform(seed, b, 1, 1)] * 2 for b in range(B)])
+    r = oracle_mod.verify(np.stack([tgt, tgt], axis=1), drf[:, None], x, T, u_accept=ua, u_resid=ur)
+    assert ((acc == 0) == (r.accepted_len == 1)).all()
+    assert (tok == np.where(r.accepted_len == 1, x[:, 0], r.out_tokens[:, 0])).all()
+
+
+def test_batched_output_law_with_philox_uniforms(oracle_mod):
+    """10^5 rows of one (p, q) pair, k = 3 candidates drawn from q: the emitted token ~ p."""
+    rng = np.random.default_rng(33)
+    B, K, V = 100_000, 3, 6
+    lt, ld = rng.normal(size=V), rng.normal(size=V)
+    tgt = np.broadcast_to(lt.astype(np.float32), (B, V)).copy()
+    drf = np.broadcast_to(ld.astype(np.float32), (B, V)).copy()
+    p = oracle_mod.normalise(lt.astype(np.float32).astype(np.float64), 1.0)
+    q = oracle_mod.normalise(ld.astype(np.float32).astype(np.float64), 1.0)
+    cand = rng.choice(V, size=(B, K), p=q).astype(np.int32)
+    tok, _, _ = oracle_mod.kseq_verify(tgt, drf, cand, np.ones(B), seed=77)
+    _, pval = stats.chisquare(np.bincount(tok, minlength=V), p * B)
+    assert pval > 1e-3
+
+
+def test_batched_status_bits(oracle_mod):
+    rng = np.random.default_rng(34)
+    B, K, V = 4, 2, 8
+    tgt = rng.normal(size=(B, V)).astype(np.float32)
+    tgt[2, 3] = np.inf
+    cand = rng.integers(0, V, (B, K)).astype(np.int32)
+    cand[1, 1] = -1
+    tok, acc, st = oracle_mod.kseq_verify(tgt, tgt.copy(), cand, np.array([1, 1, 1, -1.0]), np.array([2, 2, 2, 2]),
+                                          seed=1)
+    assert st[0] == 0 and (st[1:] != 0).all() and (tok[1:] == -1).all() and (acc[1:] == -1).all()
