@@ -21,6 +21,12 @@
  *         q_{gamma+1} treated as zero so the residual becomes p_{gamma+1}).
  *  [PHX]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *         1, 2, 3", SC'11 -- the Philox4x32-10 block function.
+ *  [AGW-G] "Speculative decoding: the art of guessing well", section 共享噪声的
+ *         采样 (Gumbel-max, shared noise, the `gumbel_verify` listing) -- the
+ *         shared-noise functions at the end of this file.
+ *  [STR]  "SpecTr: Fast Speculative Decoding via Optimal Transport" page,
+ *         section K-SEQ (eqs. (4)-(7), the residual distribution) -- the K-SEQ
+ *         functions at the end of this file (the page's p and q swapped).
  *
  * Readings taken where the pages are silent (each one also listed in the design doc):
  *  - normalisation order: temperature, softmax, top-k, renormalise, top-p,

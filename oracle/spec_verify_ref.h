@@ -13,7 +13,10 @@
  *   - "Speculative decoding: the art of guessing well", section 投机采样
  *     (the `verify` listing: bonus token via q_{gamma+1} := 0).
  * The Philox4x32-10 generator follows Salmon, Moraes, Dror and Shaw,
- * "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11).
+ * "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11).  Two adjacent
+ * methods follow at the end: shared-noise (Gumbel-coupled) verification
+ * ("the art of guessing well", section 共享噪声的采样) and K-SEQ
+ * multi-candidate verification ("SpecTr" page, section K-SEQ).
  *
  * Parity status of each function is given in its comment in the .c file.
  */
