@@ -99,6 +99,9 @@ def _load():
         lib.svr_kseq_step.restype = I
         lib.svr_kseq_verify.argtypes = [P, P, I, P, P, P, P, P, ctypes.c_uint64, I, I, I, P, P, P]
         lib.svr_kseq_verify.restype = I
+        lib.svr_spectr_round.argtypes = [P, P, I, P, I, I, I, ctypes.c_float, I, ctypes.c_float, ctypes.c_uint64,
+                                         ctypes.c_uint32, P]
+        lib.svr_spectr_round.restype = I
         _lib = lib
     return _lib
 
@@ -330,3 +333,22 @@ def kseq_verify(target, draft, cand, temperature, num_cand=None, top_k=None, top
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return tok, acc, st
+
+
+def spectr_round(target, draft, tok, temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0, *, seed: int,
+                 b: int = 0) -> np.ndarray:
+    """One SpecTr round: target [K, L+1, V], draft [K, L, V] logits, draft sequences tok [K, L].
+    Returns the emitted tokens (1..L+1 of them)."""
+    tgt, dt = _as_logits(target)
+    drf, dt2 = _as_logits(draft)
+    K, L1, V = tgt.shape
+    L = L1 - 1
+    if dt != dt2 or drf.shape != (K, L, V):
+        raise ValueError("target [K, L+1, V] and draft [K, L, V] of one dtype")
+    t = np.ascontiguousarray(tok, dtype=np.int32).reshape(K, L)
+    out = np.zeros(L + 1, dtype=np.int32)
+    n = _load().svr_spectr_round(_ptr(tgt), _ptr(drf), dt, _ptr(t), K, L, V, float(temperature), int(top_k),
+                                 float(top_p), int(seed), int(b), _ptr(out))
+    if n < 0:
+        raise ValueError("bad row")
+    return out[:n]

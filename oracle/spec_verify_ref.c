@@ -703,3 +703,74 @@ int svr_kseq_verify(const void* target, const void* draft, int dtype, const int3
     free(q);
     return 0;
 }
+
+/* One SpecTr round for one sequence [STR, section SpecTr]: K draft sequences of
+ * length L (tok[K][L]), the target rows at every candidate's prefix of length
+ * l = 0..L (target [K][L+1][V] logits) and the draft rows at lengths 0..L-1 (draft
+ * [K][L][V]); rows of candidates that share a prefix must be equal (the first alive
+ * candidate's are used).  At each position: K-SEQ over the alive candidates' next
+ * tokens (duplicates kept, in candidate order), uniforms U(seed, b, l+1, 3+i) and
+ * U(seed, b, l+1, 1); the emitted token Y keeps the candidates whose token equals
+ * it; none left ends the round; after all L positions matched, a bonus token is
+ * drawn from the target row at length L by inverse CDF with U(seed, b, L+1, 1).
+ * Writes the emitted tokens to out[0..n-1] (n <= L+1) and returns n (-1 on a bad
+ * row: a non-finite logit, a token outside [0, V), bad T / top-k / top-p). */
+int svr_spectr_round(const void* target, const void* draft, int dtype, const int32_t* tok, int K, int L, int V,
+                     float temperature, int top_k, float top_p, uint64_t seed, uint32_t b, int32_t* out) {
+    if (K < 1 || K > 13 || L < 1 || V < 1) return -1;
+    double T = (double)temperature, tp = (double)top_p;
+    if (gumbel_params(1, 1, T, top_k, tp)) return -1;
+    for (int j = 0; j < K; ++j)
+        for (int l = 0; l < L; ++l)
+            if (tok[(size_t)j * L + l] < 0 || tok[(size_t)j * L + l] >= V) return -1;
+    double* logits = (double*)malloc(sizeof(double) * (size_t)V);
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    double* q = (double*)malloc(sizeof(double) * (size_t)V);
+    int alive[13], na = K, n = 0, rc = 0;
+    for (int j = 0; j < K; ++j) alive[j] = j;
+    for (int l = 0;; ++l) {
+        const int j0 = alive[0];
+        if (l == L) { /* every position matched: the bonus token from the target row at length L */
+            if (gumbel_row(target, dtype, ((size_t)j0 * (L + 1) + L) * (size_t)V, V, T, top_k, tp, logits, p)) {
+                rc = -1;
+                break;
+            }
+            double v = svr_uniform(seed, b, (uint32_t)(L + 1), 1u), cum = 0.0;
+            int y = -1, last = -1;
+            for (int x = 0; x < V; ++x) {
+                if (!(p[x] > 0.0)) continue;
+                last = x;
+                cum += p[x];
+                if (cum > v) {
+                    y = x;
+                    break;
+                }
+            }
+            out[n++] = y >= 0 ? y : last;
+            break;
+        }
+        if (gumbel_row(target, dtype, ((size_t)j0 * (L + 1) + l) * (size_t)V, V, T, top_k, tp, logits, p) ||
+            gumbel_row(draft, dtype, ((size_t)j0 * L + l) * (size_t)V, V, T, top_k, tp, logits, q)) {
+            rc = -1;
+            break;
+        }
+        int32_t cand[13];
+        double u[13];
+        for (int i = 0; i < na; ++i) {
+            cand[i] = tok[(size_t)alive[i] * L + l];
+            u[i] = svr_uniform(seed, b, (uint32_t)(l + 1), 3u + (uint32_t)i);
+        }
+        int32_t idx;
+        const int y = svr_kseq_step(p, q, V, na, cand, u, svr_uniform(seed, b, (uint32_t)(l + 1), 1u), &idx);
+        out[n++] = y;
+        int m = 0;
+        for (int i = 0; i < na; ++i)
+            if (tok[(size_t)alive[i] * L + l] == y) alive[m++] = alive[i];
+        na = m;
+        if (na == 0) break;
+    }
+    free(logits);
+    free(p);
+    free(q);
+    return rc ? -1 : n;
+}

@@ -144,6 +144,16 @@ int svr_kseq_verify(const void* target, const void* draft, int dtype, const int3
                     const float* temperature, const int32_t* top_k, const float* top_p, uint64_t seed, int B, int K,
                     int V, int32_t* out_token, int32_t* accepted, uint32_t* status);
 
+/* One SpecTr round for sequence b ("SpecTr" page, section SpecTr): K draft sequences
+ * tok [K, L], target rows at every candidate's prefix [K, L+1, V], draft rows [K, L, V];
+ * K-SEQ at each position over the alive candidates (uniforms U(seed, b, l+1, 3+i) and
+ * U(seed, b, l+1, 1)), candidates whose token equals the emitted one stay alive, the
+ * round ends when none do, or after L matched positions with a bonus token from the
+ * target row at length L (U(seed, b, L+1, 1)).  Emitted tokens into out [L+1]; returns
+ * their count, or -1 for a bad row.  K <= 13. */
+int svr_spectr_round(const void* target, const void* draft, int dtype, const int32_t* tok, int K, int L, int V,
+                     float temperature, int top_k, float top_p, uint64_t seed, uint32_t b, int32_t* out);
+
 #ifdef __cplusplus
 }
 #endif
