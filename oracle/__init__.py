@@ -13,8 +13,10 @@ Parity status per function (also recorded in the design doc):
   * normalise / alpha / acceptance / residual -- pinned (tests/test_oracle_pins.py)
   * gumbel_verify / gumbel_draft (shared-noise verification) -- pinned
     (tests/test_gumbel_oracle.py)
-  * kseq_* (K-SEQ multi-candidate verification, one position) -- pinned
-    (tests/test_kseq_oracle.py)
+  * kseq_* / kseq_verify (K-SEQ multi-candidate verification: one position, and
+    a batch of rows) -- pinned (tests/test_kseq_oracle.py)
+  * spectr_round (one SpecTr round along the draft sequences' prefix tree) --
+    pinned (tests/test_spectr_oracle.py)
   * philox4x32_10 -- parity unpinned against a published vector; pinned only by
     statistical tests and agreement with the separately written device copy.
 """
