@@ -193,8 +193,9 @@ int spec_verify_host(const void* host_target_logits, const void* host_draft_logi
  *    batches of a few dozen sequences at 128k-152k vocabularies do); beyond it,
  *    use spec_verify with a workspace;
  *  - SV_ECUDA if the buffer's address cannot be looked up.
- * The first call on each device looks the buffer's address up (once); make
- * that call outside any stream capture.  All calls on a device share the one
+ * The first call on each device looks the buffer's address up, once per CUDA
+ * context (so again after cudaDeviceReset); make that call outside any stream
+ * capture.  All calls on a device share the one
  * buffer: calls that may overlap on the GPU race and must be ordered (one
  * stream, or events).  Nothing has to be cleared between calls.
  */

@@ -9,16 +9,18 @@ The arithmetic lives in ``spec_verify_ref.c`` (see its header for the passages
 of the pages each function follows); this module only builds that file with
 gcc and marshals numpy arrays through ctypes.
 
-Parity status per function (also recorded in the design doc):
-  * normalise / alpha / acceptance / residual -- pinned (tests/test_oracle_pins.py)
+Parity status per function:
+  * normalise / alpha / acceptance / residual -- pinned (tests/test_oracle_pins.py);
+    decision margins pinned (tests/test_oracle_margins_philox.py)
+  * lenience (verify with ``lenience``) -- pinned (tests/test_lenience_oracle.py)
   * gumbel_verify / gumbel_draft (shared-noise verification) -- pinned
     (tests/test_gumbel_oracle.py)
   * kseq_* / kseq_verify (K-SEQ multi-candidate verification: one position, and
     a batch of rows) -- pinned (tests/test_kseq_oracle.py)
   * spectr_round (one SpecTr round along the draft sequences' prefix tree) --
     pinned (tests/test_spectr_oracle.py)
-  * philox4x32_10 -- parity unpinned against a published vector; pinned only by
-    statistical tests and agreement with the separately written device copy.
+  * philox4x32_10 -- pinned against PyTorch's independent header-only Philox
+    engine on explicit counters and keys (tests/test_oracle_margins_philox.py).
 """
 from __future__ import annotations
 
@@ -43,6 +45,7 @@ ST_BAD_TOP_P = 0x04
 ST_BAD_NUM_DRAFT = 0x08
 ST_BAD_DRAFT_TOKEN = 0x10
 ST_NONFINITE = 0x20
+ST_BAD_LENIENCE = 0x80
 
 
 def build(force: bool = False) -> str:
@@ -82,6 +85,11 @@ def _load():
         lib.svr_verify.restype = ctypes.c_int
         lib.svr_verify_seeded.argtypes = common + [ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_int] + outs
         lib.svr_verify_seeded.restype = ctypes.c_int
+        lib.svr_verify_ex.argtypes = common + [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int] + outs
+        lib.svr_verify_ex.restype = ctypes.c_int
+        lib.svr_verify_ex_seeded.argtypes = common + [P, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+                                                      ctypes.c_int] + outs
+        lib.svr_verify_ex_seeded.restype = ctypes.c_int
         lib.svr_gumbel_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
         lib.svr_gumbel_uniform.restype = ctypes.c_double
         lib.svr_gumbel_verify.argtypes = [P, ctypes.c_int, P, P, P, P, P, ctypes.c_uint64, ctypes.c_int,
@@ -169,12 +177,13 @@ def _as_logits(a: np.ndarray):
 
 def verify(target, draft, draft_tokens, temperature, num_draft=None, top_k=None, top_p=None, *,
            seed: Optional[int] = None, u_accept=None, u_resid=None, all_positions: bool = False,
-           probs: bool = False) -> OracleResult:
+           probs: bool = False, lenience=None) -> OracleResult:
     """Run the oracle on one batch.
 
     ``target`` [B, G+1, V] and ``draft`` [B, G, V] are float32 arrays or bf16 bit
     patterns (uint16).  Either ``seed`` (Philox stream) or explicit ``u_accept``
-    [B, G] / ``u_resid`` [B, G+1] uniforms must be given.
+    [B, G] / ``u_resid`` [B, G+1] uniforms must be given.  ``lenience`` [B]
+    (None = 1 everywhere) scales q(x) in the acceptance test.
     """
     tgt, dt = _as_logits(target)
     drf, dt2 = _as_logits(draft)
@@ -189,6 +198,7 @@ def verify(target, draft, draft_tokens, temperature, num_draft=None, top_k=None,
     nd = None if num_draft is None else np.ascontiguousarray(num_draft, dtype=np.int32).reshape(B)
     tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32).reshape(B)
     tpp = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32).reshape(B)
+    ln = None if lenience is None else np.ascontiguousarray(np.broadcast_to(lenience, (B,)), dtype=np.float32)
 
     acc = np.zeros(B, dtype=np.int32)
     out = np.zeros((B, G + 1), dtype=np.int32)
@@ -209,13 +219,13 @@ def verify(target, draft, draft_tokens, temperature, num_draft=None, top_k=None,
             _ptr(am), _ptr(rm), _ptr(fm)]
     lib = _load()
     if seed is not None:
-        rc = lib.svr_verify_seeded(_ptr(tgt), _ptr(drf), dt, _ptr(xt), _ptr(nd), _ptr(T), _ptr(tk), _ptr(tpp),
-                                   int(seed), B, G, V, *outs)
+        rc = lib.svr_verify_ex_seeded(_ptr(tgt), _ptr(drf), dt, _ptr(xt), _ptr(nd), _ptr(T), _ptr(tk), _ptr(tpp),
+                                      _ptr(ln), int(seed), B, G, V, *outs)
     else:
         ua = np.ascontiguousarray(u_accept, dtype=np.float64).reshape(B, G)
         ur = np.ascontiguousarray(u_resid, dtype=np.float64).reshape(B, G + 1)
-        rc = lib.svr_verify(_ptr(tgt), _ptr(drf), dt, _ptr(xt), _ptr(nd), _ptr(T), _ptr(tk), _ptr(tpp),
-                            _ptr(ua), _ptr(ur), B, G, V, *outs)
+        rc = lib.svr_verify_ex(_ptr(tgt), _ptr(drf), dt, _ptr(xt), _ptr(nd), _ptr(T), _ptr(tk), _ptr(tpp),
+                               _ptr(ln), _ptr(ua), _ptr(ur), B, G, V, *outs)
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return OracleResult(acc, out, alpha, status, pa, pt, am, rm, fm, po, qo)

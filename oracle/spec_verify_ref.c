@@ -24,11 +24,14 @@
  *  [AGW-G] "Speculative decoding: the art of guessing well", section 共享噪声的
  *         采样 (Gumbel-max, shared noise, the `gumbel_verify` listing) -- the
  *         shared-noise functions at the end of this file.
+ *  [LEN]  the same review page, section Lenience: a parameter l in [0, 1]
+ *         multiplies q(x) in the acceptance test; no token is then emitted with
+ *         more than 1/l times its probability, and the acceptance rate rises.
  *  [STR]  "SpecTr: Fast Speculative Decoding via Optimal Transport" page,
  *         section K-SEQ (eqs. (4)-(7), the residual distribution) -- the K-SEQ
  *         functions at the end of this file (the page's p and q swapped).
  *
- * Readings taken where the pages are silent (each one also listed in the design doc):
+ * Readings taken where the pages are silent (each resolves a point the pages leave open):
  *  - normalisation order: temperature, softmax, top-k, renormalise, top-p,
  *    renormalise; ties in top-k / top-p / argmax go to the lower token id;
  *    the top-p set is the shortest descending prefix whose mass reaches top_p
@@ -265,12 +268,31 @@ static int residual_draw(const double* p, const double* q, int V, double u, doub
 /* Batched verification [LEV Algorithm 1; SUR section 4; AGW `verify`].       */
 /* ------------------------------------------------------------------------- */
 
+/* Acceptance mass of one token under lenience l [LEN]: q(x) * P(u l q(x) < p(x)) with
+ * u uniform on (0, 1), i.e. q(x) when l q(x) <= p(x) and p(x) > 0, else p(x) / l (which
+ * is 0 when p(x) = 0).  With l = 1 this is min(p(x), q(x)) [AGW 投机采样]. */
+static double accept_mass(double p, double q, double l) {
+    if (l * q <= p) return p > 0.0 ? q : 0.0;
+    return p / l; /* here l q > p >= 0, so l > 0 */
+}
+
 int svr_verify(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
                const int32_t* num_draft, const float* temperature, const int32_t* top_k,
                const float* top_p, const double* u_accept, const double* u_resid, int B, int G, int V,
                int32_t* accepted_len, int32_t* out_tokens, double* alpha, int32_t* pos_accept,
                int32_t* pos_token, double* p_out, double* q_out, uint32_t* status,
                double* accept_margin, double* resid_margin, double* filter_margin) {
+    return svr_verify_ex(target, draft, dtype, draft_tokens, num_draft, temperature, top_k, top_p, NULL, u_accept,
+                         u_resid, B, G, V, accepted_len, out_tokens, alpha, pos_accept, pos_token, p_out, q_out,
+                         status, accept_margin, resid_margin, filter_margin);
+}
+
+int svr_verify_ex(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                  const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+                  const float* top_p, const float* lenience, const double* u_accept, const double* u_resid,
+                  int B, int G, int V, int32_t* accepted_len, int32_t* out_tokens, double* alpha,
+                  int32_t* pos_accept, int32_t* pos_token, double* p_out, double* q_out, uint32_t* status,
+                  double* accept_margin, double* resid_margin, double* filter_margin) {
     if (B < 0 || G < 1 || V < 1) return -1;
     if (dtype != SVR_DTYPE_F32 && dtype != SVR_DTYPE_BF16) return -1;
     if (B > 0 && (!target || !draft || !draft_tokens || !temperature || !u_accept || !u_resid ||
@@ -288,9 +310,11 @@ int svr_verify(const void* target, const void* draft, int dtype, const int32_t* 
         double T = (double)temperature[b];
         int k = top_k ? top_k[b] : 0;
         double tp = top_p ? (double)top_p[b] : 1.0;
+        double len = lenience ? (double)lenience[b] : 1.0;
         if (!(T >= 0.0) || isinf(T)) st |= SVR_ST_BAD_TEMPERATURE;
         if (k < 0) st |= SVR_ST_BAD_TOP_K;
         if (!(tp > 0.0 && tp <= 1.0)) st |= SVR_ST_BAD_TOP_P;
+        if (!(len >= 0.0 && len <= 1.0)) st |= SVR_ST_BAD_LENIENCE;
         if (gamma < 1 || gamma > G) st |= SVR_ST_BAD_NUM_DRAFT;
         if (!(st & SVR_ST_BAD_NUM_DRAFT))
             for (int i = 0; i < gamma; ++i) {
@@ -339,21 +363,24 @@ int svr_verify(const void* target, const void* draft, int dtype, const int32_t* 
         if (p_out) memcpy(p_out + (size_t)b * (G + 1) * V, P, sizeof(double) * (size_t)(gamma + 1) * V);
         if (q_out) memcpy(q_out + (size_t)b * G * V, Q, sizeof(double) * (size_t)gamma * V);
 
-        /* per-position acceptance rate alpha_i = sum_x min(p_i(x), q_i(x)) [AGW 投机采样] */
+        /* per-position acceptance rate alpha_i = sum_x min(p_i(x), q_i(x)) [AGW 投机采样];
+         * under lenience l, sum_x q_i(x) P(accept | x) [LEN] */
         for (int i = 0; i < gamma; ++i) {
             double a = 0.0;
-            for (int x = 0; x < V; ++x) a += fmin(P[(size_t)i * V + x], Q[(size_t)i * V + x]);
+            for (int x = 0; x < V; ++x) a += accept_mass(P[(size_t)i * V + x], Q[(size_t)i * V + x], len);
             alpha[(size_t)b * G + i] = a;
         }
 
-        /* acceptance test left to right, stop at the first rejection [LEV Alg. 1 step 3] */
+        /* acceptance test left to right, stop at the first rejection [LEV Alg. 1 step 3];
+         * lenience multiplies q(x) in the test [LEN] */
         int n = gamma;
         for (int i = 0; i < gamma; ++i) {
             int x = draft_tokens[(size_t)b * G + i];
             double px = P[(size_t)i * V + x], qx = Q[(size_t)i * V + x];
             double u = u_accept[(size_t)b * G + i];
-            int accept = (u * qx < px);
-            if (accept_margin) accept_margin[(size_t)b * G + i] = (qx > 0.0) ? fabs(u - px / qx) : INFINITY;
+            double lq = len * qx;
+            int accept = (u * lq < px);
+            if (accept_margin) accept_margin[(size_t)b * G + i] = (lq > 0.0) ? fabs(u - px / lq) : INFINITY;
             if (pos_accept) pos_accept[(size_t)b * G + i] = accept;
             if (!accept && n == gamma) {
                 n = i;
@@ -389,13 +416,24 @@ int svr_verify_seeded(const void* target, const void* draft, int dtype, const in
                       int32_t* out_tokens, double* alpha, int32_t* pos_accept, int32_t* pos_token,
                       double* p_out, double* q_out, uint32_t* status, double* accept_margin,
                       double* resid_margin, double* filter_margin) {
+    return svr_verify_ex_seeded(target, draft, dtype, draft_tokens, num_draft, temperature, top_k, top_p, NULL,
+                                seed, B, G, V, accepted_len, out_tokens, alpha, pos_accept, pos_token, p_out,
+                                q_out, status, accept_margin, resid_margin, filter_margin);
+}
+
+int svr_verify_ex_seeded(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                         const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+                         const float* top_p, const float* lenience, uint64_t seed, int B, int G, int V,
+                         int32_t* accepted_len, int32_t* out_tokens, double* alpha, int32_t* pos_accept,
+                         int32_t* pos_token, double* p_out, double* q_out, uint32_t* status,
+                         double* accept_margin, double* resid_margin, double* filter_margin) {
     if (B < 0 || G < 1) return -1;
     double* ua = (double*)malloc(sizeof(double) * (size_t)(B > 0 ? B : 1) * (size_t)G);
     double* ur = (double*)malloc(sizeof(double) * (size_t)(B > 0 ? B : 1) * (size_t)(G + 1));
     svr_philox_uniforms(seed, B, G, ua, ur);
-    int rc = svr_verify(target, draft, dtype, draft_tokens, num_draft, temperature, top_k, top_p, ua, ur, B, G,
-                        V, accepted_len, out_tokens, alpha, pos_accept, pos_token, p_out, q_out, status,
-                        accept_margin, resid_margin, filter_margin);
+    int rc = svr_verify_ex(target, draft, dtype, draft_tokens, num_draft, temperature, top_k, top_p, lenience,
+                           ua, ur, B, G, V, accepted_len, out_tokens, alpha, pos_accept, pos_token, p_out, q_out,
+                           status, accept_margin, resid_margin, filter_margin);
     free(ua);
     free(ur);
     return rc;
@@ -413,7 +451,7 @@ int svr_verify_seeded(const void* target, const void* draft, int dtype, const in
 /* are the rows normalised as in svr_normalise (temperature, top-k, top-p);   */
 /* tokens outside the kept set have log p = -inf and are never chosen.        */
 /*                                                                           */
-/* Readings (also in the design doc): the noise of token i at position k of        */
+/* Readings where the page is silent: the noise of token i at position k of  */
 /* sequence b is u = Philox4x32-10(counter (b, k, 2, i >> 2), key seed), word */
 /* i & 3, on the same 24-bit grid as svr_uniform (draw 2: disjoint from the   */
 /* acceptance and residual draws 0 and 1); argmax ties go to the lower id;    */
@@ -575,8 +613,8 @@ int svr_gumbel_draft(const void* draft, int dtype, const int32_t* num_draft, con
 /* Special cases from the page: beta = 0 -> nothing is accepted (A = 0) and   */
 /* the residual is p itself; P_A = 1 -> the residual branch is never reached   */
 /* (numerically: a residual with no mass falls back to p).                    */
-/* Readings (also in the design doc): strict acceptance u * rho * q < p as in the  */
-/* single-candidate rule; residual order and uniform as in residual_draw.     */
+/* Readings where the page is silent: strict acceptance u * rho * q < p as in */
+/* the single-candidate rule; residual order and uniform as in residual_draw */
 /* Parity: pinned by the output law (exact enumeration and chi-square), k = 1 */
 /* equal to the single-candidate rule, the page's counterexample to the naive */
 /* rule, A_rho* = min(rho* q, p) >= min(q, p), and the page's fixed-rho closed */

@@ -40,6 +40,7 @@ extern "C" {
 #define SVR_ST_BAD_NUM_DRAFT 0x08u
 #define SVR_ST_BAD_DRAFT_TOKEN 0x10u
 #define SVR_ST_NONFINITE 0x20u
+#define SVR_ST_BAD_LENIENCE 0x80u
 
 /* Philox4x32-10 block function: ctr[4], key[2] -> out[4]. */
 void svr_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
@@ -85,6 +86,23 @@ int svr_verify(const void* target, const void* draft, int dtype, const int32_t* 
                int32_t* pos_token, double* p_out, double* q_out, uint32_t* status,
                double* accept_margin, double* resid_margin, double* filter_margin);
 
+/* svr_verify with a per-sequence lenience l_b in [0, 1] ("Fast Inference from
+ * Transformers via Speculative Decoding" review page, section Lenience: q(x) is
+ * multiplied by l in the acceptance test).  lenience [B] (NULL = 1 everywhere,
+ * which is svr_verify exactly):
+ *   accept x_i iff u * l * q_i(x_i) < p_i(x_i)   (accept_margin |u - p/(l q)|, +inf if l q = 0)
+ *   alpha_i = sum_x q_i(x) * P(accept | x) = sum_x min(q_i(x), p_i(x) / l)
+ *             (x with p(x) > 0 and l q(x) <= p(x) always pass; l = 0 accepts exactly the
+ *             tokens with p(x) > 0)
+ *   the residual / bonus draw is unchanged: norm(max(0, p - q)), q_{gamma+1} := 0.
+ * A lenience that is NaN or outside [0, 1] gives SVR_ST_BAD_LENIENCE. */
+int svr_verify_ex(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                  const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+                  const float* top_p, const float* lenience, const double* u_accept, const double* u_resid,
+                  int B, int G, int V, int32_t* accepted_len, int32_t* out_tokens, double* alpha,
+                  int32_t* pos_accept, int32_t* pos_token, double* p_out, double* q_out, uint32_t* status,
+                  double* accept_margin, double* resid_margin, double* filter_margin);
+
 /* Same, drawing the uniforms from the Philox stream keyed by (seed, b, pos, draw). */
 int svr_verify_seeded(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
                       const int32_t* num_draft, const float* temperature, const int32_t* top_k,
@@ -92,6 +110,14 @@ int svr_verify_seeded(const void* target, const void* draft, int dtype, const in
                       int32_t* out_tokens, double* alpha, int32_t* pos_accept, int32_t* pos_token,
                       double* p_out, double* q_out, uint32_t* status, double* accept_margin,
                       double* resid_margin, double* filter_margin);
+
+/* svr_verify_ex with the Philox uniforms of svr_verify_seeded. */
+int svr_verify_ex_seeded(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                         const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+                         const float* top_p, const float* lenience, uint64_t seed, int B, int G, int V,
+                         int32_t* accepted_len, int32_t* out_tokens, double* alpha, int32_t* pos_accept,
+                         int32_t* pos_token, double* p_out, double* q_out, uint32_t* status,
+                         double* accept_margin, double* resid_margin, double* filter_margin);
 
 /* Gumbel-coupled (shared-noise) verification ("Speculative decoding: the art
  * of guessing well", section 共享噪声的采样).  The noise of token i at 1-based

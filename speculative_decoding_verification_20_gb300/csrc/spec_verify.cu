@@ -154,13 +154,21 @@ struct DeviceInfo {
     bool ok = false;
 };
 
-DeviceInfo& device_info(int dev) {
+// SM count of device `dev`, cached for the first 64 devices (a device
+// attribute: it outlives any context); queried each time beyond them.
+DeviceInfo device_info(int dev) {
     static DeviceInfo infos[64];
     static std::mutex mu;
+    if (dev < 0 || dev >= 64) {
+        DeviceInfo d;
+        if (dev >= 0 && cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            d.ok = d.sms > 0;
+        return d;
+    }
     std::lock_guard<std::mutex> lock(mu);
-    DeviceInfo& d = infos[dev & 63];
+    DeviceInfo& d = infos[dev];
     if (!d.ok) {
-        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) d.sms = 0;
         d.ok = d.sms > 0;
     }
     return d;
@@ -232,7 +240,7 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SV_ECUDA;
-    const DeviceInfo& di = device_info(dev);
+    const DeviceInfo di = device_info(dev);
     if (!di.ok) return SV_ECUDA;
     cudaStream_t s = (cudaStream_t)stream;
 

@@ -10,13 +10,18 @@
 // workspace alive itself; here the library keeps one, of a fixed size.
 //
 // The buffer is one file-scope __device__ array of SV_STATIC_SCRATCH_BYTES.
-// Each device gets its own copy when this library's code is loaded there.
-// Its device address is looked up once per device with cudaGetSymbolAddress,
-// by the first spec_verify_static call made with that device current; make
-// that first call outside any stream capture.  Every call reuses the same
-// buffer, so calls that could run at the same time on one device (different
-// streams with nothing ordering them) race on it and give wrong results:
-// order them on one stream or with events.
+// Each device gets its own copy when this library's code is loaded into that
+// device's context.  Its device address is looked up with
+// cudaGetSymbolAddress by the first spec_verify_static call made with that
+// device current, and kept for that context: the cache is keyed on the
+// device and on the context's unique id, so after cudaDeviceReset (which
+// destroys the context; the next CUDA call makes a new one and loads the
+// module again, possibly elsewhere) the next call looks the address up again
+// instead of handing the kernels a stale pointer.  Make the first call on a
+// device (and the first after a reset) outside any stream capture.  Every
+// call reuses the same buffer, so calls that could run at the same time on
+// one device (different streams with nothing ordering them) race on it and
+// give wrong results: order them on one stream or with events.
 //
 // Nothing in the buffer has to start at zero: the first kernel of each call
 // resets every counter and flag the later kernels of that call read.
@@ -34,20 +39,55 @@ static __device__ __align__(256) unsigned char g_static_scratch[SV_STATIC_SCRATC
 
 constexpr int kMaxDevices = 64;
 
-// The buffer's device address on device `dev` (looked up once), or nullptr
-// if the lookup failed.
+// The driver's context queries, fetched through the runtime so the library
+// needs no link-time dependency on the driver library.
+typedef int (*CtxGetCurrentFn)(void** ctx);
+typedef int (*CtxGetIdFn)(void* ctx, unsigned long long* id);
+
+// Unique id of the calling thread's current context (0: none, or the query
+// is unavailable).  Context ids are never reused within a process.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = (CtxGetCurrentFn)f;
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = (CtxGetIdFn)f;
+        (void)cudaGetLastError();
+    });
+    if (!get_current || !get_id) return 0;
+    void* ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+    return id;
+}
+
+// The buffer's device address on device `dev` in the current context, or
+// nullptr if the lookup failed.
 void* static_scratch(int dev) {
     static void* addr[kMaxDevices] = {};
+    static unsigned long long ctx_of[kMaxDevices] = {};
     static std::mutex mu;
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
             (void)cudaGetLastError();  // do not leave the failure for the caller's next check
+            addr[dev] = nullptr;
             return nullptr;
         }
         addr[dev] = p;
+        // the lookup has made the primary context current if there was none
+        ctx_of[dev] = ctx != 0 ? ctx : current_context_id();
     }
     return addr[dev];
 }

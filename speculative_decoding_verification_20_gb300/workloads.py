@@ -21,11 +21,13 @@ logits = target logits + Gaussian noise):
                                                  target as v128k (Zipf-like)
   b1024     B=1024, G=3, V=32000,  bf16, T=1,   target as v32k, draft noise 1.5
 
-The drafter's proposal x_i is drawn with the Gumbel-max trick from its own
-temperature-scaled logits (argmax at T=0), restricted to its top-k candidates
-when top-k is set (``torch.topk``); the nucleus is not applied to the
-proposal, so a proposal may fall outside the filtered draft distribution --
-a case the verification rule handles (q(x) = 0).
+The drafter's proposal x_i is sampled from the drafter's own filtered
+distribution, the way the drafter would sample it: Gumbel-max over its
+temperature-scaled logits (argmax at T=0), restricted to the kept set of the
+row's top-k and then top-p (the smallest prefix of the drafter's tokens by
+probability, ties to the lower id, whose mass reaches top-p).  This is input
+generation only (it stands in for the draft model's sampler); the
+verification arithmetic lives in the library and, independently, in the oracle.
 """
 from __future__ import annotations
 
@@ -120,21 +122,31 @@ def _boosted_normal(rows: int, V: int, g: torch.Generator, device) -> torch.Tens
     return t
 
 
-def _propose(draft: torch.Tensor, T: torch.Tensor, top_k: Optional[torch.Tensor], g: torch.Generator) -> torch.Tensor:
-    """The drafter's own proposal per row: Gumbel-max on logits / T, argmax at T = 0."""
+def _propose(draft: torch.Tensor, T: torch.Tensor, top_k: Optional[torch.Tensor], top_p: Optional[torch.Tensor],
+             g: torch.Generator) -> torch.Tensor:
+    """The drafter's own proposal per row: Gumbel-max on logits / T over the row's
+    top-k-then-top-p kept set; argmax at T = 0."""
     B, G, V = draft.shape
     d = draft.to(torch.float32)
     u = torch.rand(d.shape, generator=g, device=d.device).clamp_(1e-12, 1.0 - 1e-7)
     gumbel = -torch.log(-torch.log(u))
     Tb = T.view(B, 1, 1).to(torch.float32)
-    score = torch.where(Tb > 0, d / Tb.clamp_min(1e-30) + gumbel, d)
-    if top_k is not None:
-        k = int(top_k.max().item())
-        if 0 < k < V:
-            cand = d.topk(k, dim=2).indices  # the drafter's top-k candidates
-            cs = score.gather(2, cand)
-            pick = cs.argmax(dim=2, keepdim=True)
-            return cand.gather(2, pick).squeeze(2).to(torch.int32)
+    z = torch.where(Tb > 0, d / Tb.clamp_min(1e-30), d)
+    if top_k is not None or top_p is not None:
+        zs, order = torch.sort(z, dim=2, descending=True, stable=True)  # ties: lower id first
+        rank = torch.arange(V, device=d.device).view(1, 1, V)
+        keep = torch.ones_like(zs, dtype=torch.bool)
+        if top_k is not None:
+            k = top_k.view(B, 1, 1).to(torch.long)
+            keep &= (k <= 0) | (k >= V) | (rank < k)
+        if top_p is not None:
+            w = torch.where(keep, torch.exp(zs - zs[:, :, :1]), torch.zeros_like(zs))
+            w = w / w.sum(dim=2, keepdim=True)
+            before = torch.cumsum(w.to(torch.float64), dim=2) - w.to(torch.float64)  # mass ahead of each token
+            keep &= before < top_p.view(B, 1, 1).to(torch.float64)
+        mask = torch.zeros_like(keep).scatter_(2, order, keep)
+        z = torch.where(mask, z, torch.full_like(z, float("-inf")))
+    score = torch.where(Tb > 0, z + gumbel, z)
     return score.argmax(dim=2).to(torch.int32)
 
 
@@ -185,7 +197,7 @@ def make(name: str, seed: int = 0, device="cpu", *, B: Optional[int] = None, G: 
         target = target.contiguous()
         draft = draft.contiguous()
     T = T.to(torch.float32)
-    tokens = _propose(draft, T, top_k, g)
+    tokens = _propose(draft, T, top_k, top_p, g)
     if num_draft is not None:  # padding positions past gamma_b are never read; keep them valid anyway
         pos = torch.arange(G, device=device).view(1, G)
         tokens = torch.where(pos < num_draft.view(B, 1).to(torch.long), tokens, torch.zeros_like(tokens))

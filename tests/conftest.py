@@ -30,3 +30,17 @@ def golden():
             return json.load(f)
 
     return load
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Every parity report checked in this session: decisions, low-margin and
+    excused counts, the largest alpha / probability errors and the excused rows."""
+    try:
+        from tests.parity import REPORTS
+    except Exception:
+        return
+    if not REPORTS:
+        return
+    terminalreporter.section("parity reports")
+    for name, text in REPORTS:
+        terminalreporter.write_line(f"{name}: {text}")

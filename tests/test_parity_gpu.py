@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from tests.parity import ParityReport, compare, compare_probs, to_np
+from tests.parity import ParityReport, assert_ok, compare, compare_probs, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -43,12 +43,8 @@ def run(wl, seed=None, path="auto", probs=False, rows=None, report=None):
     g = {k: v[torch.as_tensor(rows, device=v.device)] for k, v in gpu.items()}
     rep = compare(g, ora, sub.gammas(), wl.G, report)
     if probs:
-        compare_probs(g, ora, sub.gammas(), rep)
+        compare_probs(g, ora, sub.gammas(), rep, inputs=ni, oracle_mod=oracle)
     return rep, g, ora
-
-
-def assert_ok(rep: ParityReport):
-    assert rep.ok(), str(rep)
 
 
 # ---------------------------------------------------------------------------
