@@ -72,6 +72,7 @@ typedef enum {
 #define SV_ROW_BAD_DRAFT_TOKEN 0x10u /* a draft token outside [0, V) */
 #define SV_ROW_NONFINITE 0x20u       /* NaN or +inf logit, or a row with no finite logit */
 #define SV_ROW_INTERNAL 0x40u        /* a device-side wait gave up (internal error); outputs are defaults */
+#define SV_ROW_BAD_LENIENCE 0x80u    /* lenience NaN or outside [0, 1] (spec_verify_ex) */
 
 /* supported maxima */
 #define SV_MAX_GAMMA 32
@@ -137,6 +138,21 @@ typedef enum {
  *   ev_dense   the same around the dense cluster kernel (top-k > 256)
  *   ev_free    the same around the whole-row kernel of rows with no top-k
  *              (its per-unit tail kernel follows, outside the events)
+ *   lenience   [B] float or NULL (1 everywhere): the lenient acceptance test of
+ *              the review page's section Lenience -- draft token x_i is accepted
+ *              iff u_i * l_b * q_i(x_i) < p_i(x_i), so no token is emitted with
+ *              more than 1/l_b times its probability under p, and alpha_i becomes
+ *              the acceptance probability sum_x min(q_i(x), p_i(x) / l_b).  The
+ *              residual draw is unchanged.  l_b = 1 is the exact rule; NaN or a
+ *              value outside [0, 1] gives SV_ROW_BAD_LENIENCE.
+ *   wait_limit_ns  limit of each device-side wait on another warp or on a copy
+ *              (0 = the default, 2 s; below 1000 a wait gives up after one try,
+ *              since the device timer ticks about once a microsecond).  A wait that runs out makes the call mark
+ *              SV_ROW_INTERNAL on the sequences of the kernel that gave up and of
+ *              the paths whose kernels run after it in the same call (their
+ *              outputs are the defaults of an invalid sequence); the context stays
+ *              usable and the next call is unaffected.  For tests of that path;
+ *              production callers leave it 0.
  */
 typedef struct {
     uint32_t struct_size;
@@ -146,6 +162,8 @@ typedef struct {
     void* ev_stream[2];
     void* ev_dense[2];
     void* ev_free[2];
+    const float* lenience;
+    uint64_t wait_limit_ns;
 } sv_options;
 
 int spec_verify_ex(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,

@@ -28,6 +28,8 @@ ROW_BAD_TOP_P = 0x04
 ROW_BAD_NUM_DRAFT = 0x08
 ROW_BAD_DRAFT_TOKEN = 0x10
 ROW_NONFINITE = 0x20
+ROW_INTERNAL = 0x40
+ROW_BAD_LENIENCE = 0x80
 
 # every symbol include/spec_verify.h declares
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_verify_host",
@@ -46,7 +48,7 @@ class SpecVerifyError(RuntimeError):
 class _Options(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32), ("pos_accept", ctypes.c_void_p), ("pos_token", ctypes.c_void_p),
                 ("path", ctypes.c_int32), ("ev_stream", ctypes.c_void_p * 2), ("ev_dense", ctypes.c_void_p * 2),
-                ("ev_free", ctypes.c_void_p * 2)]
+                ("ev_free", ctypes.c_void_p * 2), ("lenience", ctypes.c_void_p), ("wait_limit_ns", ctypes.c_uint64)]
 
 
 _lib = None
@@ -143,7 +145,7 @@ def _dev_vec(x, B: int, dtype: torch.dtype, device, name: str) -> Optional[torch
 def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor, temperature,
                 num_draft=None, top_k=None, top_p=None, *, seed: int, probs: bool = False,
                 positions: bool = False, path: str = "auto", events: Optional[dict] = None, stream=None,
-                workspace: Optional[torch.Tensor] = None) -> dict:
+                workspace: Optional[torch.Tensor] = None, lenience=None, wait_limit_ns: int = 0) -> dict:
     """Verify one batch of drafts on the GPU.
 
     target [B, G+1, V] and draft [B, G, V] (float32 or bfloat16, CUDA, contiguous),
@@ -153,7 +155,9 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.T
     request, p_out / q_out (probs=True) and pos_accept / pos_token (positions=True).
     events: {"stream": (begin, end), "dense": (begin, end), "free": (begin, end)} torch.cuda.Event
     pairs that the library records on the launching stream around its streaming top-k, dense
-    cluster and whole-row (no top-k) kernels.
+    cluster and whole-row (no top-k) kernels.  lenience: per-sequence l in [0, 1] (None = 1, the
+    exact rule): accept iff u * l * q(x) < p(x).  wait_limit_ns: limit of the kernels' waits on
+    one another (0 = the default 2 s; a test hook for the give-up path).
     """
     lib = load_library()
     if not (target.is_cuda and draft.is_cuda):
@@ -177,6 +181,7 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.T
     nd = _dev_vec(num_draft, B, torch.int32, dev, "num_draft")
     tk = _dev_vec(top_k, B, torch.int32, dev, "top_k")
     tp = _dev_vec(top_p, B, torch.float32, dev, "top_p")
+    ln = _dev_vec(lenience, B, torch.float32, dev, "lenience")
 
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     out = torch.empty(B, G + 1, dtype=torch.int32, device=dev)
@@ -191,6 +196,8 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.T
     ws = workspace if workspace is not None else _workspace(need, dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     opts = _Options(ctypes.sizeof(_Options), _ptr(pa), _ptr(pt), SV_PATH_DENSE if path == "dense" else SV_PATH_AUTO)
+    opts.lenience = None if ln is None else ln.data_ptr()
+    opts.wait_limit_ns = int(wait_limit_ns)
     for key in ("stream", "dense", "free"):  # optional (begin, end) torch.cuda.Event pairs around each kernel
         if events and events.get(key):
             getattr(opts, "ev_" + key)[0] = events[key][0].cuda_event

@@ -54,15 +54,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
         const int b = b0 + threadIdx.x;
         uint32_t nrows = 0, nunits = 0, st = 0, mode = kModeErr;
         int gamma = 0, k = 0;
-        float T = 0.0f, P = 1.0f;
+        float T = 0.0f, P = 1.0f, L = 1.0f;
         if (b < a.B) {
             gamma = a.num_draft ? a.num_draft[b] : G;
             T = a.temperature[b];
             const int kr = a.top_k ? a.top_k[b] : 0;
             const float pr = a.top_p ? a.top_p[b] : 1.0f;
+            L = a.lenience ? a.lenience[b] : 1.0f;
             if (!(T >= 0.0f) || isinf(T)) st |= SV_ROW_BAD_TEMPERATURE;
             if (kr < 0) st |= SV_ROW_BAD_TOP_K;
             if (!(pr > 0.0f && pr <= 1.0f)) st |= SV_ROW_BAD_TOP_P;
+            if (!(L >= 0.0f && L <= 1.0f)) st |= SV_ROW_BAD_LENIENCE;
             if (gamma < 1 || gamma > G) {
                 st |= SV_ROW_BAD_NUM_DRAFT;
             } else {
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
             si.T = T;
             si.P = P;
             si.row_off = base_rows + off_r;
-            si.pad = 0;
+            si.L = L;
             a.seq[b] = si;
             a.seq_done[b] = 0;
             a.seq_status[b] = st;
@@ -254,7 +256,9 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
     a.temperature = temperature;
     a.top_k = top_k;
     a.top_p = top_p;
+    a.lenience = opt.lenience;
     a.seed = seed;
+    a.wait_ns = opt.wait_limit_ns ? (unsigned long long)opt.wait_limit_ns : kWaitLimitNs;
     a.B = B;
     a.G = gamma_max;
     a.V = V;

@@ -272,17 +272,19 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
         return;
     }
 
-    // acceptance test u * q(x) < p(x)
+    // acceptance test u * l * q(x) < p(x) (l = 1: the exact rule)
     int accept = 0;
     if (pair) {
         const int x = a.draft_tokens[(size_t)b * G + unit];
         const double px = (double)prob_of(sm.byid[0], sm.prob[0], kt, x);
         const double qx = (double)prob_of(sm.byid[1], sm.prob[1], kd, x);
-        accept = (u_acc * qx < px) ? 1 : 0;
+        accept = lenient_accept(u_acc, si.L, qx, px) ? 1 : 0;
     }
 
-    // alpha_i = sum_x min(p, q) and the residual weights, in ascending token id
-    // over the target's kept ids (an id kept only by the draft has p = 0)
+    // alpha_i = sum_x min(p, q) (under lenience l, sum_x min(q, p / l)) and the
+    // residual weights, in ascending token id over the target's kept ids (an id
+    // kept only by the draft has p = 0, so it adds nothing to either)
+    const float invl = lenience_inv(si.L);
     float rr[kStreamMaxK / 32];
     CF alpha{0.0f, 0.0f}, Z{0.0f, 0.0f}, Zp{0.0f, 0.0f};
 #pragma unroll
@@ -293,7 +295,7 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
             const unsigned long long e = sm.byid[0][j];
             const float p = sm.prob[0][(uint32_t)e];
             const float q = pair ? prob_of(sm.byid[1], sm.prob[1], kd, (int)(e >> 32)) : 0.0f;
-            alpha = cf_add(alpha, CF{fminf(p, q), 0.0f});
+            alpha = cf_add(alpha, CF{accept_mass(p, q, invl), 0.0f});
             rr[m] = fmaxf(p - q, 0.0f);  // bonus: q_{gamma+1} := 0
             Z = cf_add(Z, CF{rr[m], 0.0f});
             Zp = cf_add(Zp, CF{p, 0.0f});

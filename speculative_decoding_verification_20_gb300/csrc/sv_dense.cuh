@@ -7,7 +7,7 @@
 //   max            -> softmax with temperature via exp2 (one exponential per logit)
 //   radix select   -> top-k (count-weighted) then top-p (mass-weighted), ties by id
 //   alpha_i        =  sum_x min(p, q)
-//   acceptance     u * q(x) < p(x)
+//   acceptance     u * l * q(x) < p(x)   (lenience l, 1 = the exact rule)
 //   residual/bonus inverse CDF in ascending token id (hierarchical search:
 //                  cluster prefix -> load group -> thread scan -> element).
 // Cross-CTA values move through distributed shared memory (DSMEM) with one
@@ -440,13 +440,18 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
     const int V = a.V, G = a.G;
     grid_dependency_wait();  // the previous kernels of the call (the plan's lists)
     const uint32_t n_units = a.counts[kCntDenseUnits];
+    // a wait of an earlier kernel gave up: the whole-row tail kernel has then
+    // already finished (as failed) every unit that kernel handed over here
+    const bool failed = a.counts[kCntError] != 0u;
     const uint32_t cid = blockIdx.x / (uint32_t)c.cs, ncl = gridDim.x / (uint32_t)c.cs;
 
     for (uint32_t w = cid; w < n_units; w += ncl) {
         const uint32_t item = a.dense_units[w];
         const int b = (int)(item >> 8), u = (int)(item & 0xFFu);
         const SeqInfo si = a.seq[b];
+        if (failed && si.mode == kModeFree) continue;  // uniform over the cluster: every CTA skips it
         const bool pair = u < si.gamma;
+        const float Lb = si.L;
         const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
         const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
 
@@ -564,6 +569,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
 
         // ---- alpha, acceptance gather; the residual weights replace q in place
         const int x_tok = pair ? a.draft_tokens[(size_t)b * G + u] : -1;
+        const float invl = lenience_inv(Lb);  // alpha under lenience: sum_x min(q, p / l)
         double part[4] = {0.0, 0.0, 0.0, 0.0};
         {
             float al = 0.0f, rs = 0.0f;
@@ -573,7 +579,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
                 for (int j = 0; j < C::VEC; ++j) {
                     const int i = l * C::VEC + j;
                     const float p = xt[i], q = xd[i];
-                    al += fminf(p, q);
+                    al += accept_mass(p, q, invl);
                     if (col_of<TIn, R>(c, l, j) == x_tok) {
                         part[1] = (double)p;
                         part[2] = (double)q;
@@ -599,7 +605,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
         // v = u * Z, with Z the search's own hierarchical total, so that v < Z exactly
         const int token = ordered_search<TIn, R>(
             c, sm, [&](int l, int j) -> float { return xd[l * C::VEC + j]; }, ur, true, true, &cum);
-        const int accept = pair ? ((ua * qx < px) ? 1 : 0) : 0;
+        const int accept = pair ? (lenient_accept(ua, Lb, qx, px) ? 1 : 0) : 0;
 
         if (c.crank == 0) {
             if (t == 0) {

@@ -12,7 +12,8 @@
 //   - alpha = sum_x min(p, q) and the residual weights r = max(0, p - q)
 //     (p for the bonus row),
 //   - the acceptance test u * q(x) < p(x) of the draft token
-//     ("Speculative decoding: the art of guessing well", section 投机采样),
+//     ("Speculative decoding: the art of guessing well", section 投机采样), with
+//     q(x) scaled by the sequence's lenience (review page, section Lenience),
 //   - the residual / bonus draw: v = u * sum r and the first token id at which
 //     the running sum of r passes v.
 //
@@ -47,7 +48,6 @@ namespace {
 
 constexpr int kFStages = 3;
 constexpr int kFVec = kFreeBlockBytes / 16 / 32;  // 16-byte vectors per lane per segment (4)
-constexpr unsigned long long kFWaitNs = 2000000000ull;
 // W consumer warps and a producer warp; up to 128 registers a thread either way
 // (7: 2 CTAs per SM, 15: 1 CTA per SM)
 template <int W>
@@ -95,6 +95,8 @@ struct FreeSmem {
     int ncnt[2];                      // per row: crossing elements collected
     uint32_t cut_key[2], cut_id[2];   // per row: the last kept element (key, id)
     float kinv[2];                    // per row: 1 / (sum x kept mass); -1: too many ties at the cut
+    float lhdr[kFStages];             // the unit's lenience, with uhdr
+    unsigned long long wait_ns;       // limit of every wait on another warp or a copy (Args::wait_ns)
 };
 
 // 228 KB of shared memory per SM, less 1 KB reserved per CTA
@@ -114,12 +116,12 @@ __device__ __forceinline__ void fbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void fbar_expect(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fs_u32(bar)), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ bool fbar_try(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool fbar_try(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(fs_u32(bar)), "r"(parity), "r"(1000000u)
+        : "r"(fs_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -128,11 +130,14 @@ __device__ __forceinline__ unsigned long long fs_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-__device__ __forceinline__ bool fbar_wait(uint64_t* bar, uint32_t parity) {
-    if (fbar_try(bar, parity)) return true;
+// bounded wait: false after about limit_ns (each try sleeps at most min(limit_ns, 1 ms))
+__device__ __forceinline__ bool fbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+    const uint32_t hint = limit_ns < 1000000ull ? (uint32_t)limit_ns : 1000000u;
+    if (fbar_try(bar, parity, hint)) return true;
+    if (limit_ns < 1000ull) return false;  // below the timer's ~1 us resolution: one try only
     const unsigned long long t0 = fs_ns();
-    while (!fbar_try(bar, parity))
-        if (fs_ns() - t0 > kFWaitNs) return false;
+    while (!fbar_try(bar, parity, hint))
+        if (fs_ns() - t0 > limit_ns) return false;
     return true;
 }
 __device__ __forceinline__ void ftma(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -151,7 +156,7 @@ __device__ __forceinline__ bool fsync(FreeSmem<W>& sm, FSync& g) {
     __syncwarp();
     if (!g.ok) return false;
     if ((threadIdx.x & 31) == 0) fbar_arrive(&sm.gsync);
-    g.ok = __all_sync(0xFFFFFFFFu, fbar_wait(&sm.gsync, g.ph));
+    g.ok = __all_sync(0xFFFFFFFFu, fbar_wait(&sm.gsync, g.ph, sm.wait_ns));
     g.ph ^= 1u;
     return g.ok;
 }
@@ -602,6 +607,7 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
         }
         fbar_init(&sm.gsync, kFWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        sm.wait_ns = a.wait_ns;
     }
     __syncthreads();
     grid_dependency_wait();  // the previous kernels of the call (the plan's lists)
@@ -633,13 +639,14 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
                     const int pass = nucleus ? pi : (pi == 0 ? 0 : kPassFinal);
                     for (int tile = 0; tile < ntiles && ok; ++tile) {
                         const int col = tile * TS, n = min(TS, V - col);
-                        if (!fbar_wait(&sm.empty[stage], ph)) {
+                        if (!fbar_wait(&sm.empty[stage], ph, sm.wait_ns)) {
                             ok = false;
                             break;
                         }
                         if (lane == 0) {
                             sm.hdr[stage] = make_int4((int)w, pass, tile, n);
                             sm.uhdr[stage] = make_int4((int)item, si.gamma, __float_as_int(si.T), __float_as_int(si.P));
+                            sm.lhdr[stage] = si.L;
                         }
                         if (TMA) {
                             const uint32_t bytes = (uint32_t)(n * sizeof(TIn));
@@ -664,15 +671,17 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
                     }
                 }
             }
-            if (ok && fbar_wait(&sm.empty[stage], ph)) {
+            if (ok && fbar_wait(&sm.empty[stage], ph, sm.wait_ns)) {
                 if (lane == 0) {
                     sm.hdr[stage] = make_int4(-1, 0, 0, 0);
                     fbar_arrive(&sm.full[stage]);
                 }
             } else if (lane == 0) {
                 atomicOr(&a.counts[kCntError], 1u);
-                for (int s = 0; s < kFStages; ++s)  // let every copy already issued land
-                    if (issued[s] >= 0) (void)fbar_wait(&sm.full[s], (uint32_t)issued[s]);
+                // let every copy already issued land (with the full limit: a copy in
+                // flight must not outlive the CTA)
+                for (int s = 0; s < kFStages; ++s)
+                    if (issued[s] >= 0) (void)fbar_wait(&sm.full[s], (uint32_t)issued[s], kWaitLimitNs);
             }
         }
         return;
@@ -688,7 +697,7 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
     int b = 0, u = 0, par = 1;
     bool pair = false, nf = false, dead = false;
     bool nuc = false, fall = false;  // top-p < 1; the unit goes to the cluster kernel
-    float c = 1.0f, Pf = 1.0f;
+    float c = 1.0f, Pf = 1.0f, invl = 1.0f;  // invl: 1 / lenience (alpha = sum_x min(q, p * invl))
     Online op, oq;
     float Mp = 0.0f, Mq = 0.0f, Sp = 0.0f, Sq = 0.0f, invp = 0.0f, invq = 0.0f, invp2 = 0.0f, invq2 = 0.0f;
     float nmcp = 0.0f, nmcq = 0.0f;  // row_nmc of each row's maximum
@@ -707,7 +716,7 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
         for (int i = kFWarps; i < kFreeWarpsWide; ++i) R.alpha[i] = 0.0f;
     };
     while (true) {
-        if (!__all_sync(0xFFFFFFFFu, fbar_wait(&sm.full[stage], ph))) {
+        if (!__all_sync(0xFFFFFFFFu, fbar_wait(&sm.full[stage], ph, sm.wait_ns))) {
             g.ok = false;
             break;
         }
@@ -723,6 +732,7 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
             const float T = __int_as_float(uh.z);
             c = 1.4426950408889634f / T;
             Pf = __int_as_float(uh.w);
+            invl = lenience_inv(sm.lhdr[stage]);
             nuc = Pf < 1.0f;
             fall = false;
             cutp = cutq = 0ull;
@@ -919,7 +929,7 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
                         const uint32_t id = (uint32_t)(col + e0 + j);
                         const float p = j < valid ? kept_prob<CUT>(xp[j], id, c, nmcp, invp2, cutp) : 0.0f;
                         const float q = j < valid ? kept_prob<CUT>(xq[j], id, c, nmcq, invq2, cutq) : 0.0f;
-                        ma[j] = fminf(p, q);
+                        ma[j] = accept_mass(p, q, invl);
                         ra[j] = resid_f(p, q);
                         pa[j] = p;
                     }
@@ -956,8 +966,9 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
         };
         // a full tile without the debug outputs: packed pairs, no bounds per element;
         // the sums run over the thread's pairs in order
-        auto final_fast = [&](auto cut_on) {
+        auto final_fast = [&](auto cut_on, auto len_on) {
             constexpr bool CUT = decltype(cut_on)::value;
+            constexpr bool LEN = decltype(len_on)::value;  // lenience < 1: alpha term min(q, p / l)
             constexpr int H = F::VEC / 2;
             const float2 c2 = make_float2(c, c), np2 = make_float2(nmcp, nmcp), nq2 = make_float2(nmcq, nmcq);
             const float2 ip2 = make_float2(invp2, invp2), iq2 = make_float2(invq2, invq2);
@@ -986,7 +997,10 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
                             if (!kept_at(xq[k].y, id0 + 2 * k + 1, lcq, icq)) q.y = 0.0f;
                         }
                         const float2 d = __ffma2_rn(q, m1, p);  // p - q, one rounding
-                        am = __fadd2_rn(am, make_float2(fminf(p.x, q.x), fminf(p.y, q.y)));
+                        if (LEN)
+                            am = __fadd2_rn(am, make_float2(accept_mass(p.x, q.x, invl), accept_mass(p.y, q.y, invl)));
+                        else
+                            am = __fadd2_rn(am, make_float2(fminf(p.x, q.x), fminf(p.y, q.y)));
                         ar = __fadd2_rn(ar, make_float2(fmaxf(d.x, 0.0f), fmaxf(d.y, 0.0f)));
                     }
                     ap = __fadd2_rn(ap, p);
@@ -997,10 +1011,16 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
             alpha.add(am.x + am.y);
         };
         if (n == TS && !(a.p_out || a.q_out)) {
-            if (nuc)
-                final_fast(std::true_type{});
-            else
-                final_fast(std::false_type{});
+            if (invl != 1.0f) {
+                if (nuc)
+                    final_fast(std::true_type{}, std::true_type{});
+                else
+                    final_fast(std::false_type{}, std::true_type{});
+            } else if (nuc) {
+                final_fast(std::true_type{}, std::false_type{});
+            } else {
+                final_fast(std::false_type{}, std::false_type{});
+            }
         } else if (nuc) {
             final_tile(std::true_type{});
         } else {
@@ -1175,7 +1195,7 @@ __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
                 const double px = kx < cutp ? 0.0 : (double)exp2_prod(lpx, Mp, c, clo, nmcp) * (double)invp2;
                 const double qx = kqx < cutq ? 0.0 : (double)exp2_prod(lqx, Mq, c, clo, nmcq) * (double)invq2;
                 const double ua = uniform01(a.seed, (uint32_t)b, (uint32_t)(u + 1), 0u);
-                accept = (ua * qx < px) ? 1 : 0;
+                accept = lenient_accept(ua, si.L, qx, px) ? 1 : 0;
             }
         }
         if (lane == 0) {

@@ -41,6 +41,8 @@ namespace sv {
 // configuration
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
+// default limit of every bounded wait (an mbarrier phase, a peer warp): 2 s
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr int kTileBytes = 28672;   // one TMA bulk copy: 7 16-byte vectors per consumer thread
 constexpr int kTilesPerPiece = 10;  // a piece of a row: up to 280 KB of logits (a whole 128k bf16 row)
 constexpr int kStreamMaxK = SV_STREAM_MAX_TOP_K;
@@ -93,7 +95,7 @@ struct SeqInfo {
     float T;          // temperature (0 = greedy)
     float P;          // effective top-p (1 = off)
     uint32_t row_off; // index of this sequence's first row in the stream row list
-    uint32_t pad;
+    float L;          // lenience in [0, 1] (1 = the exact rule)
 };
 
 // Everything a kernel needs, passed by value.
@@ -105,7 +107,9 @@ struct Args {
     const float* temperature;
     const int32_t* top_k;
     const float* top_p;
+    const float* lenience;  // [B] or nullptr (1 everywhere)
     uint64_t seed;
+    unsigned long long wait_ns;  // limit of each bounded wait on another warp (kWaitLimitNs by default)
     int B, G, V;
     int32_t* accepted_len;
     int32_t* out_tokens;
@@ -213,6 +217,20 @@ __device__ __forceinline__ uint32_t philox_w0(uint32_t c0, uint32_t c1, uint32_t
     }
     return c0;
 }
+
+// Acceptance under lenience L ("Fast Inference from Transformers via
+// Speculative Decoding" review page, section Lenience: q(x) is multiplied by L
+// in the test): accept iff u * (L * q(x)) < p(x), formed in double.  L = 1 is
+// the exact rule u * q(x) < p(x).
+__device__ __forceinline__ bool lenient_accept(double u, float L, double qx, double px) {
+    return u * ((double)L * qx) < px;
+}
+// 1 / L for the acceptance mass below (a huge finite value for L = 0, so that
+// 0 * invl stays 0); exactly 1 for L = 1.
+__device__ __forceinline__ float lenience_inv(float L) { return L > 0.0f ? 1.0f / L : 3.0e38f; }
+// Acceptance mass of one token, q(x) P(accept | x) = min(q(x), p(x) / L); with
+// L = 1 it is min(p(x), q(x)) bit for bit.
+__device__ __forceinline__ float accept_mass(float p, float q, float invl) { return fminf(q, p * invl); }
 
 // U(seed, b, pos, draw) = ((w >> 8) + 0.5) * 2^-24 (exact in double)
 __device__ __forceinline__ double uniform01(uint64_t seed, uint32_t b, uint32_t pos, uint32_t draw) {

@@ -48,7 +48,6 @@ constexpr int kStages = 3;
 constexpr int kConsumerWarps = 7;  // with the producer, 8 warps: 2 CTAs per SM at up to 128 registers
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kSelThreads = kConsumers + 32;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // ---------------------------------------------------------------------------
 // PTX helpers: mbarriers, TMA bulk copies, the consumer-only named barrier
@@ -65,13 +64,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 // try_wait with a suspend-time hint: the thread sleeps until the phase completes
-// (or about 1 ms passes) instead of spinning and taking issue slots
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// (or about hint_ns passes) instead of spinning and taking issue slots
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -80,12 +79,15 @@ __device__ __forceinline__ unsigned long long global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// bounded wait for the phase of parity `parity` to complete
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+// bounded wait for the phase of parity `parity` to complete: false after
+// about limit_ns (each try sleeps at most min(limit_ns, 1 ms))
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+    const uint32_t hint = limit_ns < 1000000ull ? (uint32_t)limit_ns : 1000000u;
+    if (mbar_try_wait(bar, parity, hint)) return true;
+    if (limit_ns < 1000ull) return false;  // below the timer's ~1 us resolution: one try only
     const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+    while (!mbar_try_wait(bar, parity, hint))
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
 }
 __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -119,6 +121,7 @@ struct SelSmem {
     int red[kConsumerWarps];
     int scan[kConsumerWarps];
     int hist[16];
+    unsigned long long wait_ns;        // limit of every wait on another warp or a copy (Args::wait_ns)
 };
 
 
@@ -133,7 +136,7 @@ __device__ __forceinline__ bool gbar(SelSmem& sm, GSync& g) {
     __syncwarp();
     if (!g.ok) return false;
     if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.gsync);
-    g.ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sm.gsync, g.ph));
+    g.ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sm.gsync, g.ph, sm.wait_ns));
     g.ph ^= 1u;
     return g.ok;
 }
@@ -765,6 +768,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (t < kConsumerWarps) sm.pub[t] = 0u;
+    if (t == 0) sm.wait_ns = a.wait_ns;
     __syncthreads();
     grid_dependency_wait();  // the plan kernel's lists and counters
     grid_dependents_go();
@@ -812,7 +816,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
                 const int c0 = piece * PE, c1 = min(V, c0 + PE);
                 for (int col = c0, tile = 0; col < c1 && ok; col += TE, ++tile) {
                     const int n = min(TE, c1 - col);
-                    if (!mbar_wait(&sm.empty[stage], ph)) {
+                    if (!mbar_wait(&sm.empty[stage], ph, sm.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -841,16 +845,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
                 gamma = gamma_next;
                 k = k_next;
             }
-            if (ok && mbar_wait(&sm.empty[stage], ph)) {
+            if (ok && mbar_wait(&sm.empty[stage], ph, sm.wait_ns)) {
                 if (lane == 0) {
                     sm.hdr[stage] = make_int4(-1, 0, 0, 0);
                     mbar_arrive(&sm.full[stage]);
                 }
             } else if (lane == 0) {
                 atomicOr(&a.counts[kCntError], 1u);
-                // let every copy already issued land before the CTA leaves
+                // let every copy already issued land before the CTA leaves (always
+                // with the full limit: a copy in flight must not outlive the CTA)
                 for (int s = 0; s < kStages; ++s)
-                    if (issued[s] >= 0) (void)mbar_wait(&sm.full[s], (uint32_t)issued[s]);
+                    if (issued[s] >= 0) (void)mbar_wait(&sm.full[s], (uint32_t)issued[s], kWaitLimitNs);
             }
         }
         return;
@@ -864,7 +869,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
     CState cs;
     cs.st = WarpList{0, 0u};
     while (true) {
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sm.full[stage], ph))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sm.full[stage], ph, sm.wait_ns))) {
             g.ok = false;
             break;
         }

@@ -45,7 +45,9 @@ def test_recorded_traffic_only_for_its_kernel_full_batch_and_sources():
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         rec = json.load(f)
     for wl, r in rec.items():
-        assert bench.recorded_traffic(wl, r["path"], True) == r["bytes_per_launch"]
+        # a record counts only while its kernel's sources are those it was captured with
+        current = r["kernel_hash"] == bench.kernel_hash(r["path"])
+        assert bench.recorded_traffic(wl, r["path"], True) == (r["bytes_per_launch"] if current else None)
         assert bench.recorded_traffic(wl, r["path"], False) is None  # another batch size
         other = "free" if r["path"] == "stream" else "stream"
         assert bench.recorded_traffic(wl, other, True) is None  # another kernel

@@ -26,12 +26,12 @@ def _built():
     oracle.build()
 
 
-def run(wl, seed=None, path="auto", probs=False, rows=None, report=None):
+def run(wl, seed=None, path="auto", probs=False, rows=None, report=None, lenience=None):
     seed = wl.seed if seed is None else seed
     dev = torch.device("cuda")
     w = wl.to(dev)
     gpu = sv.spec_verify(w.target, w.draft, w.draft_tokens, w.temperature, w.num_draft, w.top_k, w.top_p,
-                         seed=seed, positions=True, probs=probs, path=path)
+                         seed=seed, positions=True, probs=probs, path=path, lenience=lenience)
     torch.cuda.synchronize()
     rows = np.arange(wl.B) if rows is None else np.asarray(rows)
     sub = wl.subset(rows) if len(rows) != wl.B else wl
@@ -39,7 +39,7 @@ def run(wl, seed=None, path="auto", probs=False, rows=None, report=None):
     ua, ur = oracle.philox_uniforms(seed, wl.B, wl.G)
     ora = oracle.verify(ni["target"], ni["draft"], ni["draft_tokens"], ni["temperature"], ni["num_draft"],
                         ni["top_k"], ni["top_p"], u_accept=ua[rows], u_resid=ur[rows], all_positions=True,
-                        probs=probs)
+                        probs=probs, lenience=None if lenience is None else np.asarray(lenience)[rows])
     g = {k: v[torch.as_tensor(rows, device=v.device)] for k, v in gpu.items()}
     rep = compare(g, ora, sub.gammas(), wl.G, report)
     if probs:
