@@ -114,7 +114,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
             a.seq[b] = si;
             a.seq_done[b] = 0;
             a.seq_status[b] = st;
-            for (int u = 0; u <= G; ++u) a.unit_done[(size_t)b * (G + 1) + u] = 0;
             for (uint32_t r = 0; r < nrows; ++r) a.stream_rows[base_rows + off_r + r] = ((uint32_t)b << 8) | r;
             for (uint32_t u = 0; u < nunits; ++u) a.dense_units[base_units + off_u + u] = ((uint32_t)b << 8) | u;
             for (uint32_t u = 0; u < nsunits; ++u) a.stream_units[base_sunits + off_s + u] = ((uint32_t)b << 8) | u;
@@ -275,7 +274,6 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
     a.seq = (SeqInfo*)(ws + L.seq);
     a.seq_done = (uint32_t*)(ws + L.seq_done);
     a.seq_status = (uint32_t*)(ws + L.seq_status);
-    a.unit_done = (uint32_t*)(ws + L.unit_done);
     a.unit_acc = (int32_t*)(ws + L.unit_acc);
     a.unit_tok = (int32_t*)(ws + L.unit_tok);
     a.stream_rows = (uint32_t*)(ws + L.stream_rows);

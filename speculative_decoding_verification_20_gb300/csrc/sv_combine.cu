@@ -21,7 +21,7 @@ constexpr int kCombineThreads = 128;  // 4 warps
 // ---------------------------------------------------------------------------
 constexpr int kCombineWarps = 4;  // two units per CTA, a warp pair per unit
 static_assert(kCombineWarps == 4, "pair_sync names two pairs");
-constexpr int kSelBuf = 512;      // a warp's scratch for a row's candidates
+constexpr int kSelBuf = 288;      // a warp's scratch for a row's candidates (a top-k plus one load step)
 static_assert(kSelBuf >= kStreamMaxK + 32, "the scratch holds a top-k plus one load step");
 
 // shared memory of one unit: row r = 0 (target) is handled by the pair's first
@@ -259,7 +259,7 @@ __device__ void combine_row(const Args& a, const SeqInfo& si, int unit, int r, C
 
 // The rest of a unit, by the pair's first warp once both rows are done.
 template <typename TIn>
-__device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, CombPair& sm, int lane) {
+__device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, CombPair& sm, int lane, int x) {
     const int G = a.G;
     const bool pair = unit < si.gamma;
     const int kt = sm.kept[0], kd = pair ? sm.kept[1] : 0;
@@ -275,7 +275,6 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
     // acceptance test u * l * q(x) < p(x) (l = 1: the exact rule)
     int accept = 0;
     if (pair) {
-        const int x = a.draft_tokens[(size_t)b * G + unit];
         const double px = (double)prob_of(sm.byid[0], sm.prob[0], kt, x);
         const double qx = (double)prob_of(sm.byid[1], sm.prob[1], kd, x);
         accept = lenient_accept(u_acc, si.L, qx, px) ? 1 : 0;
@@ -285,43 +284,34 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
     // residual weights, in ascending token id over the target's kept ids (an id
     // kept only by the draft has p = 0, so it adds nothing to either)
     const float invl = lenience_inv(si.L);
-    float rr[kStreamMaxK / 32];
+    // the residual weights in id order, kept in the target row's free scratch
+    float* rr = reinterpret_cast<float*>(sm.buf[0]);
     CF alpha{0.0f, 0.0f}, Z{0.0f, 0.0f}, Zp{0.0f, 0.0f};
-#pragma unroll
-    for (int m = 0; m < kStreamMaxK / 32; ++m) {
-        const int j = lane + 32 * m;
-        rr[m] = 0.0f;
-        if (j < kt) {
-            const unsigned long long e = sm.byid[0][j];
-            const float p = sm.prob[0][(uint32_t)e];
-            const float q = pair ? prob_of(sm.byid[1], sm.prob[1], kd, (int)(e >> 32)) : 0.0f;
-            alpha = cf_add(alpha, CF{accept_mass(p, q, invl), 0.0f});
-            rr[m] = fmaxf(p - q, 0.0f);  // bonus: q_{gamma+1} := 0
-            Z = cf_add(Z, CF{rr[m], 0.0f});
-            Zp = cf_add(Zp, CF{p, 0.0f});
-        }
+    for (int j = lane; j < kt; j += 32) {
+        const unsigned long long e = sm.byid[0][j];
+        const float p = sm.prob[0][(uint32_t)e];
+        const float q = pair ? prob_of(sm.byid[1], sm.prob[1], kd, (int)(e >> 32)) : 0.0f;
+        alpha = cf_add(alpha, CF{accept_mass(p, q, invl), 0.0f});
+        const float r = fmaxf(p - q, 0.0f);  // bonus: q_{gamma+1} := 0
+        rr[j] = r;
+        Z = cf_add(Z, CF{r, 0.0f});
+        Zp = cf_add(Zp, CF{p, 0.0f});
     }
     const float alpha_v = cf_val(warp_cf_sum(alpha));
     float Zt = cf_val(warp_cf_sum(Z));
     const bool use_p = !(Zt > 0.0f);  // p <= q everywhere: fall back to p
     if (use_p) {
         Zt = cf_val(warp_cf_sum(Zp));
-#pragma unroll
-        for (int m = 0; m < kStreamMaxK / 32; ++m) {
-            const int j = lane + 32 * m;
-            rr[m] = j < kt ? sm.prob[0][(uint32_t)sm.byid[0][j]] : 0.0f;
-        }
+        for (int j = lane; j < kt; j += 32) rr[j] = sm.prob[0][(uint32_t)sm.byid[0][j]];
     }
+    __syncwarp();
     // inverse CDF: the first id whose running sum passes v
     const double v = u_res * (double)Zt;
     int token = -1, last_pos = -1;
     CF carry{0.0f, 0.0f};
-#pragma unroll
-    for (int m = 0; m < kStreamMaxK / 32; ++m) {
-        const int c0 = 32 * m;
-        if (c0 >= kt || token >= 0) break;
+    for (int c0 = 0; c0 < kt && token < 0; c0 += 32) {
         const int j = c0 + lane;
-        const float r = rr[m];
+        const float r = j < kt ? rr[j] : 0.0f;
         const CF x = cf_add(carry, warp_cf_scan(CF{r, 0.0f}, lane));
         const unsigned pos = __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0f);
         if (pos) last_pos = c0 + 31 - __clz(pos);
@@ -361,8 +351,10 @@ __device__ __forceinline__ void pair_sync(int pr) {
 
 // a warp pair per unit (target row i with draft row i, or the bonus row alone):
 // the two rows are selected and normalised at the same time
+// 7 CTAs (14 units) per SM: the whole unit list of a 256-sequence, 8-unit batch
+// in one wave on 152 SMs (shared memory 7 x 29 KB, at most 73 registers)
 template <typename TIn>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(Args a) {
+__global__ void __launch_bounds__(kCombineThreads, 7) combine_kernel(Args a) {
     extern __shared__ __align__(16) uint8_t comb_raw[];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int pr = wid >> 1, r = wid & 1;
@@ -384,9 +376,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Args a) {
             }
             continue;
         }
+        // the draft token, loaded early: its latency hides behind the row work
+        const int x = (r == 0 && unit < si.gamma) ? a.draft_tokens[(size_t)b * a.G + unit] : 0;
         if (r == 0 || unit < si.gamma) combine_row<TIn>(a, si, unit, r, sm, lane);
         pair_sync(pr);
-        if (r == 0) combine_unit<TIn>(a, b, unit, si, sm, lane);
+        if (r == 0) combine_unit<TIn>(a, b, unit, si, sm, lane, x);
         pair_sync(pr);  // the rows may be rebuilt
     }
 }

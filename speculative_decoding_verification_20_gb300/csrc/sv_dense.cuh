@@ -440,6 +440,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
     const int V = a.V, G = a.G;
     grid_dependency_wait();  // the previous kernels of the call (the plan's lists)
     const uint32_t n_units = a.counts[kCntDenseUnits];
+    if (n_units == 0) return;  // nothing for any cluster: no shared memory is ever shared
     // a wait of an earlier kernel gave up: the whole-row tail kernel has then
     // already finished (as failed) every unit that kernel handed over here
     const bool failed = a.counts[kCntError] != 0u;
@@ -660,10 +661,16 @@ cudaError_t launch_dense_cluster(const Args& a, int cs, int sms, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3((unsigned)cs);
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters < 1) {
-        cudaGetLastError();
-        clusters = sms / cs > 0 ? sms / cs : 1;
+    // clusters of size cs resident at once (queried on the first launch of each size)
+    static int cached[17] = {};
+    if (cs < 1 || cs > 16) return cudaErrorInvalidValue;
+    int clusters = cached[cs];
+    if (clusters < 1) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters < 1) {
+            (void)cudaGetLastError();
+            clusters = sms / cs > 0 ? sms / cs : 1;
+        }
+        cached[cs] = clusters;
     }
     const long long upper = (long long)a.B * (a.G + 1);
     long long n = clusters;

@@ -613,6 +613,7 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
     grid_dependency_wait();  // the previous kernels of the call (the plan's lists)
     grid_dependents_go();
     const uint32_t n_units = a.counts[kCntFreeUnits];
+    if (n_units == 0) return;  // no sequence takes this path (the same value for every thread)
 
     if (warp == kFWarps) {
         // ------------------------------ producer ------------------------------

@@ -125,7 +125,6 @@ struct Args {
     SeqInfo* seq;
     uint32_t* seq_done;
     uint32_t* seq_status;
-    uint32_t* unit_done;
     int32_t* unit_acc;
     int32_t* unit_tok;
     uint32_t* stream_rows;
@@ -141,7 +140,7 @@ struct Args {
 };
 
 struct WsLayout {
-    size_t seq, seq_done, seq_status, unit_done, unit_acc, unit_tok, stream_rows, dense_units, stream_units, free_units,
+    size_t seq, seq_done, seq_status, unit_acc, unit_tok, stream_rows, dense_units, stream_units, free_units,
         counts, cand, cand_cnt, free_rec, free_blk, total;
     int ppr, free_nblk;
 };
@@ -171,7 +170,6 @@ __host__ __device__ inline WsLayout ws_layout(int B, int G, int V, int dtype) {
     L.seq = o;         o = align_up(o + sizeof(SeqInfo) * B, 256);
     L.seq_done = o;    o = align_up(o + 4 * (size_t)B, 256);
     L.seq_status = o;  o = align_up(o + 4 * (size_t)B, 256);
-    L.unit_done = o;   o = align_up(o + 4 * units, 256);
     L.unit_acc = o;    o = align_up(o + 4 * (size_t)B * G, 256);
     L.unit_tok = o;    o = align_up(o + 4 * units, 256);
     L.stream_rows = o; o = align_up(o + 4 * rows, 256);

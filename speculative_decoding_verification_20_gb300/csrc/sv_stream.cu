@@ -116,6 +116,7 @@ struct SelSmem {
     uint64_t gsync;                    // consumer-warp barrier (one arrival per warp, bounded waits)
     int4 hdr[kStages];                 // piece index (-1: no more work), tile index, elements, first column
     int2 seqk[kStages];                // sequence b and its top-k for the piece
+    int2 pce[kStages];                 // the piece's end column and its number of tiles
     uint32_t pub[kConsumerWarps];      // per warp: its ceil(k/W)-th largest key of the piece so far (0: none)
     uint32_t spec[32];                 // warp w's largest lane maxima of a piece's first tile at [4w, 4w + 4)
     int red[kConsumerWarps];
@@ -550,9 +551,56 @@ __device__ __forceinline__ bool consume_tile(SelSmem& sm, GSync& g, const uint4 
     const float thv = th == 0u ? -INFINITY : (float)E::key_value(th);
     // filter: one pass bit per element of this thread's vectors (bit q * VEC + j)
     static_assert(Q * E::VEC <= 64, "a thread's elements of a tile fit one mask");
+    static_assert(Q * kConsumers * E::VEC * (int)sizeof(TIn) == kTileBytes, "a full tile is whole vectors");
+    unsigned long long pm = 0ull;
+    if (n == kTileBytes / (int)sizeof(TIn)) {
+        // A full tile: the NaN-propagating maximum of each vector, then of the
+        // thread's Q vectors (a tree); only when that reaches the threshold are
+        // the vectors tested one by one.  A NaN anywhere makes the thread's
+        // maximum NaN, which passes nothing and flags the row (whose outputs
+        // are then the defaults of a non-finite sequence, whatever was appended).
+        if constexpr (sizeof(TIn) == 2) {
+            const __nv_bfloat162 th2 = __float2bfloat162_rn(thv);
+            __nv_bfloat162 mq[Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q)
+                mq[q] = __hmax2_nan(__hmax2_nan(as_bf2(v[q].x), as_bf2(v[q].y)),
+                                    __hmax2_nan(as_bf2(v[q].z), as_bf2(v[q].w)));
+            __nv_bfloat162 tm[Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) tm[q] = mq[q];
+#pragma unroll
+            for (int w2 = Q / 2; w2 > 0; w2 >>= 1)
+#pragma unroll
+                for (int q = 0; q < w2; ++q) tm[q] = __hmax2_nan(tm[q], tm[q + w2]);
+            cs.run_max = fmax_nan(cs.run_max, __bfloat162float(__hmax_nan(__low2bfloat16(tm[0]), __high2bfloat16(tm[0]))));
+            if (__hge2_mask(tm[0], th2)) {
+#pragma unroll
+                for (int q = 0; q < Q; ++q)
+                    if (__hge2_mask(mq[q], th2))
+                        pm |= (unsigned long long)pass_mask(v[q], thv, (TIn*)nullptr) << (q * E::VEC);
+            }
+        } else {
+            float mq[Q], tm[Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                mq[q] = vmax_nan(v[q], (TIn*)nullptr);
+                tm[q] = mq[q];
+            }
+#pragma unroll
+            for (int w2 = Q / 2; w2 > 0; w2 >>= 1)
+#pragma unroll
+                for (int q = 0; q < w2; ++q) tm[q] = fmax_nan(tm[q], tm[q + w2]);
+            cs.run_max = fmax_nan(cs.run_max, tm[0]);
+            if (tm[0] >= thv) {
+#pragma unroll
+                for (int q = 0; q < Q; ++q)
+                    if (mq[q] >= thv) pm |= (unsigned long long)pass_mask(v[q], thv, (TIn*)nullptr) << (q * E::VEC);
+            }
+        }
+    } else {
     typename RunOf<TIn>::type rs;
     run_init(rs, thv);
-    unsigned long long pm = 0ull;
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
         const int e0 = (q * kConsumers + t) * E::VEC;
@@ -572,11 +620,19 @@ __device__ __forceinline__ bool consume_tile(SelSmem& sm, GSync& g, const uint4 
         pm |= (unsigned long long)msk << (q * E::VEC);
     }
     cs.run_max = fmax_nan(cs.run_max, run_value(rs));
+    }
 
     // append: what passed is read back from the tile (elem) by index
     if (__any_sync(0xFFFFFFFFu, pm != 0ull)) {
-        int tot;
-        const int pre = warp_prefix<7>((unsigned)__popcll(pm), &tot);
+        int tot, pre;
+        const int cl = __popcll(pm);
+        if (__all_sync(0xFFFFFFFFu, cl <= 1)) {  // the usual case: at most one per lane, one ballot
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, cl != 0);
+            pre = __popc(bal & lanemask_lt());
+            tot = __popc(bal);
+        } else {
+            pre = warp_prefix<7>((unsigned)cl, &tot);
+        }
         if (cs.st.cnt + tot <= kWarpCap) {
             int slot = cs.st.cnt + pre;
             while (pm) {
@@ -773,6 +829,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
     grid_dependency_wait();  // the plan kernel's lists and counters
     grid_dependents_go();
     const uint32_t n_pieces = a.counts[kCntStreamRows] * (uint32_t)ppr;
+    if (n_pieces == 0) return;  // no sequence takes this path (the same value for every thread)
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
@@ -823,6 +880,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
                     if (lane == 0) {
                         sm.hdr[stage] = make_int4((int)w, tile, n, col);
                         sm.seqk[stage] = make_int2(b, k);
+                        sm.pce[stage] = make_int2(c1, (c1 - c0 + TE - 1) / TE);
                     }
                     if (TMA) {
                         mbar_arrive_expect_tx(&sm.full[stage], (uint32_t)(n * sizeof(TIn)));
@@ -876,10 +934,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
         const int4 h = sm.hdr[stage];
         if (h.x < 0) break;
         const int2 bk = sm.seqk[stage];
+        const int2 pc = sm.pce[stage];
         const int w = h.x, tile_idx = h.y, n = h.z, col0 = h.w;
-        const uint32_t row_slot = (uint32_t)w / (uint32_t)ppr;
-        const int piece = w - (int)row_slot * ppr;
-        const int c0 = piece * PE, c1 = min(V, c0 + PE);
+        const int c1 = pc.x, tiles = pc.y;
+        const int c0 = col0 - tile_idx * TE;
         const bool last = col0 + n >= c1;
         // this warp's vectors of the tile into registers; the stage goes straight back
         // this warp's vectors of the tile into registers; the stage goes back once the
@@ -891,10 +949,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
         if (tile_idx == 0) {
             b = bk.x;
             k = bk.y;
-            cs.spec = spec_rank(k, (c1 - c0 + TE - 1) / TE) > 0;
+            cs.spec = spec_rank(k, tiles) > 0;
         }
         const bool ok = consume_tile<TIn>(sm, g, v, reinterpret_cast<const TIn*>(sm.buf[stage]), n, col0,
-                                          tile_idx == 0, last, (c1 - c0 + TE - 1) / TE, k, cs, warp, lane);
+                                          tile_idx == 0, last, tiles, k, cs, warp, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
         if (++stage == kStages) {
