@@ -276,6 +276,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling of smaller cases)")
+    ap.add_argument("--eager", action="store_true", help="time calls issued one by one (no CUDA graph)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -323,13 +324,40 @@ def main():
     torch.cuda.synchronize(dev)
     props = torch.cuda.get_device_properties(dev)
     smi_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    # The timed region replays the K calls from CUDA graphs captured once (up to
+    # 100 calls each, every call with its own seed), as a decode loop issues its
+    # steps: the device time of the library's own kernels, without the Python
+    # binding's per-call host overhead (which bounds small batches when the
+    # calls are issued one by one; that eager figure is reported beside it).
+    graphs = []
+    if not args.eager:
+        left, seed = args.steps, 1_000_000
+        while left > 0:
+            n = min(100, left)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    step(seed + i)
+            graphs.append(g)
+            seed += n
+            left -= n
+        for g in graphs:  # one untimed replay of each graph
+            g.replay()
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
     with ClockSampler(smi_id) as clk:
         wall0 = time.perf_counter()
         # the timed region: K production steps back to back, nothing recorded
         # between the call's kernels (their programmatic dependent launches overlap)
         t0.record(stream)
-        for i in range(args.steps):
-            step(1_000_000 + i)
+        if graphs:
+            for g in graphs:
+                g.replay()
+        else:
+            for i in range(args.steps):
+                step(1_000_000 + i)
         t1.record(stream)
         torch.cuda.synchronize(dev)
         wall1 = time.perf_counter()
@@ -337,6 +365,15 @@ def main():
         dist.barrier()
     ms_total = max_over_ranks(t0.elapsed_time(t1), dev)
     ms_step = ms_total / args.steps
+    # the same K calls issued one by one from Python (host launch overhead included)
+    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    q0.record(stream)
+    for i in range(args.steps):
+        step(2_000_000 + i)
+    q1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_step_eager = max_over_ranks(q0.elapsed_time(q1), dev) / args.steps
     positions = wl.positions()
     value = whole_job_rate(positions, world, ms_step * 1e-3)
 
@@ -396,7 +433,10 @@ def main():
     traffic = recorded_traffic(args.workload, main, args.batch is None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms_step, "ms_per_step_eager": ms_step_eager,
+        "timed_region": ("K calls replayed from CUDA graphs of up to 100 captured calls" if graphs
+                         else "K calls issued one by one"),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic",
         "config": dict(workload_config(args.workload, B),
                        l2="inputs larger than L2: %.0f MB of logits per step vs 129 MB L2" % (bytes_per_launch / 1e6),

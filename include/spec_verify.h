@@ -225,6 +225,41 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, int 
                        int32_t* accepted_len, int32_t* out_tokens, float* alpha, float* p_out, float* q_out,
                        uint32_t* row_status, void* stream);
 
+/*
+ * Shared-noise (Gumbel-coupled) verification ("Speculative decoding: the art of
+ * guessing well", section 共享噪声的采样, the gumbel_verify listing and the
+ * Gumbel-max identity: sampling from softmax(l) is argmax(l + g) with g Gumbel).
+ * The drafter and the target use the same noise g_k at each position k, so the
+ * target's own sample there is t_k = argmax_i(log p_k(i) + g_k,i); the round keeps
+ * the longest prefix of draft tokens equal to t_1, t_2, ..., then emits the target's
+ * token at the first difference (t_{gamma_b+1} when every draft token matched).
+ * The emitted tokens are exactly the target's own samples, whatever the drafter.
+ *
+ * p_k is the target row k normalised as in spec_verify (temperature, top-k, top-p;
+ * log p = -inf outside the kept set); argmax ties go to the lower token id;
+ * temperature 0 is the plain argmax of the logits (no noise).  The noise of token i
+ * at 1-based position k of sequence b is g = -ln(-ln u), u = ((w >> 8) + 1/2) 2^-24,
+ * w = word (i & 3) of Philox4x32-10(counter = (b, k, 2, i >> 2), key = (lo32(seed),
+ * hi32(seed))) -- draw 2, apart from the draws 0 and 1 of spec_verify.  A drafter
+ * sharing the noise proposes argmax_i(log q_k(i) + g_k,i) with the same g.
+ *
+ * target_logits [B, gamma_max+1, V] dtype     (no draft logits are needed)
+ * draft_tokens, num_draft, temperature, top_k, top_p, seed, B, gamma_max, V: as spec_verify
+ * accepted_len  [B] int32 out                 n_b: draft tokens before the first difference
+ * out_tokens    [B, gamma_max+1] int32 out    x_1..x_n, t_{n+1}, then -1
+ * target_tokens [B, gamma_max+1] int32 out or NULL: t_k for k <= gamma_b + 1 (-1 beyond)
+ * row_status    [B] uint32 out or NULL        SV_ROW_* bits (lenience does not apply)
+ * workspace     spec_verify_workspace_size() bytes for the same shape and dtype
+ * options       NULL or sv_options: path, pos_accept (draft k equals t_k), wait_limit_ns
+ *               and the events are honoured; lenience is ignored
+ * Errors and asynchrony as spec_verify.
+ */
+int spec_verify_gumbel(const void* target_logits, int dtype, const int32_t* draft_tokens, const int32_t* num_draft,
+                       const float* temperature, const int32_t* top_k, const float* top_p, uint64_t seed, int B,
+                       int gamma_max, int V, int32_t* accepted_len, int32_t* out_tokens, int32_t* target_tokens,
+                       uint32_t* row_status, void* workspace, size_t workspace_bytes, void* stream,
+                       const sv_options* options);
+
 /* A static English description of a status code. */
 const char* spec_verify_strerror(int status);
 

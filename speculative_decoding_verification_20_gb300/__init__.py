@@ -33,7 +33,7 @@ ROW_BAD_LENIENCE = 0x80
 
 # every symbol include/spec_verify.h declares
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_verify_host",
-            "spec_verify_host_staging_size", "spec_verify_strerror", "spec_verify_static")
+            "spec_verify_host_staging_size", "spec_verify_strerror", "spec_verify_static", "spec_verify_gumbel")
 
 SV_ESCRATCH = -6
 STATIC_SCRATCH_BYTES = 8 << 20  # SV_STATIC_SCRATCH_BYTES
@@ -81,6 +81,9 @@ def load_library():
     lib.spec_verify_host.restype = I
     lib.spec_verify_static.argtypes = [P, P, I, P, P, P, P, P, U64, I, I, I, P, P, P, P, P, P, P]
     lib.spec_verify_static.restype = I
+    lib.spec_verify_gumbel.argtypes = [P, I, P, P, P, P, P, U64, I, I, I, P, P, P, P, P, SZ, P,
+                                       ctypes.POINTER(_Options)]
+    lib.spec_verify_gumbel.restype = I
     lib.spec_verify_strerror.argtypes = [I]
     lib.spec_verify_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -213,6 +216,56 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.T
         res.update(p_out=p_out, q_out=q_out)
     if positions:
         res.update(pos_accept=pa, pos_token=pt)
+    return res
+
+
+def spec_verify_gumbel(target: torch.Tensor, draft_tokens: torch.Tensor, temperature, num_draft=None, top_k=None,
+                       top_p=None, *, seed: int, positions: bool = False, path: str = "auto",
+                       events: Optional[dict] = None, stream=None, workspace: Optional[torch.Tensor] = None,
+                       wait_limit_ns: int = 0) -> dict:
+    """Shared-noise verification of one batch on the GPU: target [B, G+1, V] logits
+    (float32 or bfloat16, CUDA), the drafter's tokens [B, G].  Returns accepted_len [B],
+    out_tokens [B, G+1], target_tokens [B, G+1] (the target's noisy argmax at every
+    position, -1 beyond gamma_b + 1), row_status [B] and, with positions=True,
+    pos_accept [B, G] (draft k equals the target's token k)."""
+    lib = load_library()
+    if not target.is_cuda or target.dim() != 3:
+        raise ValueError("target must be a CUDA tensor [B, G+1, V]")
+    dt = _dtype_code(target)
+    B, G1, V = target.shape
+    G = G1 - 1
+    dev = target.device
+    target = target.contiguous()
+    toks = draft_tokens.to(device=dev, dtype=torch.int32).contiguous()
+    if tuple(toks.shape) != (B, G):
+        raise ValueError("draft_tokens must be [B, G]")
+    T = _dev_vec(temperature, B, torch.float32, dev, "temperature")
+    nd = _dev_vec(num_draft, B, torch.int32, dev, "num_draft")
+    tk = _dev_vec(top_k, B, torch.int32, dev, "top_k")
+    tp = _dev_vec(top_p, B, torch.float32, dev, "top_p")
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty(B, G + 1, dtype=torch.int32, device=dev)
+    tt = torch.empty(B, G + 1, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    pa = torch.empty(B, G, dtype=torch.int32, device=dev) if positions else None
+    need = workspace_size(B, G, V, dt)
+    ws = workspace if workspace is not None else _workspace(need, dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    opts = _Options(ctypes.sizeof(_Options), _ptr(pa), None, SV_PATH_DENSE if path == "dense" else SV_PATH_AUTO)
+    opts.wait_limit_ns = int(wait_limit_ns)
+    for key in ("stream", "dense", "free"):
+        if events and events.get(key):
+            getattr(opts, "ev_" + key)[0] = events[key][0].cuda_event
+            getattr(opts, "ev_" + key)[1] = events[key][1].cuda_event
+    with torch.cuda.device(dev):
+        rc = lib.spec_verify_gumbel(_ptr(target), dt, _ptr(toks), _ptr(nd), _ptr(T), _ptr(tk), _ptr(tp),
+                                    ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF), B, G, V, _ptr(acc), _ptr(out),
+                                    _ptr(tt), _ptr(status), _ptr(ws), ws.numel(), ctypes.c_void_p(s.cuda_stream),
+                                    ctypes.byref(opts))
+    _check(rc)
+    res = dict(accepted_len=acc, out_tokens=out, target_tokens=tt, row_status=status)
+    if positions:
+        res["pos_accept"] = pa
     return res
 
 

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
                 // no top-k: the whole-row kernel (with the nucleus cut when top-p < 1)
                 mode = a.force_dense ? kModeDense : stream ? kModeStream : k == 0 ? kModeFree : kModeDense;
                 if (mode == kModeStream)
-                    nrows = 2 * gamma + 1;
+                    nrows = a.gumbel ? gamma + 1 : 2 * gamma + 1;  // shared noise: target rows only
                 else if (mode == kModeDense)
                     nunits = gamma + 1;
             }
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
             for (uint32_t u = 0; u < nfunits; ++u) a.free_units[base_funits + off_f + u] = ((uint32_t)b << 8) | u;
             const int first_pad = st ? 0 : gamma;
             for (int i = first_pad; i < G; ++i) {
-                a.alpha[(size_t)b * G + i] = 0.0f;
+                if (a.alpha) a.alpha[(size_t)b * G + i] = 0.0f;
                 if (a.pos_accept) a.pos_accept[(size_t)b * G + i] = -1;
             }
             if (a.pos_token)
@@ -218,18 +218,21 @@ extern "C" const char* spec_verify_strerror(int status) {
     }
 }
 
-extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logits, int dtype,
-                              const int32_t* draft_tokens, const int32_t* num_draft, const float* temperature,
-                              const int32_t* top_k, const float* top_p, uint64_t seed, int B, int gamma_max, int V,
-                              int32_t* accepted_len, int32_t* out_tokens, float* alpha, float* p_out, float* q_out,
-                              uint32_t* row_status, void* workspace, size_t workspace_bytes, void* stream,
-                              const sv_options* options) {
+namespace {
+// One call of either verification rule: arguments checked on the host, then the
+// plan and the path kernels enqueued on `stream`.  gumbel: shared-noise
+// verification (target rows only; no draft logits, alpha or probabilities).
+int verify_call(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                const int32_t* num_draft, const float* temperature, const int32_t* top_k, const float* top_p,
+                uint64_t seed, int B, int gamma_max, int V, int32_t* accepted_len, int32_t* out_tokens, float* alpha,
+                float* p_out, float* q_out, uint32_t* row_status, void* workspace, size_t workspace_bytes,
+                void* stream, const sv_options* options, bool gumbel) {
     const int rc = check_shape(B, gamma_max, V, dtype);
     if (rc != SV_OK) return rc;
     if (B == 0) return SV_OK;
-    if (!target_logits || !draft_logits || !draft_tokens || !temperature || !accepted_len || !out_tokens || !alpha)
-        return SV_EINVAL;
-    if (((uintptr_t)target_logits & 15u) || ((uintptr_t)draft_logits & 15u)) return SV_EINVAL;
+    if (!target_logits || !draft_tokens || !temperature || !accepted_len || !out_tokens) return SV_EINVAL;
+    if (!gumbel && (!draft_logits || !alpha)) return SV_EINVAL;
+    if (((uintptr_t)target_logits & 15u) || (!gumbel && ((uintptr_t)draft_logits & 15u))) return SV_EINVAL;
     if (options && options->struct_size < sizeof(uint32_t)) return SV_EINVAL;
     const WsLayout L = ws_layout(B, gamma_max, V, dtype);
     if (!workspace || workspace_bytes < L.total) return SV_EWORKSPACE;
@@ -249,13 +252,13 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
     Args a;
     memset(&a, 0, sizeof a);
     a.target = target_logits;
-    a.draft = draft_logits;
+    a.draft = gumbel ? target_logits : draft_logits;  // never read by the shared-noise rule
     a.draft_tokens = draft_tokens;
     a.num_draft = num_draft;
     a.temperature = temperature;
     a.top_k = top_k;
     a.top_p = top_p;
-    a.lenience = opt.lenience;
+    a.lenience = gumbel ? nullptr : opt.lenience;
     a.seed = seed;
     a.wait_ns = opt.wait_limit_ns ? (unsigned long long)opt.wait_limit_ns : kWaitLimitNs;
     a.B = B;
@@ -263,13 +266,14 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
     a.V = V;
     a.accepted_len = accepted_len;
     a.out_tokens = out_tokens;
-    a.alpha = alpha;
-    a.p_out = p_out;
-    a.q_out = q_out;
+    a.alpha = gumbel ? nullptr : alpha;
+    a.p_out = gumbel ? nullptr : p_out;
+    a.q_out = gumbel ? nullptr : q_out;
     a.row_status = row_status;
     a.pos_accept = opt.pos_accept;
     a.pos_token = opt.pos_token;
     a.force_dense = opt.path == SV_PATH_DENSE;
+    a.gumbel = gumbel ? 1 : 0;
     a.ppr = L.ppr;
     a.seq = (SeqInfo*)(ws + L.seq);
     a.seq_done = (uint32_t*)(ws + L.seq_done);
@@ -288,9 +292,9 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
     a.free_nblk = L.free_nblk;
 
     const size_t es = dtype == SV_BF16 ? 2 : 4;
-    if (p_out && cudaMemsetAsync(p_out, 0, sizeof(float) * (size_t)B * (gamma_max + 1) * V, s) != cudaSuccess)
+    if (a.p_out && cudaMemsetAsync(a.p_out, 0, sizeof(float) * (size_t)B * (gamma_max + 1) * V, s) != cudaSuccess)
         return SV_ECUDA;
-    if (q_out && cudaMemsetAsync(q_out, 0, sizeof(float) * (size_t)B * gamma_max * V, s) != cudaSuccess)
+    if (a.q_out && cudaMemsetAsync(a.q_out, 0, sizeof(float) * (size_t)B * gamma_max * V, s) != cudaSuccess)
         return SV_ECUDA;
     // one CTA of min(1024, B rounded up to a warp) threads: a small batch pays
     // for no idle warps at the plan's block-wide scans
@@ -301,6 +305,37 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
     const bool vector = ((size_t)V * es) % 16 == 0;
     const cudaError_t e = launch_all(dtype, vector, a, di.sms, s, opt);
     return e == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+}  // namespace
+
+extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_tokens, const int32_t* num_draft, const float* temperature,
+                              const int32_t* top_k, const float* top_p, uint64_t seed, int B, int gamma_max, int V,
+                              int32_t* accepted_len, int32_t* out_tokens, float* alpha, float* p_out, float* q_out,
+                              uint32_t* row_status, void* workspace, size_t workspace_bytes, void* stream,
+                              const sv_options* options) {
+    return verify_call(target_logits, draft_logits, dtype, draft_tokens, num_draft, temperature, top_k, top_p, seed,
+                       B, gamma_max, V, accepted_len, out_tokens, alpha, p_out, q_out, row_status, workspace,
+                       workspace_bytes, stream, options, false);
+}
+
+extern "C" int spec_verify_gumbel(const void* target_logits, int dtype, const int32_t* draft_tokens,
+                                  const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+                                  const float* top_p, uint64_t seed, int B, int gamma_max, int V,
+                                  int32_t* accepted_len, int32_t* out_tokens, int32_t* target_tokens,
+                                  uint32_t* row_status, void* workspace, size_t workspace_bytes, void* stream,
+                                  const sv_options* options) {
+    sv_options opt;
+    memset(&opt, 0, sizeof opt);
+    if (options) {
+        if (options->struct_size < sizeof(uint32_t)) return SV_EINVAL;
+        memcpy(&opt, options, options->struct_size < sizeof opt ? options->struct_size : sizeof opt);
+    }
+    opt.struct_size = sizeof opt;
+    if (target_tokens) opt.pos_token = target_tokens;
+    return verify_call(target_logits, nullptr, dtype, draft_tokens, num_draft, temperature, top_k, top_p, seed, B,
+                       gamma_max, V, accepted_len, out_tokens, nullptr, nullptr, nullptr, row_status, workspace,
+                       workspace_bytes, stream, &opt, true);
 }
 
 extern "C" int spec_verify(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,

@@ -340,6 +340,63 @@ __device__ void combine_unit(const Args& a, int b, int unit, const SeqInfo& si, 
     unit_finished_warp(a, b, lane);
 }
 
+// Shared-noise verification of one position ("Speculative decoding: the art
+// of guessing well", section 共享噪声的采样): the target's token is the argmax over
+// the row's kept set of log p(i) + g(i), which for kept tokens is (l_i - l_max) / T
+// + g(i) up to one constant (the renormalisation), with g the Philox noise of
+// token i at this position; ties go to the lower id; T = 0 is the argmax itself.
+// The draft token passes iff it is that token.  One warp, from the sorted kept
+// list of the target row.
+template <typename TIn>
+__device__ void gumbel_unit(const Args& a, int b, int unit, const SeqInfo& si, CombPair& sm, int lane, int x) {
+    const int G = a.G;
+    const bool pair = unit < si.gamma;
+    const int kt = sm.kept[0];
+    if (kt < 0) {
+        if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+        unit_finished_warp(a, b, lane);
+        return;
+    }
+    int token;
+    if (si.T == 0.0f) {
+        token = comp_id(sm.top[0][0]);  // the largest logit, lowest id among equals
+    } else {
+        const float lmax = key_logit<TIn>(comp_key(sm.top[0][0]));
+        const float c = 1.0f / si.T;
+        const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
+        unsigned long long best = 0ull;
+        for (int j = lane; j < kt; j += 32) {
+            if (!(sm.prob[0][j] > 0.0f)) continue;  // past the nucleus cut
+            const unsigned long long e = sm.top[0][j];
+            const uint32_t id = (uint32_t)comp_id(e);
+            const uint4 w = philox4((uint32_t)b, (uint32_t)(unit + 1), 2u, id >> 2, k0, k1);
+            const uint32_t wi = (id & 3u) == 0 ? w.x : (id & 3u) == 1 ? w.y : (id & 3u) == 2 ? w.z : w.w;
+            const float sc = fmaf(key_logit<TIn>(comp_key(e)) - lmax, c, gumbel_of_word(wi));
+            const unsigned long long kk = score_key(sc, id);
+            best = kk > best ? kk : best;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            best = y > best ? y : best;
+        }
+        token = score_key_id(best);
+    }
+    if (lane == 0) {
+        if (pair) {
+            const int acc = (x == token) ? 1 : 0;
+            a.unit_acc[(size_t)b * G + unit] = acc;
+            if (a.pos_accept) a.pos_accept[(size_t)b * G + unit] = acc;
+        }
+        a.unit_tok[(size_t)b * (G + 1) + unit] = token;
+        if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + unit] = token;
+    }
+    if (a.p_out)
+        for (int j = lane; j < kt; j += 32)
+            a.p_out[((size_t)b * (G + 1) + unit) * a.V + comp_id(sm.top[0][j])] = sm.prob[0][j];
+    unit_finished_warp(a, b, lane);
+}
+
 // named barrier of warp pair pr (ids 1 and 2; the ids are constants so the
 // kernel holds only the barriers it uses)
 __device__ __forceinline__ void pair_sync(int pr) {
@@ -378,9 +435,15 @@ __global__ void __launch_bounds__(kCombineThreads, 7) combine_kernel(Args a) {
         }
         // the draft token, loaded early: its latency hides behind the row work
         const int x = (r == 0 && unit < si.gamma) ? a.draft_tokens[(size_t)b * a.G + unit] : 0;
-        if (r == 0 || unit < si.gamma) combine_row<TIn>(a, si, unit, r, sm, lane);
+        // shared-noise verification reads the target rows only
+        if (r == 0 || (unit < si.gamma && !a.gumbel)) combine_row<TIn>(a, si, unit, r, sm, lane);
         pair_sync(pr);
-        if (r == 0) combine_unit<TIn>(a, b, unit, si, sm, lane, x);
+        if (r == 0) {
+            if (a.gumbel)
+                gumbel_unit<TIn>(a, b, unit, si, sm, lane, x);
+            else
+                combine_unit<TIn>(a, b, unit, si, sm, lane, x);
+        }
         pair_sync(pr);  // the rows may be rebuilt
     }
 }

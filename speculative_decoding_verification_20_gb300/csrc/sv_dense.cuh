@@ -451,7 +451,8 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
         const int b = (int)(item >> 8), u = (int)(item & 0xFFu);
         const SeqInfo si = a.seq[b];
         if (failed && si.mode == kModeFree) continue;  // uniform over the cluster: every CTA skips it
-        const bool pair = u < si.gamma;
+        const bool has_draft = u < si.gamma;
+        const bool pair = has_draft && !a.gumbel;  // the draft row is read (not by shared noise)
         const float Lb = si.L;
         const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
         const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
@@ -526,6 +527,65 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
             __syncthreads();
             select_keep<TIn, R>(c, sm, xt, V, true, (double)Pf * St);
             if (pair) select_keep<TIn, R>(c, sm, xd, V, true, (double)Pf * Sd);
+        }
+
+        if (a.gumbel) {
+            // ---- shared noise ("Speculative decoding: the art of guessing well", section
+            // 共享噪声的采样): the target's token is the argmax over the kept tokens of
+            // log p + g; log of the kept weight 2^((x - M) log2(e) / T) is (x - M) / T, the
+            // renormalisation being one constant; ties go to the lower id; greedy: the
+            // one kept token
+            const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
+            float bs = -INFINITY;
+            int bid = 0x7FFFFFFF;
+#pragma unroll
+            for (int l = 0; l < R; ++l) {
+                const int col0 = col_of<TIn, R>(c, l, 0);  // a multiple of 4
+#pragma unroll
+                for (int h = 0; h < C::VEC / 4; ++h) {
+                    uint4 wq = make_uint4(0u, 0u, 0u, 0u);
+                    if (!greedy && col0 + 4 * h < V)
+                        wq = philox4((uint32_t)b, (uint32_t)(u + 1), 2u, (uint32_t)(col0 >> 2) + h, k0, k1);
+                    const uint32_t ws4[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const int j = 4 * h + j4, col = col0 + j;
+                        const float e = xt[l * C::VEC + j];
+                        if (col < V && e > 0.0f) {
+                            const float sc =
+                                greedy ? 0.0f : fmaf(__log2f(e), 0.693147180559945309f, gumbel_of_word(ws4[j4]));
+                            if (sc > bs || (sc == bs && col < bid)) {
+                                bs = sc;
+                                bid = col;
+                            }
+                        }
+                    }
+                }
+            }
+            // over the cluster: the largest score, then the lowest id holding it
+            double v1[1] = {(double)bs};
+            block_max_vec<1>(v1, sm, s_vals);
+            cluster_combine(c, sm, s_vals, 1, true);
+            const float top = (float)sm.res[0];
+            __syncthreads();
+            double v2[1] = {bs == top ? -(double)bid : -INFINITY};
+            block_max_vec<1>(v2, sm, s_vals);
+            cluster_combine(c, sm, s_vals, 1, true);
+            const int token = (int)(-sm.res[0]);
+            __syncthreads();
+            if (c.crank == 0) {
+                if (t == 0) {
+                    if (has_draft) {
+                        const int acc = a.draft_tokens[(size_t)b * G + u] == token ? 1 : 0;
+                        a.unit_acc[(size_t)b * G + u] = acc;
+                        if (a.pos_accept) a.pos_accept[(size_t)b * G + u] = acc;
+                    }
+                    a.unit_tok[(size_t)b * (G + 1) + u] = token;
+                    if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + u] = token;
+                }
+                unit_finished(a, b);
+            }
+            continue;
         }
 
         // ---- normalisers of the kept mass

@@ -42,7 +42,7 @@ __device__ __forceinline__ void finalize_sequence(const Args& a, int b) {
     }
     if (st) {  // a data problem found on the device: the defaults of an invalid sequence
         for (int i = threadIdx.x; i < G; i += blockDim.x) {
-            a.alpha[(size_t)b * G + i] = 0.0f;
+            if (a.alpha) a.alpha[(size_t)b * G + i] = 0.0f;
             if (a.pos_accept) a.pos_accept[(size_t)b * G + i] = -1;
         }
         if (a.pos_token)
@@ -110,7 +110,7 @@ static __device__ __noinline__ void finalize_sequence_warp(const Args& a, int b,
     }
     if (st) {
         for (int i = lane; i < G; i += 32) {
-            a.alpha[(size_t)b * G + i] = 0.0f;
+            if (a.alpha) a.alpha[(size_t)b * G + i] = 0.0f;
             if (a.pos_accept) a.pos_accept[(size_t)b * G + i] = -1;
         }
         if (a.pos_token)

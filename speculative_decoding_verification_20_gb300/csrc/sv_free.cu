@@ -632,12 +632,15 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
                 const uint32_t item = a.free_units[w];
                 const int b = (int)(item >> 8), u = (int)(item & 0xFFu);
                 const SeqInfo si = a.seq[b];
-                const bool pair = u < si.gamma;
+                const bool pair = !a.gumbel && u < si.gamma;  // shared noise reads the target row only
                 const bool nucleus = si.P < 1.0f;
                 const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
                 const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
-                for (int pi = 0; pi < (nucleus ? 5 : 2) && ok; ++pi) {
-                    const int pass = nucleus ? pi : (pi == 0 ? 0 : kPassFinal);
+                // passes: the statistics (not needed by shared noise without top-p), the
+                // nucleus passes when top-p < 1, the final pass
+                const int npass = nucleus ? 5 : (a.gumbel ? 1 : 2);
+                for (int pi = 0; pi < npass && ok; ++pi) {
+                    const int pass = nucleus ? pi : (pi + 1 == npass ? kPassFinal : 0);
                     for (int tile = 0; tile < ntiles && ok; ++tile) {
                         const int col = tile * TS, n = min(TS, V - col);
                         if (!fbar_wait(&sm.empty[stage], ph, sm.wait_ns)) {
@@ -695,7 +698,9 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
     FSync g{0u, true};
     const int vbase = warp * (32 * kFVec) + lane;  // this thread's vectors of a segment: vbase + 32 i
     const size_t nblk = (size_t)a.free_nblk;
-    int b = 0, u = 0, par = 1;
+    int b = 0, u = 0, par = 1, cur_w = -1;
+    float cg = 1.0f;                // 1 / T (shared noise: the score is l / T + g)
+    unsigned long long gbest = 0ull;  // shared noise: this thread's best (score, id) key of the unit
     bool pair = false, nf = false, dead = false;
     bool nuc = false, fall = false;  // top-p < 1; the unit goes to the cluster kernel
     float c = 1.0f, Pf = 1.0f, invl = 1.0f;  // invl: 1 / lenience (alpha = sum_x min(q, p * invl))
@@ -725,13 +730,17 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
         if (h.x < 0) break;
         const int w = h.x, pass = h.y, tile = h.z, n = h.w;
         const int col = tile * TS;
-        if (pass == 0 && tile == 0) {  // a new unit (from the producer's header: no global loads)
+        if (w != cur_w) {  // a new unit (from the producer's header: no global loads)
+            cur_w = w;
             const int4 uh = sm.uhdr[stage];  // read before the stage is released
             b = uh.x >> 8;
             u = uh.x & 0xFF;
-            pair = u < uh.y;
+            pair = !a.gumbel && u < uh.y;
             const float T = __int_as_float(uh.z);
             c = 1.4426950408889634f / T;
+            cg = 1.0f / T;
+            gbest = 0ull;
+            dead = false;
             Pf = __int_as_float(uh.w);
             invl = lenience_inv(sm.lhdr[stage]);
             nuc = Pf < 1.0f;
@@ -908,6 +917,56 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
         }
         if (fall || dead) continue;  // nothing more to sum (the cluster kernel, or the tail kernel's flags)
 
+        if (a.gumbel) {
+            // ---- shared noise ("Speculative decoding: the art of guessing well", section
+            // 共享噪声的采样): the target's token is the argmax over the kept tokens of
+            // l / T + g, g the Philox noise of the token at this position (ties: lower id)
+            const float lcp = key_value32((uint32_t)(cutp >> 32));
+            const uint32_t icp = ~(uint32_t)cutp;
+            const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
+#pragma unroll
+            for (int i = 0; i < kFVec; ++i) {
+                const int e0 = (vbase + 32 * i) * F::VEC;
+                const int valid = min(F::VEC, n - e0);
+                if (valid <= 0) continue;
+                float x[F::VEC];
+                F::unpack(vp[i], x);
+                const uint32_t id0 = (uint32_t)(col + e0);  // a multiple of 4
+#pragma unroll
+                for (int h = 0; h < F::VEC / 4; ++h) {
+                    const uint4 wq = philox4((uint32_t)b, (uint32_t)(u + 1), 2u, (id0 >> 2) + h, k0, k1);
+                    const uint32_t ws4[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const int j = 4 * h + j4;
+                        if (j >= valid) continue;
+                        const float xv = x[j];
+                        const uint32_t id = id0 + (uint32_t)j;
+                        nf |= (xv != xv) || xv == INFINITY;
+                        if (!(xv > -INFINITY)) continue;  // p = 0 (and NaN)
+                        if (nuc && !kept_at(xv, id, lcp, icp)) continue;
+                        const unsigned long long kk = score_key(fmaf(xv, cg, gumbel_of_word(ws4[j4])), id);
+                        gbest = kk > gbest ? kk : gbest;
+                    }
+                }
+            }
+            if (tile == ntiles - 1) {
+                unsigned long long bk = gbest;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
+                    bk = y > bk ? y : bk;
+                }
+                const bool wnf = __any_sync(0xFFFFFFFFu, nf);
+                if (lane == 0) {  // this warp's best key: high word (0xFFFFFFFF: a NaN or +inf seen), id
+                    float* rrow = a.free_blk + (size_t)w * 2 * nblk;
+                    rrow[warp] = __uint_as_float(wnf ? 0xFFFFFFFFu : (uint32_t)(bk >> 32));
+                    rrow[nblk + warp] = __uint_as_float((uint32_t)score_key_id(bk));
+                }
+            }
+            continue;
+        }
+
         // ---- final pass: alpha and the residual weights, summed per block
         float tr = 0.0f, tp = 0.0f;
         // the per-element work, specialised on whether the rows are filtered (one
@@ -1069,10 +1128,41 @@ __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
             continue;
         }
         const FreeRec* rec = a.free_rec + w;
-        const uint32_t flags = rec->flags;
+        // (shared noise without top-p: no statistics pass, so no record was written)
+        const uint32_t flags = (a.gumbel && !(si.P < 1.0f)) ? 0u : rec->flags;
         if (flags & kRecFall) continue;  // the cluster kernel finishes this unit
         if (flags & kRecDead) {
             if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+            unit_finished_warp(a, b, lane);
+            continue;
+        }
+        if (a.gumbel) {
+            // the target's token: the best of the warps' (score, id) keys
+            const float* rrow = a.free_blk + (size_t)w * 2 * nblk;
+            const uint32_t hi = lane < a.free_warps ? __float_as_uint(rrow[lane]) : 0u;
+            const uint32_t id = lane < a.free_warps ? __float_as_uint(rrow[nblk + lane]) : 0u;
+            const bool bad = __any_sync(0xFFFFFFFFu, hi == 0xFFFFFFFFu);
+            unsigned long long bk = hi ? (((unsigned long long)hi << 32) | (unsigned long long)(~id)) : 0ull;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
+                bk = y > bk ? y : bk;
+            }
+            if (bad || bk == 0ull) {  // a NaN or +inf logit, or no finite one
+                if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+                unit_finished_warp(a, b, lane);
+                continue;
+            }
+            const int token = score_key_id(bk);
+            if (lane == 0) {
+                if (pair) {
+                    const int acc = a.draft_tokens[(size_t)b * G + u] == token ? 1 : 0;
+                    a.unit_acc[(size_t)b * G + u] = acc;
+                    if (a.pos_accept) a.pos_accept[(size_t)b * G + u] = acc;
+                }
+                a.unit_tok[(size_t)b * (G + 1) + u] = token;
+                if (a.pos_token) a.pos_token[(size_t)b * (G + 1) + u] = token;
+            }
             unit_finished_warp(a, b, lane);
             continue;
         }
@@ -1226,6 +1316,7 @@ cudaError_t launch_free_w(const Args& a0, int sms, cudaStream_t s, void* const e
     }();
     Args a = a0;
     a.free_nblk = free_blocks(a.V, sizeof(TIn) == 2 ? SV_BF16 : SV_F32, W);  // the record stride of this variant
+    a.free_warps = W;
     const long long units = (long long)a.B * (a.G + 1);
     long long grid = (long long)occ * sms;
     if (grid > units) grid = units;

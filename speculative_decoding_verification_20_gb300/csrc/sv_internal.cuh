@@ -120,6 +120,7 @@ struct Args {
     int32_t* pos_accept;
     int32_t* pos_token;
     int force_dense;
+    int gumbel;  // shared-noise verification: target rows only, accept iff x = argmax(log p + g)
     int ppr;  // stream pieces per row
     // workspace
     SeqInfo* seq;
@@ -137,6 +138,7 @@ struct Args {
     FreeRec* free_rec;        // [units] by free list index
     float* free_blk;          // [units][2][free_nblk]: per block sums of r (residual weights) and p
     int free_nblk;            // blocks per row of the free kernel's variant (set by its launcher)
+    int free_warps;           // consumer warps of that variant (set by its launcher)
 };
 
 struct WsLayout {
@@ -229,6 +231,55 @@ __device__ __forceinline__ float lenience_inv(float L) { return L > 0.0f ? 1.0f 
 // Acceptance mass of one token, q(x) P(accept | x) = min(q(x), p(x) / L); with
 // L = 1 it is min(p(x), q(x)) bit for bit.
 __device__ __forceinline__ float accept_mass(float p, float q, float invl) { return fminf(q, p * invl); }
+
+// All four output words of the same block function.
+__device__ __forceinline__ uint4 philox4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                         uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t a_lo = 0xD2511F53u * c0, a_hi = __umulhi(0xD2511F53u, c0);
+        const uint32_t b_lo = 0xCD9E8D57u * c2, b_hi = __umulhi(0xCD9E8D57u, c2);
+        c0 = b_hi ^ c1 ^ k0;
+        c1 = b_lo;
+        c2 = a_hi ^ c3 ^ k1;
+        c3 = a_lo;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
+// Gumbel noise g = -ln(-ln u) of a uniform u = ((w >> 8) + 1/2) 2^-24 given by its
+// Philox word w ("Speculative decoding: the art of guessing well", section
+// 共享噪声的采样: sampling from softmax(l) is argmax(l + g)).  In fp32 with
+// every input exact: for u < 1/2, u itself is exact and -ln u = -log2(u) ln 2
+// (relative error about 2^-22); for u >= 1/2, 1 - u = (2 (2^24 - a) - 1) 2^-25 is
+// exact and -ln u = -log1p(-(1 - u)) to about an ulp.  Then g = -log2(L) ln 2:
+// an absolute error of a few 1e-6 at most (at the largest g), far below the
+// 1e-4 gap by which decisions are compared with the fp64 oracle.
+__device__ __forceinline__ float gumbel_of_word(uint32_t w) {
+    const uint32_t a = w >> 8;
+    float L;
+    if (a < (1u << 23)) {
+        const float u = ((float)a + 0.5f) * 5.9604644775390625e-8f;  // (a + 1/2) 2^-24, exact
+        L = -__log2f(u) * 0.693147180559945309f;
+    } else {
+        const float y = (float)(2u * ((1u << 24) - a) - 1u) * 2.98023223876953125e-8f;  // 1 - u, exact
+        L = -log1pf(-y);
+    }
+    return -__log2f(L) * 0.693147180559945309f;
+}
+
+// (score, token id) as one 64-bit key whose maximum is the largest score and,
+// among equal scores, the lowest id: the argmax rule of the shared-noise test.
+// A NaN score never wins (it maps below -inf).
+__device__ __forceinline__ unsigned long long score_key(float s, uint32_t id) {
+    const uint32_t bits = __float_as_uint(s);
+    uint32_t k = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+    if (s != s) k = 0u;
+    return ((unsigned long long)k << 32) | (unsigned long long)(~id);
+}
+__device__ __forceinline__ int score_key_id(unsigned long long k) { return (int)(~(uint32_t)k); }
 
 // U(seed, b, pos, draw) = ((w >> 8) + 0.5) * 2^-24 (exact in double)
 __device__ __forceinline__ double uniform01(uint64_t seed, uint32_t b, uint32_t pos, uint32_t draw) {

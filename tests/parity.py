@@ -193,3 +193,56 @@ def compare_probs(gpu: dict, ora, gammas, rep: ParityReport, inputs: dict | None
                 continue
             rep.prob_err = max(rep.prob_err, err)
     return rep
+
+
+# ---------------------------------------------------------------------------
+# shared-noise (Gumbel-coupled) verification
+# ---------------------------------------------------------------------------
+# The kernel scores a kept token as l / T + g in fp32 (g = -ln(-ln u) from fast
+# base-2 logarithms, an absolute error of a few 1e-6 at most at the largest g;
+# l / T rounded once), against the oracle's fp64 log p + g: two scores can swap
+# only when the oracle's gap between the best and the second best is within
+# about 1e-5.  Positions whose oracle gap is below GUMBEL_MARGIN = 1e-4 are
+# low-margin: a mismatch there is excused and counted against the same budget.
+GUMBEL_MARGIN = 1e-4
+
+
+def compare_gumbel(gpu: dict, ora, draft_tokens, gammas, rep: ParityReport | None = None) -> ParityReport:
+    """gpu: spec_verify_gumbel(..., positions=True) outputs; ora: oracle.gumbel_verify result."""
+    rep = rep or ParityReport()
+    acc, out = to_np(gpu["accepted_len"]), to_np(gpu["out_tokens"])
+    tt, st = to_np(gpu["target_tokens"]), to_np(gpu["row_status"]).astype(np.uint32)
+    x = to_np(draft_tokens)
+    G = x.shape[1]
+    for b in range(acc.shape[0]):
+        if st[b] != ora.status[b]:
+            rep.hard.append(("status", b, int(st[b]), int(ora.status[b])))
+            continue
+        if ora.status[b]:
+            if acc[b] != 0 or (out[b] != -1).any():
+                rep.hard.append(("invalid-row-outputs", b))
+            continue
+        g = int(gammas[b])
+        for k in range(g + 1):
+            rep.decisions += 1
+            low = ora.margin[b, k] < GUMBEL_MARGIN
+            rep.low_margin += int(low)
+            if tt[b, k] != ora.target_tokens[b, k]:
+                if low:
+                    rep.excused += 1
+                else:
+                    rep.hard.append(("token", b, k, int(tt[b, k]), int(ora.target_tokens[b, k]),
+                                     float(ora.margin[b, k])))
+        if (tt[b, g + 1:] != -1).any():
+            rep.hard.append(("padding", b))
+        # the round follows from the kernel's own tokens: the longest matching prefix, then t_{n+1}
+        n = 0
+        while n < g and x[b, n] == tt[b, n]:
+            n += 1
+        want = list(x[b, :n]) + [tt[b, n]] + [-1] * (G - n)
+        if acc[b] != n or list(out[b]) != want:
+            rep.hard.append(("round", b, int(acc[b]), n))
+        if (acc[b] != ora.accepted_len[b] or (out[b] != ora.out_tokens[b]).any()) and \
+                (tt[b, :g + 1] == ora.target_tokens[b, :g + 1]).all():
+            rep.hard.append(("round-vs-oracle", b))
+    return rep
