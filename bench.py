@@ -63,6 +63,28 @@ def kernel_hash(path: str = "stream") -> str:
     return h.hexdigest()[:16]
 
 
+# Issue peak of the SMs for an ALU-bound kernel: 152 SMs x 4 schedulers x one
+# 32-thread instruction per cycle at the 2070 MHz maximum SM clock.
+ALU_PEAK_TINST = 152 * 4 * 32 * 2.070e9 / 1e12
+
+
+def recorded_instructions(rule: str, workload: str, path: str, default_batch: bool):
+    """Thread instructions per launch of the dominant kernel (ncu
+    smsp__thread_inst_executed.sum), from profiles/instructions.json; None for
+    another batch size or kernel, or once its sources changed."""
+    p = os.path.join(ROOT, "profiles", "instructions.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(f"{rule}:{workload}")
+    except Exception:
+        return None
+    if not default_batch or not rec or rec.get("path") != path or path not in KERNEL_SOURCES:
+        return None
+    if rec.get("kernel_hash") != kernel_hash(path):
+        return None
+    return rec.get("thread_inst_per_launch")
+
+
 def recorded_traffic(workload: str, path: str, default_batch: bool):
     """DRAM bytes per launch of the dominant kernel at the workload's full size,
     from the committed ncu summary; None for another batch size, another
@@ -141,7 +163,8 @@ def _cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def _oracle_rate(workload: str, threads: int, budget_s: float, seed0: int, max_batches: int = 256):
+def _oracle_rate(workload: str, threads: int, budget_s: float, seed0: int, max_batches: int = 256,
+                 rule: str = "sampling"):
     """Positions per second of the fp64 oracle on whole sequences of the workload
     recipe, `threads` sequences at a time on `threads` host threads (rows are
     independent; the oracle is C called through ctypes, which releases the
@@ -155,8 +178,12 @@ def _oracle_rate(workload: str, threads: int, budget_s: float, seed0: int, max_b
 
     def one(ni, b, seed):
         row = lambda x: None if x is None else x[b:b + 1]
-        oracle.verify(row(ni["target"]), row(ni["draft"]), row(ni["draft_tokens"]), row(ni["temperature"]),
-                      row(ni["num_draft"]), row(ni["top_k"]), row(ni["top_p"]), seed=seed)
+        if rule == "gumbel":
+            oracle.gumbel_verify(row(ni["target"]), row(ni["draft_tokens"]), row(ni["temperature"]),
+                                 row(ni["num_draft"]), row(ni["top_k"]), row(ni["top_p"]), seed=seed)
+        else:
+            oracle.verify(row(ni["target"]), row(ni["draft"]), row(ni["draft_tokens"]), row(ni["temperature"]),
+                          row(ni["num_draft"]), row(ni["top_k"]), row(ni["top_p"]), seed=seed)
 
     elapsed, positions, batches = 0.0, 0, 0
     with ThreadPoolExecutor(threads) as ex:
@@ -171,13 +198,13 @@ def _oracle_rate(workload: str, threads: int, budget_s: float, seed0: int, max_b
     return positions / elapsed, batches * threads, positions, elapsed
 
 
-def cpu_baseline(workload: str, budget_s: float = 10.0):
+def cpu_baseline(workload: str, budget_s: float = 10.0, rule: str = "sampling"):
     """The fp64 oracle, as it stands, on this host: one thread per core (rows are
     independent) and single-threaded, each on a bounded sample of whole
     sequences of the same workload recipe."""
     cores = os.cpu_count() or 1
-    v1, n1, p1, e1 = _oracle_rate(workload, 1, budget_s, 10_000)
-    vn, nn, pn, en = _oracle_rate(workload, cores, budget_s, 50_000)
+    v1, n1, p1, e1 = _oracle_rate(workload, 1, budget_s, 10_000, rule=rule)
+    vn, nn, pn, en = _oracle_rate(workload, cores, budget_s, 50_000, rule=rule)
     return {"value": vn, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": _cpu_model(),
             "single_thread_value": v1,
             "sample": f"{nn} whole sequences of the {workload} recipe ({pn} positions, {en:.1f} s wall on {cores} "
@@ -193,7 +220,7 @@ def run_reference(args):
     times, positions = [], 0
     for step in range(args.warmup + args.steps):
         # each step: `cores` whole sequences of the workload, one per host thread
-        v, n, pos, el = _oracle_rate(args.workload, cores, 0.0, 20_000 + step, max_batches=1)
+        v, n, pos, el = _oracle_rate(args.workload, cores, 0.0, 20_000 + step, max_batches=1, rule=args.rule)
         if step >= args.warmup:
             times.append(el)
             positions += pos
@@ -235,10 +262,12 @@ def rank_seed(rank: int) -> int:
     return rank
 
 
-def bytes_by_path(wl, stream_max_k: int) -> dict:
+def bytes_by_path(wl, stream_max_k: int, rule: str = "sampling") -> dict:
     """Algorithmic logit bytes each path of the library reads for this batch:
     greedy or 1 <= top_k <= stream_max_k rows stream (select kernel); rows with
-    no top-k the whole-row kernel (free); larger top-k the cluster kernel."""
+    no top-k the whole-row kernel (free); larger top-k the cluster kernel.  The
+    sampling rule reads 2 gamma_b + 1 rows per sequence, shared noise the
+    gamma_b + 1 target rows only."""
     import numpy as np
 
     gam = wl.gammas()
@@ -248,7 +277,7 @@ def bytes_by_path(wl, stream_max_k: int) -> dict:
     stream = (T == 0) | ((k >= 1) & (k <= stream_max_k))
     free = ~stream & (k == 0)
     es = 2 if wl.dtype == "bf16" else 4
-    rowb = (2 * gam + 1) * wl.V * es
+    rowb = ((gam + 1) if rule == "gumbel" else (2 * gam + 1)) * wl.V * es
     return {"stream": int(rowb[stream].sum()), "free": int(rowb[free].sum()),
             "dense": int(rowb[~stream & ~free].sum())}
 
@@ -266,6 +295,92 @@ def workload_config(name: str, B: int | None = None) -> dict:
             "B": c["B"], "gamma": c["G"], "V": c["V"], "logits": c["dtype"]}
 
 
+def run_kseq(args, sv, workloads, world, rank, dev):
+    """K-SEQ: one position per row with k candidates; the cluster kernel holds each
+    row's target and draft on chip while it finds rho*.  Positions = rows."""
+    import torch
+    import torch.distributed as dist
+
+    wl = workloads.make_kseq(args.workload, seed=rank_seed(rank), device=dev, B=args.batch)
+    B, K, V = wl.B, wl.K, wl.V
+    dt = sv.SV_BF16 if wl.dtype == "bf16" else sv.SV_F32
+    ws = torch.empty(max(int(sv.load_library().spec_verify_kseq_workspace_size(B, K, V, dt)), 256), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(seed, events=None):
+        return sv.spec_verify_kseq(wl.target, wl.draft, wl.candidates, wl.temperature, wl.num_candidates, wl.top_k,
+                                   wl.top_p, seed=seed, workspace=ws, events=events)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    graphs = []
+    left, seed = args.steps, 1_000_000
+    while left > 0 and not args.eager:
+        n = min(100, left)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                step(seed + i)
+        graphs.append(g)
+        seed += n
+        left -= n
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    props = torch.cuda.get_device_properties(dev)
+    smi_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(int(os.environ.get("LOCAL_RANK", "0")))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(smi_id) as clk:
+        wall0 = time.perf_counter()
+        t0.record(stream)
+        if graphs:
+            for g in graphs:
+                g.replay()
+        else:
+            for i in range(args.steps):
+                step(1_000_000 + i)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall1 = time.perf_counter()
+    ms_step = max_over_ranks(t0.elapsed_time(t1), dev) / args.steps
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in kev:
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        step(3_000_000 + i, events={"dense": kev[i]})
+    torch.cuda.synchronize(dev)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    peak, peak_kind = measured_peak()
+    nbytes = wl.logit_bytes()
+    value = whole_job_rate(wl.positions(), world, ms_step * 1e-3)
+    if rank != 0:
+        return 0
+    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "timed_region": ("K calls replayed from CUDA graphs of up to 100 captured calls"
+                                                 if graphs else "K calls issued one by one"),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": f"{args.workload}: B={B} rows (one position each), K={K} candidates, V={V}, "
+                               f"{wl.dtype} logits", "rule": "kseq", "B": B, "K": K, "V": V, "logits": wl.dtype,
+                   "l2": "%.0f MB of logits per step vs 129 MB L2" % (nbytes / 1e6)},
+        "hbm_gbs_step": nbytes / (ms_step * 1e-3) / 1e9, "hbm_frac_step": nbytes / (ms_step * 1e-3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "kernel": "dense_kernel (cluster path, K-SEQ)", "kernel_ms": kernel_ms,
+                     "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+        "e2e": None, "gpu_launches": LAUNCHES_PER_STEP * args.steps, "clocks": clk.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -277,6 +392,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling of smaller cases)")
     ap.add_argument("--eager", action="store_true", help="time calls issued one by one (no CUDA graph)")
+    ap.add_argument("--rule", default="sampling", choices=["sampling", "gumbel", "kseq"],
+                    help="verification rule: speculative sampling (spec_verify), shared noise "
+                         "(spec_verify_gumbel) or K-SEQ candidates at one position (spec_verify_kseq; "
+                         "workloads kseq32k, kseq128k)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -301,6 +420,8 @@ def main():
         dist.barrier()
     sv.load_library()
 
+    if args.rule == "kseq":
+        return run_kseq(args, sv, workloads, world, rank, dev)
     wl = workloads.make(args.workload, seed=rank_seed(rank), device=dev, B=args.batch)
     B, G, V = wl.B, wl.G, wl.V
     stream = torch.cuda.current_stream(dev)
@@ -308,6 +429,9 @@ def main():
                      device=dev)
 
     def step(seed, events=None):
+        if args.rule == "gumbel":
+            return sv.spec_verify_gumbel(wl.target, wl.draft_tokens, wl.temperature, wl.num_draft, wl.top_k,
+                                         wl.top_p, seed=seed, workspace=ws, events=events)
         return sv.spec_verify(wl.target, wl.draft, wl.draft_tokens, wl.temperature, wl.num_draft, wl.top_k, wl.top_p,
                               seed=seed, workspace=ws, events=events)
 
@@ -316,7 +440,7 @@ def main():
     torch.cuda.synchronize(dev)
 
     # the dominant kernel: the path that reads the most logits
-    path_bytes = bytes_by_path(wl, sv.SV_STREAM_MAX_TOP_K)
+    path_bytes = bytes_by_path(wl, sv.SV_STREAM_MAX_TOP_K, args.rule)
     main = max(path_bytes, key=path_bytes.get)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -395,14 +519,43 @@ def main():
     ms_step_with_events = e0.elapsed_time(e1) / args.steps
     kernel_ms = [a.elapsed_time(b) for a, b in kev]
     kernel_ms_avg = sum(kernel_ms) / len(kernel_ms)
-    bytes_per_launch = wl.logit_bytes()
+    bytes_per_launch = sum(path_bytes.values())
     main_bytes = path_bytes[main]
     achieved = main_bytes / (kernel_ms_avg * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
 
     # end to end through the host-buffer entry point: pinned inputs in, results out, every step
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and args.rule == "gumbel":
+        # end to end through the Python API: pinned inputs copied in, results copied out
+        pin = lambda x: None if x is None else x.detach().cpu().contiguous().pin_memory()
+        h = [pin(x) for x in (wl.target, wl.draft_tokens, wl.temperature, wl.num_draft, wl.top_k, wl.top_p)]
+        dbuf = [None if x is None else torch.empty_like(x, device=dev) for x in h]
+        hout = [torch.empty(B, dtype=torch.int32).pin_memory(), torch.empty(B, G + 1, dtype=torch.int32).pin_memory()]
+
+        def e2e_step(seed):
+            for d, x in zip(dbuf, h):
+                if x is not None:
+                    d.copy_(x, non_blocking=True)
+            r = sv.spec_verify_gumbel(dbuf[0], dbuf[1], dbuf[2], dbuf[3], dbuf[4], dbuf[5], seed=seed, workspace=ws)
+            hout[0].copy_(r["accepted_len"], non_blocking=True)
+            hout[1].copy_(r["out_tokens"], non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+
+        for i in range(3):
+            e2e_step(i)
+        if world > 1:
+            dist.barrier()
+        w0 = time.perf_counter()
+        for i in range(args.e2e_steps):
+            e2e_step(2_000_000 + i)
+        w1 = time.perf_counter()
+        e_step = max_over_ranks(w1 - w0, dev) / args.e2e_steps
+        e2e = {"value": whole_job_rate(positions, world, e_step), "unit": UNIT,
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in h if x is not None),
+               "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in hout), "steps": args.e2e_steps,
+               "ms_per_step": e_step * 1e3}
+    elif args.e2e_steps > 0:
         pin = lambda x: None if x is None else x.detach().cpu().contiguous().pin_memory()
         h = [pin(x) for x in (wl.target, wl.draft, wl.draft_tokens, wl.temperature, wl.num_draft, wl.top_k,
                                wl.top_p)]
@@ -430,7 +583,30 @@ def main():
             dist.destroy_process_group()
         return 0
     clocks = clk.summary(wall0, wall1)
-    traffic = recorded_traffic(args.workload, main, args.batch is None)
+    traffic = recorded_traffic(args.workload, main, args.batch is None) if args.rule == "sampling" else None
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "kernel": {"stream": "select_kernel (streaming top-k path)",
+                           "free": "free_kernel (whole-row path: rows without top-k)",
+                           "dense": "dense_kernel (cluster path)"}[main],
+                "kernel_ms": kernel_ms_avg, "algorithmic_bytes_per_launch": main_bytes,
+                "traffic": traffic,
+                "timing": "kernel events in a separate run of K steps "
+                          f"({ms_step_with_events:.4f} ms per step with the events recorded)"}
+    if args.rule == "gumbel" and main == "free":
+        # shared noise on rows without top-k: a Philox block per 4 tokens and two logarithms
+        # per token make the whole-row kernel issue-bound, not HBM-bound
+        inst = recorded_instructions(args.rule, args.workload, main, args.batch is None)
+        hbm = dict(roofline)
+        roofline = {"bound": "alu", "unit": "T thread-inst/s", "peak": ALU_PEAK_TINST,
+                    "peak_source": "152 SMs x 4 schedulers x 32 threads x 2070 MHz (one instruction per scheduler "
+                                   "per cycle)",
+                    "achieved": None if inst is None else inst / (kernel_ms_avg * 1e-3) / 1e12,
+                    "thread_inst_per_launch": inst, "kernel": hbm["kernel"], "kernel_ms": kernel_ms_avg,
+                    "hbm": {"achieved_gbs": achieved, "frac": achieved / peak, "peak": peak}, "traffic": None,
+                    "timing": hbm["timing"]}
+        roofline["frac"] = None if inst is None else roofline["achieved"] / ALU_PEAK_TINST
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "ms_per_step_eager": ms_step_eager,
@@ -438,27 +614,18 @@ def main():
                          else "K calls issued one by one"),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic",
-        "config": dict(workload_config(args.workload, B),
+        "config": dict(workload_config(args.workload, B), rule=args.rule,
                        l2="inputs larger than L2: %.0f MB of logits per step vs 129 MB L2" % (bytes_per_launch / 1e6),
                        parallelism=f"replicas x{world} (independent batches per GPU)"),
         "hbm_gbs_step": bytes_per_launch / (ms_step * 1e-3) / 1e9,
         "hbm_frac_step": bytes_per_launch / (ms_step * 1e-3) / 1e9 / peak,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                     else "fallback 6.8 TB/s",
-                     "kernel": {"stream": "select_kernel (streaming top-k path)",
-                                "free": "free_kernel (whole-row path: rows without top-k)",
-                                "dense": "dense_kernel (cluster path)"}[main],
-                     "kernel_ms": kernel_ms_avg, "algorithmic_bytes_per_launch": main_bytes,
-                     "traffic": traffic,
-                     "timing": "kernel events in a separate run of K steps "
-                               f"({ms_step_with_events:.4f} ms per step with the events recorded)"},
+        "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.workload)
+        line["cpu_baseline"] = cpu_baseline(args.workload, rule=args.rule)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

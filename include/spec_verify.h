@@ -78,6 +78,7 @@ typedef enum {
 #define SV_MAX_GAMMA 32
 #define SV_MAX_VOCAB 262144
 #define SV_MAX_BATCH 16777216
+#define SV_MAX_KSEQ 13 /* candidates per row of spec_verify_kseq */
 
 /*
  * Bytes of device workspace one call needs for this shape (a pure host
@@ -259,6 +260,41 @@ int spec_verify_gumbel(const void* target_logits, int dtype, const int32_t* draf
                        int gamma_max, int V, int32_t* accepted_len, int32_t* out_tokens, int32_t* target_tokens,
                        uint32_t* row_status, void* workspace, size_t workspace_bytes, void* stream,
                        const sv_options* options);
+
+/*
+ * K-SEQ multi-candidate verification of one position per row ("SpecTr: Fast
+ * Speculative Decoding via Optimal Transport" page, section K-SEQ, eqs. (4)-(7)
+ * and the residual distribution; that page names the draft p and the target q,
+ * here p is the target and q the draft).  Row b holds k_b candidates X_i drawn
+ * independently from the drafter's q.  With beta(rho) = sum_x min(q(x), p(x)/rho)
+ * and rho* the root in [1, k] of 1 - (1 - beta)^k = rho beta, candidate i (in the
+ * given order) is accepted iff u_i rho* q(X_i) < p(X_i); the first accepted one is
+ * emitted; if none is, a token is drawn from the residual p - A with
+ * A(x) = (P_A / beta) min(q(x), p(x)/rho*), P_A = 1 - (1 - beta)^k, by the inverse
+ * CDF in ascending token id (no residual mass: from p itself).  The output law is
+ * exactly p.  Uniforms: u_i = U(seed, b, 1, 3 + i), the residual's U(seed, b, 1, 1)
+ * (U as for spec_verify).  p and q are normalised as in spec_verify.
+ *
+ * target_logits  [B, V] dtype, draft_logits [B, V] dtype
+ * candidates     [B, K] int32 in [0, V); entries past k_b are ignored
+ * num_candidates [B] int32 k_b in [1, K], or NULL = all K (K <= SV_MAX_KSEQ)
+ * temperature, top_k, top_p: as spec_verify
+ * out_token      [B] int32 out: the emitted token (-1 for an invalid row)
+ * accepted       [B] int32 out: the index of the accepted candidate, or -1 (residual)
+ * row_status     [B] uint32 out or NULL: SV_ROW_* bits (SV_ROW_BAD_NUM_DRAFT for k_b,
+ *                SV_ROW_BAD_DRAFT_TOKEN for a candidate outside [0, V))
+ * workspace      spec_verify_kseq_workspace_size() bytes
+ * options        NULL or sv_options: ev_dense (the events around the cluster kernel) and
+ *                wait_limit_ns are honoured; the rest is ignored
+ * Each row is one unit of the cluster kernel (the rows are held on chip while
+ * rho* is found).  Errors and asynchrony as spec_verify.
+ */
+size_t spec_verify_kseq_workspace_size(int B, int K, int V, int dtype);
+int spec_verify_kseq(const void* target_logits, const void* draft_logits, int dtype, const int32_t* candidates,
+                     const int32_t* num_candidates, const float* temperature, const int32_t* top_k,
+                     const float* top_p, uint64_t seed, int B, int K, int V, int32_t* out_token, int32_t* accepted,
+                     uint32_t* row_status, void* workspace, size_t workspace_bytes, void* stream,
+                     const sv_options* options);
 
 /* A static English description of a status code. */
 const char* spec_verify_strerror(int status);

@@ -33,7 +33,9 @@ ROW_BAD_LENIENCE = 0x80
 
 # every symbol include/spec_verify.h declares
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_verify_host",
-            "spec_verify_host_staging_size", "spec_verify_strerror", "spec_verify_static", "spec_verify_gumbel")
+            "spec_verify_host_staging_size", "spec_verify_strerror", "spec_verify_static", "spec_verify_gumbel",
+            "spec_verify_kseq", "spec_verify_kseq_workspace_size")
+SV_MAX_KSEQ = 13
 
 SV_ESCRATCH = -6
 STATIC_SCRATCH_BYTES = 8 << 20  # SV_STATIC_SCRATCH_BYTES
@@ -84,6 +86,11 @@ def load_library():
     lib.spec_verify_gumbel.argtypes = [P, I, P, P, P, P, P, U64, I, I, I, P, P, P, P, P, SZ, P,
                                        ctypes.POINTER(_Options)]
     lib.spec_verify_gumbel.restype = I
+    lib.spec_verify_kseq_workspace_size.argtypes = [I, I, I, I]
+    lib.spec_verify_kseq_workspace_size.restype = SZ
+    lib.spec_verify_kseq.argtypes = [P, P, I, P, P, P, P, P, U64, I, I, I, P, P, P, P, SZ, P,
+                                     ctypes.POINTER(_Options)]
+    lib.spec_verify_kseq.restype = I
     lib.spec_verify_strerror.argtypes = [I]
     lib.spec_verify_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -267,6 +274,49 @@ def spec_verify_gumbel(target: torch.Tensor, draft_tokens: torch.Tensor, tempera
     if positions:
         res["pos_accept"] = pa
     return res
+
+
+def spec_verify_kseq(target: torch.Tensor, draft: torch.Tensor, candidates: torch.Tensor, temperature,
+                     num_candidates=None, top_k=None, top_p=None, *, seed: int, stream=None,
+                     workspace: Optional[torch.Tensor] = None, events: Optional[dict] = None) -> dict:
+    """K-SEQ verification of one position per row on the GPU: target and draft logits
+    [B, V] (float32 or bfloat16, CUDA), k candidates per row [B, K] (K <= 13).  Returns
+    out_token [B], accepted [B] (the accepted candidate's index, -1: the residual draw)
+    and row_status [B]."""
+    lib = load_library()
+    if not (target.is_cuda and draft.is_cuda) or target.dim() != 2 or tuple(draft.shape) != tuple(target.shape):
+        raise ValueError("target and draft must be CUDA tensors [B, V] of one shape")
+    dt = _dtype_code(target)
+    if _dtype_code(draft) != dt:
+        raise TypeError("target and draft dtypes differ")
+    B, V = target.shape
+    dev = target.device
+    target, draft = target.contiguous(), draft.contiguous()
+    cand = candidates.to(device=dev, dtype=torch.int32).contiguous()
+    if cand.dim() != 2 or cand.shape[0] != B:
+        raise ValueError("candidates must be [B, K]")
+    K = cand.shape[1]
+    T = _dev_vec(temperature, B, torch.float32, dev, "temperature")
+    nc = _dev_vec(num_candidates, B, torch.int32, dev, "num_candidates")
+    tk = _dev_vec(top_k, B, torch.int32, dev, "top_k")
+    tp = _dev_vec(top_p, B, torch.float32, dev, "top_p")
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    need = int(lib.spec_verify_kseq_workspace_size(B, K, V, dt))
+    ws = workspace if workspace is not None else _workspace(max(need, 256), dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    opts = _Options(ctypes.sizeof(_Options), None, None, SV_PATH_DENSE)
+    if events and events.get("dense"):  # (begin, end) torch.cuda.Event around the cluster kernel
+        opts.ev_dense[0] = events["dense"][0].cuda_event
+        opts.ev_dense[1] = events["dense"][1].cuda_event
+    with torch.cuda.device(dev):
+        rc = lib.spec_verify_kseq(_ptr(target), _ptr(draft), dt, _ptr(cand), _ptr(nc), _ptr(T), _ptr(tk), _ptr(tp),
+                                  ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF), B, K, V, _ptr(tok), _ptr(acc),
+                                  _ptr(status), _ptr(ws), ws.numel(), ctypes.c_void_p(s.cuda_stream),
+                                  ctypes.byref(opts))
+    _check(rc)
+    return dict(out_token=tok, accepted=acc, row_status=status)
 
 
 def spec_verify_host(target, draft, draft_tokens, temperature, num_draft=None, top_k=None, top_p=None, *,

@@ -88,10 +88,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
                 const bool stream = (k >= 1 && k <= kStreamMaxK);
                 // no top-k: the whole-row kernel (with the nucleus cut when top-p < 1)
                 mode = a.force_dense ? kModeDense : stream ? kModeStream : k == 0 ? kModeFree : kModeDense;
+                if (a.kseq) mode = kModeDense;  // K-SEQ: one unit per row, held by a cluster
                 if (mode == kModeStream)
                     nrows = a.gumbel ? gamma + 1 : 2 * gamma + 1;  // shared noise: target rows only
                 else if (mode == kModeDense)
-                    nunits = gamma + 1;
+                    nunits = a.kseq ? 1 : gamma + 1;
             }
         }
         const uint32_t nsunits = (mode == kModeStream) ? (uint32_t)(gamma + 1) : 0u;
@@ -118,17 +119,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
             for (uint32_t u = 0; u < nunits; ++u) a.dense_units[base_units + off_u + u] = ((uint32_t)b << 8) | u;
             for (uint32_t u = 0; u < nsunits; ++u) a.stream_units[base_sunits + off_s + u] = ((uint32_t)b << 8) | u;
             for (uint32_t u = 0; u < nfunits; ++u) a.free_units[base_funits + off_f + u] = ((uint32_t)b << 8) | u;
-            const int first_pad = st ? 0 : gamma;
-            for (int i = first_pad; i < G; ++i) {
-                if (a.alpha) a.alpha[(size_t)b * G + i] = 0.0f;
-                if (a.pos_accept) a.pos_accept[(size_t)b * G + i] = -1;
-            }
-            if (a.pos_token)
-                for (int j = st ? 0 : gamma + 1; j <= G; ++j) a.pos_token[(size_t)b * (G + 1) + j] = -1;
-            if (st) {
-                a.accepted_len[b] = 0;
-                for (int j = 0; j <= G; ++j) a.out_tokens[(size_t)b * (G + 1) + j] = -1;
-                if (a.row_status) a.row_status[b] = st;
+            if (a.kseq) {  // outputs [B]: the token and the accepted candidate's index
+                if (st) {
+                    a.accepted_len[b] = -1;
+                    a.out_tokens[b] = -1;
+                    if (a.row_status) a.row_status[b] = st;
+                }
+            } else {
+                const int first_pad = st ? 0 : gamma;
+                for (int i = first_pad; i < G; ++i) {
+                    if (a.alpha) a.alpha[(size_t)b * G + i] = 0.0f;
+                    if (a.pos_accept) a.pos_accept[(size_t)b * G + i] = -1;
+                }
+                if (a.pos_token)
+                    for (int j = st ? 0 : gamma + 1; j <= G; ++j) a.pos_token[(size_t)b * (G + 1) + j] = -1;
+                if (st) {
+                    a.accepted_len[b] = 0;
+                    for (int j = 0; j <= G; ++j) a.out_tokens[(size_t)b * (G + 1) + j] = -1;
+                    if (a.row_status) a.row_status[b] = st;
+                }
             }
         }
         base_rows += tot_r;
@@ -226,15 +235,17 @@ int verify_call(const void* target_logits, const void* draft_logits, int dtype, 
                 const int32_t* num_draft, const float* temperature, const int32_t* top_k, const float* top_p,
                 uint64_t seed, int B, int gamma_max, int V, int32_t* accepted_len, int32_t* out_tokens, float* alpha,
                 float* p_out, float* q_out, uint32_t* row_status, void* workspace, size_t workspace_bytes,
-                void* stream, const sv_options* options, bool gumbel) {
+                void* stream, const sv_options* options, bool gumbel, bool kseq = false) {
     const int rc = check_shape(B, gamma_max, V, dtype);
     if (rc != SV_OK) return rc;
+    if (kseq && gamma_max > SV_MAX_KSEQ) return SV_ETOO_LARGE;
     if (B == 0) return SV_OK;
     if (!target_logits || !draft_tokens || !temperature || !accepted_len || !out_tokens) return SV_EINVAL;
     if (!gumbel && (!draft_logits || !alpha)) return SV_EINVAL;
     if (((uintptr_t)target_logits & 15u) || (!gumbel && ((uintptr_t)draft_logits & 15u))) return SV_EINVAL;
     if (options && options->struct_size < sizeof(uint32_t)) return SV_EINVAL;
-    const WsLayout L = ws_layout(B, gamma_max, V, dtype);
+    // K-SEQ rows are single positions: the workspace of one draft position per row
+    const WsLayout L = kseq ? ws_layout(B, 1, V, dtype) : ws_layout(B, gamma_max, V, dtype);
     if (!workspace || workspace_bytes < L.total) return SV_EWORKSPACE;
     if ((uintptr_t)workspace & 255u) return SV_EINVAL;
 
@@ -266,7 +277,7 @@ int verify_call(const void* target_logits, const void* draft_logits, int dtype, 
     a.V = V;
     a.accepted_len = accepted_len;
     a.out_tokens = out_tokens;
-    a.alpha = gumbel ? nullptr : alpha;
+    a.alpha = (gumbel || kseq) ? nullptr : alpha;
     a.p_out = gumbel ? nullptr : p_out;
     a.q_out = gumbel ? nullptr : q_out;
     a.row_status = row_status;
@@ -274,6 +285,7 @@ int verify_call(const void* target_logits, const void* draft_logits, int dtype, 
     a.pos_token = opt.pos_token;
     a.force_dense = opt.path == SV_PATH_DENSE;
     a.gumbel = gumbel ? 1 : 0;
+    a.kseq = kseq ? 1 : 0;
     a.ppr = L.ppr;
     a.seq = (SeqInfo*)(ws + L.seq);
     a.seq_done = (uint32_t*)(ws + L.seq_done);
@@ -317,6 +329,35 @@ extern "C" int spec_verify_ex(const void* target_logits, const void* draft_logit
     return verify_call(target_logits, draft_logits, dtype, draft_tokens, num_draft, temperature, top_k, top_p, seed,
                        B, gamma_max, V, accepted_len, out_tokens, alpha, p_out, q_out, row_status, workspace,
                        workspace_bytes, stream, options, false);
+}
+
+extern "C" size_t spec_verify_kseq_workspace_size(int B, int K, int V, int dtype) {
+    if (check_shape(B, 1, V, dtype) != SV_OK || K < 1 || K > SV_MAX_KSEQ) return 0;
+    return ws_layout(B, 1, V, dtype).total;
+}
+
+extern "C" int spec_verify_kseq(const void* target_logits, const void* draft_logits, int dtype,
+                                const int32_t* candidates, const int32_t* num_candidates, const float* temperature,
+                                const int32_t* top_k, const float* top_p, uint64_t seed, int B, int K, int V,
+                                int32_t* out_token, int32_t* accepted, uint32_t* row_status, void* workspace,
+                                size_t workspace_bytes, void* stream, const sv_options* options) {
+    if (K < 1) return SV_EINVAL;
+    if (K > SV_MAX_KSEQ) return SV_ETOO_LARGE;
+    float dummy_alpha = 0.0f;  // satisfies the sampling rule's argument check; K-SEQ writes no alpha
+    sv_options opt;
+    memset(&opt, 0, sizeof opt);
+    if (options) {
+        if (options->struct_size < sizeof(uint32_t)) return SV_EINVAL;
+        memcpy(&opt, options, options->struct_size < sizeof opt ? options->struct_size : sizeof opt);
+    }
+    opt.struct_size = sizeof opt;
+    opt.path = SV_PATH_DENSE;
+    opt.pos_accept = nullptr;
+    opt.pos_token = nullptr;
+    opt.lenience = nullptr;
+    return verify_call(target_logits, draft_logits, dtype, candidates, num_candidates, temperature, top_k, top_p, seed,
+                       B, K, V, accepted, out_token, &dummy_alpha, nullptr, nullptr, row_status, workspace,
+                       workspace_bytes, stream, &opt, false, true);
 }
 
 extern "C" int spec_verify_gumbel(const void* target_logits, int dtype, const int32_t* draft_tokens,

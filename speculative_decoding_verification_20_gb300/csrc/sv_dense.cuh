@@ -25,10 +25,11 @@ namespace cg = cooperative_groups;
 
 namespace sv {
 
-constexpr int kXch = 24;  // doubles per exchange slot
+constexpr int kXch = 32;  // doubles per exchange slot
 
 struct DenseSmem {
     float hist[16][kDenseThreads];  // per-thread histogram columns
+    float hist2[16][kDenseThreads]; // a second mass per bin (K-SEQ: the target's p beside the draft's q)
     double red[kDenseThreads / 32][kXch];
     double xch[2][kXch];
     double res[2 * kXch];
@@ -428,6 +429,204 @@ __device__ __forceinline__ void load_row(const TIn* row, const Ctx& c, int V, fl
     }
 }
 
+// K-SEQ verification of one position with k candidates ("SpecTr: Fast
+// Speculative Decoding via Optimal Transport" page, section K-SEQ, eqs. (4)-(7)
+// and the residual distribution; the page names the draft p and the target q,
+// here p is the target and q the draft).  p, q: the unit's normalised rows held
+// by this cluster.  With m(x) = min(q(x), p(x) / rho) and beta(rho) = sum_x m(x):
+//   rho* solves 1 - (1 - beta)^k = rho beta on [1, k] (the left side minus the right,
+//     f, does not increase with rho);
+//   candidate i (in the given order) is accepted iff u_i rho* q(X_i) < p(X_i);
+//   if none is, the token is drawn from p - A, A = (P_A / beta) m(x) at rho*,
+//     P_A = 1 - (1 - beta)^k, by the inverse CDF in ascending token id.
+// rho*: beta(rho) = Q(rho) + P(rho) / rho with Q the draft mass of the tokens whose
+// ratio r = p / q is at least rho and P the target mass of the others (tokens with
+// p = 0 or q = 0 add nothing).  A radix descent over the float bits of rho finds the
+// largest float rho_lo with f(rho_lo) > 0, four bits per round, f being evaluated
+// in fp64 at the 16 digit boundaries from a cluster histogram of the q and p mass
+// of the ratio keys in the current range; inside (rho_lo, next float) no ratio
+// lies, so Q and P are constants there and f = 0 is solved by fp64 bisection.
+template <typename TIn, int R>
+__device__ void kseq_unit(const Args& a, Ctx& c, DenseSmem& sm, double* s_vals, const float (&p)[DenseCfg<TIn, R>::EPR],
+                          const float (&q)[DenseCfg<TIn, R>::EPR], int b, int k, int V) {
+    using C = DenseCfg<TIn, R>;
+    const int t = threadIdx.x;
+    const double kd = (double)k;
+    auto fval = [&](double rho, double Q, double P) -> double {  // f at rho for fixed Q, P
+        const double beta = Q + (P > 0.0 ? P / rho : 0.0);
+        double pw = 1.0;  // (1 - beta)^k, k <= 13: repeated products
+        for (int i = 0; i < k; ++i) pw *= (1.0 - beta);
+        return 1.0 - pw - rho * beta;
+    };
+    // ---- the radix descent
+    uint32_t prefix = 0u;
+    double Qhi = 0.0, Plo = 0.0;  // q mass of ratio keys above the current range, p mass below it
+    __shared__ int s_sel;
+    __shared__ double s_q[16], s_p[16];
+    for (int d = 7; d >= 0; --d) {
+        const int sh = 4 * d;
+#pragma unroll
+        for (int bin = 0; bin < 16; ++bin) {
+            sm.hist[bin][t] = 0.0f;
+            sm.hist2[bin][t] = 0.0f;
+        }
+#pragma unroll
+        for (int l = 0; l < R; ++l)
+#pragma unroll
+            for (int j = 0; j < C::VEC; ++j) {
+                const int i = l * C::VEC + j;
+                if (col_of<TIn, R>(c, l, j) < V && p[i] > 0.0f && q[i] > 0.0f) {
+                    const uint32_t key = __float_as_uint(p[i] / q[i]);
+                    if (d == 7 || (key >> (sh + 4)) == (prefix >> (sh + 4))) {
+                        sm.hist[(key >> sh) & 15u][t] += q[i];
+                        sm.hist2[(key >> sh) & 15u][t] += p[i];
+                    }
+                }
+            }
+        __syncthreads();
+        {  // block sums of the 32 (bin, mass) columns: 8 threads per column
+            const int col = t & 31, part = t >> 5;
+            const float* h = (col < 16) ? &sm.hist[col][0] : &sm.hist2[col - 16][0];
+            double sum = 0.0;
+#pragma unroll 4
+            for (int i = 0; i < kDenseThreads / 8; ++i) sum += (double)h[part * (kDenseThreads / 8) + i];
+            sm.red[part][col] = sum;
+        }
+        __syncthreads();
+        if (t < 32) {
+            double sum = 0.0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) sum += sm.red[w][t];
+            s_vals[t] = sum;
+        }
+        __syncthreads();
+        cluster_combine(c, sm, s_vals, 32, false);
+        if (t < 16) {
+            s_q[t] = sm.res[t];
+            s_p[t] = sm.res[16 + t];
+        }
+        __syncthreads();
+        if (t < 32) {
+            // digit t of this round: is f > 0 at the start of its range?  (rho < 1: yes,
+            // f(1) >= 0 and rho* >= 1; rho > k: no; sign-bit keys are not ratios)
+            bool pos = false;
+            if (t < 16 && !(d == 7 && t >= 8)) {
+                const float rho_f = __uint_as_float(prefix | ((uint32_t)t << sh));
+                const double rho = (double)rho_f;
+                if (rho < 1.0) {
+                    pos = true;
+                } else if (rho <= kd) {
+                    double Q = Qhi, P = Plo;
+                    for (int j = 0; j < 16; ++j) {
+                        if (j >= t) Q += s_q[j];
+                        else P += s_p[j];
+                    }
+                    pos = fval(rho, Q, P) > 0.0;
+                }
+            }
+            const unsigned m = __ballot_sync(0xFFFFFFFFu, pos);
+            if (t == 0) s_sel = m ? 31 - __clz(m) : 0;  // f does not increase: the largest such digit
+        }
+        __syncthreads();
+        const int sel = s_sel;
+#pragma unroll 1
+        for (int j = 0; j < 16; ++j) {
+            if (j > sel) Qhi += s_q[j];
+            if (j < sel) Plo += s_p[j];
+        }
+        prefix |= (uint32_t)sel << sh;
+        __syncthreads();
+    }
+    // the ratios equal to rho_lo are below every rho in (rho_lo, next float)
+    const double Q = Qhi, P = Plo + s_p[prefix & 15u];
+    __shared__ double s_rho, s_beta;
+    __shared__ int s_tok, s_idx;
+    if (t == 0) {
+        double lo = fmax(1.0, (double)__uint_as_float(prefix));
+        double hi = fmin(kd, (double)__uint_as_float(prefix + 1u));
+        if (!(lo < hi)) lo = hi;
+        for (int it = 0; it < 200 && hi - lo > 1e-15 * hi; ++it) {
+            const double mid = 0.5 * (lo + hi);
+            if (fval(mid, Q, P) > 0.0)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        s_rho = hi;
+        s_beta = Q + (P > 0.0 ? P / hi : 0.0);
+    }
+    __syncthreads();
+    const double rho = s_rho, beta = s_beta;
+    // ---- the candidates' probabilities: each column is held by one thread of the
+    // cluster, which writes them to its CTA's slots; the cluster sum collects them
+    __shared__ int s_cand[SV_MAX_KSEQ];
+    if (t < SV_MAX_KSEQ) s_cand[t] = t < k ? a.draft_tokens[(size_t)b * a.G + t] : -1;
+    if (t < 2 * SV_MAX_KSEQ) s_vals[t] = 0.0;
+    __syncthreads();
+#pragma unroll
+    for (int l = 0; l < R; ++l)
+#pragma unroll
+        for (int j = 0; j < C::VEC; ++j) {
+            const int col = col_of<TIn, R>(c, l, j);
+            if (col >= V) continue;
+            for (int i = 0; i < k; ++i)
+                if (s_cand[i] == col) {
+                    s_vals[2 * i] = (double)p[l * C::VEC + j];
+                    s_vals[2 * i + 1] = (double)q[l * C::VEC + j];
+                }
+        }
+    __syncthreads();
+    cluster_combine(c, sm, s_vals, 2 * SV_MAX_KSEQ, false);
+    if (t == 0) {
+        int idx = -1;
+        for (int i = 0; i < k && idx < 0; ++i) {
+            const double u = uniform01(a.seed, (uint32_t)b, 1u, 3u + (uint32_t)i);
+            if (u * rho * sm.res[2 * i + 1] < sm.res[2 * i]) idx = i;
+        }
+        s_idx = idx;
+        s_tok = idx >= 0 ? s_cand[idx] : -1;
+    }
+    __syncthreads();
+    int token = s_tok;
+    const int idx = s_idx;
+    if (idx < 0) {
+        // ---- the residual p - A at rho*, by the inverse CDF in ascending id
+        const double PA = beta > 0.0 ? 1.0 - [&] {
+            double pw = 1.0;
+            for (int i = 0; i < k; ++i) pw *= (1.0 - beta);
+            return pw;
+        }() : 0.0;
+        const float As = beta > 0.0 ? (float)(PA / beta) : 0.0f;
+        const float inv_rho = (float)(1.0 / rho);
+        auto resid = [&](int l, int j) -> float {
+            const int i = l * C::VEC + j;
+            return fmaxf(p[i] - As * fminf(q[i], p[i] * inv_rho), 0.0f);
+        };
+        float rs = 0.0f;
+#pragma unroll
+        for (int l = 0; l < R; ++l)
+#pragma unroll
+            for (int j = 0; j < C::VEC; ++j) rs += resid(l, j);
+        double z1[1] = {(double)rs};
+        block_sum_vec<1>(z1, sm, s_vals);
+        cluster_combine(c, sm, s_vals, 1, false);
+        const double Z = sm.res[0];
+        __syncthreads();
+        const double ur = uniform01(a.seed, (uint32_t)b, 1u, 1u);
+        double cum;
+        if (Z > 0.0)
+            token = ordered_search<TIn, R>(c, sm, resid, ur, true, true, &cum);
+        else  // no residual mass (P_A = 1 up to rounding): fall back to p
+            token = ordered_search<TIn, R>(
+                c, sm, [&](int l, int j) -> float { return p[l * C::VEC + j]; }, ur, true, true, &cum);
+    }
+    if (c.crank == 0 && t == 0) {
+        a.out_tokens[b] = token;
+        a.accepted_len[b] = idx;
+        if (a.row_status) a.row_status[b] = 0u;
+    }
+}
+
 template <typename TIn, int R, bool VECTOR>
 __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
     using C = DenseCfg<TIn, R>;
@@ -454,8 +653,9 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
         const bool has_draft = u < si.gamma;
         const bool pair = has_draft && !a.gumbel;  // the draft row is read (not by shared noise)
         const float Lb = si.L;
-        const TIn* trow = (const TIn*)a.target + ((size_t)b * (G + 1) + u) * (size_t)V;
-        const TIn* drow = (const TIn*)a.draft + ((size_t)b * G + u) * (size_t)V;
+        // K-SEQ rows are [B, V] (one position per row); otherwise target [B, G+1, V], draft [B, G, V]
+        const TIn* trow = (const TIn*)a.target + (a.kseq ? (size_t)b : (size_t)b * (G + 1) + u) * (size_t)V;
+        const TIn* drow = (const TIn*)a.draft + (a.kseq ? (size_t)b : (size_t)b * G + u) * (size_t)V;
 
         float xt[C::EPR], xd[C::EPR];
         bool bad = false;
@@ -484,8 +684,16 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
         __syncthreads();
         if (nonfinite) {
             if (c.crank == 0) {
-                if (t == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
-                unit_finished(a, b);
+                if (a.kseq) {
+                    if (t == 0) {
+                        a.out_tokens[b] = -1;
+                        a.accepted_len[b] = -1;
+                        if (a.row_status) a.row_status[b] = SV_ROW_NONFINITE;
+                    }
+                } else {
+                    if (t == 0) atomicOr(&a.seq_status[b], SV_ROW_NONFINITE);
+                    unit_finished(a, b);
+                }
             }
             continue;
         }
@@ -626,6 +834,11 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
                         if (a.q_out && pair) a.q_out[((size_t)b * G + u) * V + col] = xd[l * C::VEC + j];
                     }
                 }
+        }
+
+        if (a.kseq) {
+            kseq_unit<TIn, R>(a, c, sm, s_vals, xt, xd, b, si.gamma, V);
+            continue;
         }
 
         // ---- alpha, acceptance gather; the residual weights replace q in place

@@ -701,6 +701,7 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
     int b = 0, u = 0, par = 1, cur_w = -1;
     float cg = 1.0f;                // 1 / T (shared noise: the score is l / T + g)
     unsigned long long gbest = 0ull;  // shared noise: this thread's best (score, id) key of the unit
+    float gbs = -INFINITY;            // and its score
     bool pair = false, nf = false, dead = false;
     bool nuc = false, fall = false;  // top-p < 1; the unit goes to the cluster kernel
     float c = 1.0f, Pf = 1.0f, invl = 1.0f;  // invl: 1 / lenience (alpha = sum_x min(q, p * invl))
@@ -740,6 +741,7 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
             c = 1.4426950408889634f / T;
             cg = 1.0f / T;
             gbest = 0ull;
+            gbs = -INFINITY;
             dead = false;
             Pf = __int_as_float(uh.w);
             invl = lenience_inv(sm.lhdr[stage]);
@@ -921,9 +923,27 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
             // ---- shared noise ("Speculative decoding: the art of guessing well", section
             // 共享噪声的采样): the target's token is the argmax over the kept tokens of
             // l / T + g, g the Philox noise of the token at this position (ties: lower id)
+            // The thread's Philox blocks of this tile first, in straight-line code (the
+            // independent 10-round chains interleave); then each token: it beats the
+            // thread's best only if g(u) >= D = best - l / T, i.e. u >= U(D) =
+            // exp(-exp(-D)) (g increases with u), and no noise on the 24-bit grid exceeds
+            // g(1 - 2^-25) = 25 ln 2 = 17.33 (kGMax adds a margin).  U is formed with fast
+            // base-2 exponentials (error below 1e-6); tokens with u below U - 1e-5 are
+            // rejected without their exact noise.  Exact: a rejected token scores strictly
+            // below the thread's best.
+            constexpr float kGMax = 17.5f;
+            constexpr int NB = kFVec * F::VEC / 4;  // Philox blocks per thread per tile
             const float lcp = key_value32((uint32_t)(cutp >> 32));
             const uint32_t icp = ~(uint32_t)cutp;
             const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
+            uint4 wq[NB];
+#pragma unroll
+            for (int i = 0; i < kFVec; ++i)
+#pragma unroll
+                for (int h = 0; h < F::VEC / 4; ++h) {
+                    const uint32_t id0 = (uint32_t)(col + (vbase + 32 * i) * F::VEC);  // a multiple of 4
+                    wq[i * (F::VEC / 4) + h] = philox4((uint32_t)b, (uint32_t)(u + 1), 2u, (id0 >> 2) + h, k0, k1);
+                }
 #pragma unroll
             for (int i = 0; i < kFVec; ++i) {
                 const int e0 = (vbase + 32 * i) * F::VEC;
@@ -931,22 +951,27 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
                 if (valid <= 0) continue;
                 float x[F::VEC];
                 F::unpack(vp[i], x);
-                const uint32_t id0 = (uint32_t)(col + e0);  // a multiple of 4
+                const uint32_t id0 = (uint32_t)(col + e0);
 #pragma unroll
-                for (int h = 0; h < F::VEC / 4; ++h) {
-                    const uint4 wq = philox4((uint32_t)b, (uint32_t)(u + 1), 2u, (id0 >> 2) + h, k0, k1);
-                    const uint32_t ws4[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-                    for (int j4 = 0; j4 < 4; ++j4) {
-                        const int j = 4 * h + j4;
-                        if (j >= valid) continue;
-                        const float xv = x[j];
-                        const uint32_t id = id0 + (uint32_t)j;
-                        nf |= (xv != xv) || xv == INFINITY;
-                        if (!(xv > -INFINITY)) continue;  // p = 0 (and NaN)
-                        if (nuc && !kept_at(xv, id, lcp, icp)) continue;
-                        const unsigned long long kk = score_key(fmaf(xv, cg, gumbel_of_word(ws4[j4])), id);
-                        gbest = kk > gbest ? kk : gbest;
+                for (int j = 0; j < F::VEC; ++j) {
+                    if (j >= valid) continue;
+                    const uint4 w4 = wq[i * (F::VEC / 4) + j / 4];
+                    const uint32_t wj = (j & 3) == 0 ? w4.x : (j & 3) == 1 ? w4.y : (j & 3) == 2 ? w4.z : w4.w;
+                    const float xv = x[j];
+                    const uint32_t id = id0 + (uint32_t)j;
+                    nf |= (xv != xv) || xv == INFINITY;
+                    if (!(xv > -INFINITY)) continue;  // p = 0 (and NaN)
+                    if (nuc && !kept_at(xv, id, lcp, icp)) continue;
+                    const float s0 = xv * cg;
+                    const float D = gbs - s0;
+                    if (!(D < kGMax)) continue;
+                    const float uf = fmaf((float)(wj >> 8), 5.9604644775390625e-8f, 2.98023223876953125e-8f);
+                    if (uf < fex2(-fex2(-D * 1.44269504088896341f) * 1.44269504088896341f) - 1e-5f) continue;
+                    const float sc = s0 + gumbel_of_word(wj);
+                    const unsigned long long kk = score_key(sc, id);
+                    if (kk > gbest) {
+                        gbest = kk;
+                        gbs = sc;
                     }
                 }
             }

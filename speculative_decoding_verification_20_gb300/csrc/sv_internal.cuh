@@ -121,6 +121,7 @@ struct Args {
     int32_t* pos_token;
     int force_dense;
     int gumbel;  // shared-noise verification: target rows only, accept iff x = argmax(log p + g)
+    int kseq;    // K-SEQ: one position per row ([B, V] rows), draft_tokens = the k candidates
     int ppr;  // stream pieces per row
     // workspace
     SeqInfo* seq;

@@ -205,3 +205,77 @@ def make(name: str, seed: int = 0, device="cpu", *, B: Optional[int] = None, G: 
                     draft=draft.contiguous(), draft_tokens=tokens.contiguous(), num_draft=num_draft,
                     temperature=T.contiguous(), top_k=top_k, top_p=top_p,
                     seed=int(seed if verify_seed is None else verify_seed))
+
+
+# ---------------------------------------------------------------------------
+# K-SEQ (several candidates at one position per row)
+# ---------------------------------------------------------------------------
+KSEQ_CONFIGS = {
+    # one decode position per row, k candidates drawn independently from the drafter
+    "kseq32k": dict(B=256, K=4, V=32000, dtype="bf16"),   # v32k's rows, T = 0.8, no filter
+    "kseq128k": dict(B=64, K=8, V=128256, dtype="bf16"),  # v128k's rows, T = 1, top-k 50, top-p 0.9
+}
+
+
+@dataclass
+class KseqWorkload:
+    name: str
+    B: int
+    K: int
+    V: int
+    dtype: str
+    target: torch.Tensor        # [B, V]
+    draft: torch.Tensor         # [B, V]
+    candidates: torch.Tensor    # int32 [B, K]: i.i.d. draws from the drafter's filtered q
+    num_candidates: Optional[torch.Tensor]  # int32 [B] or None (all K)
+    temperature: torch.Tensor
+    top_k: Optional[torch.Tensor]
+    top_p: Optional[torch.Tensor]
+    seed: int
+
+    def numpy_inputs(self) -> dict:
+        def logits(t):
+            t = t.detach().cpu().contiguous()
+            if t.dtype == torch.bfloat16:
+                return t.view(torch.int16).numpy().view(np.uint16)
+            return t.numpy()
+        g = lambda t: None if t is None else t.detach().cpu().numpy()
+        return dict(target=logits(self.target), draft=logits(self.draft), candidates=g(self.candidates),
+                    num_candidates=g(self.num_candidates), temperature=g(self.temperature), top_k=g(self.top_k),
+                    top_p=g(self.top_p))
+
+    def positions(self) -> int:
+        """Verified positions per call: one per row."""
+        return self.B
+
+    def logit_bytes(self) -> int:
+        return 2 * self.B * self.V * (2 if self.dtype == "bf16" else 4)
+
+
+def make_kseq(name: str, seed: int = 0, device="cpu", *, B: Optional[int] = None, K: Optional[int] = None,
+              V: Optional[int] = None) -> KseqWorkload:
+    """A K-SEQ batch: the target and draft rows of one position per row (the v32k or
+    v128k recipe) and K candidates per row, each an independent draw of the drafter."""
+    cfg = dict(KSEQ_CONFIGS[name])
+    B = cfg["B"] if B is None else B
+    K = cfg["K"] if K is None else K
+    V = cfg["V"] if V is None else V
+    device = torch.device(device)
+    g = _gen(seed, sum(map(ord, name)), device)
+    top_k = top_p = None
+    if name == "kseq32k":
+        target = _boosted_normal(B, V, g, device)
+        sigma, T = 1.0, torch.full((B,), 0.8, device=device)
+    else:
+        target = _zipf_logits(B, V, g, device)
+        sigma, T = 0.8, torch.ones(B, device=device)
+        top_k = torch.full((B,), 50, dtype=torch.int32, device=device)
+        top_p = torch.full((B,), 0.9, dtype=torch.float32, device=device)
+    draft = target + torch.randn(B, V, generator=g, device=device) * sigma
+    if cfg["dtype"] == "bf16":
+        target, draft = target.to(torch.bfloat16), draft.to(torch.bfloat16)
+    T = T.to(torch.float32)
+    # K independent proposals of the drafter: its row repeated K times, fresh noise each
+    cand = _propose(draft.unsqueeze(1).expand(B, K, V), T, top_k, top_p, g)
+    return KseqWorkload(name, B, K, V, cfg["dtype"], target.contiguous(), draft.contiguous(), cand.contiguous(), None,
+                        T.contiguous(), top_k, top_p, int(seed))

@@ -1,0 +1,198 @@
+"""K-SEQ multi-candidate verification on the GPU against the fp64 oracle ("SpecTr:
+Fast Speculative Decoding via Optimal Transport" page, section K-SEQ, eqs. (4)-(7)
+and the residual distribution; p = target, q = draft here).
+
+Through the C ABI (spec_verify_kseq).  The emitted token and the accepted
+candidate's index must equal the oracle's (svr_kseq_verify), except when a
+decision the oracle takes is within 1e-6 of its boundary: a candidate test
+|u_i - p(X_i) / (rho* q(X_i))|, the residual draw's distance to a CDF edge
+(relative to its mass), or a filter boundary of either row.  Those margins come
+from the oracle's own primitives (normalise, kseq_rho, kseq_direct, uniform).
+The page's counterexample (draft always A, target uniform on {A, B}, k = 2:
+the naive rule emits A with probability 3/4, K-SEQ with exactly 1/2) and the
+output law (= p, chi-square) are reproduced on the GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity import MARGIN, ParityReport, assert_ok, to_np
+
+pytestmark = pytest.mark.gpu
+
+sv = pytest.importorskip("speculative_decoding_verification_20_gb300")
+from speculative_decoding_verification_20_gb300 import workloads  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_verification_20_gb300 import _build
+
+    _build.build()
+    oracle.build()
+
+
+def _as_f32(a):
+    return (a.astype(np.uint32) << 16).view(np.float32) if a.dtype == np.uint16 else a
+
+
+def _row_margins(ni, b, seed, k):
+    """(list of (decision, margin)) of the oracle's K-SEQ step on row b."""
+    T = float(ni["temperature"][b])
+    tk = 0 if ni["top_k"] is None else int(ni["top_k"][b])
+    tp = 1.0 if ni["top_p"] is None else float(np.float32(ni["top_p"][b]))
+    p, mp = oracle.normalise(_as_f32(ni["target"][b]), np.float32(T), tk, np.float32(tp), with_margin=True)
+    q, mq = oracle.normalise(_as_f32(ni["draft"][b]), np.float32(T), tk, np.float32(tp), with_margin=True)
+    filt = min(mp, mq)
+    rho = oracle.kseq_rho(p, q, k)
+    out = []
+    for i in range(k):
+        x = int(ni["candidates"][b, i])
+        u = oracle.uniform(seed, b, 1, 3 + i)
+        m = abs(u - p[x] / (rho * q[x])) if q[x] > 0 else np.inf
+        out.append(min(m, filt))
+        if u * rho * q[x] < p[x]:
+            return out
+    A, pa, _ = oracle.kseq_direct(p, q, k)
+    r = np.maximum(p - A, 0.0)
+    if not r.sum() > 0:
+        r = p.copy()
+    Z = r.sum()
+    v = oracle.uniform(seed, b, 1, 1) * Z
+    cum = np.cumsum(r)
+    j = int(np.searchsorted(cum, v, side="right"))
+    lo = cum[j - 1] if j > 0 else 0.0
+    hi = cum[min(j, len(cum) - 1)]
+    out.append(min(min(v - lo, hi - v) / Z, filt))
+    return out
+
+
+def run_kseq(wl, seed, rep=None):
+    rep = rep or ParityReport()
+    ni = wl.numpy_inputs()
+    dev = torch.device("cuda")
+    g = sv.spec_verify_kseq(wl.target.to(dev), wl.draft.to(dev), wl.candidates.to(dev), wl.temperature.to(dev),
+                            None if wl.num_candidates is None else wl.num_candidates.to(dev),
+                            None if wl.top_k is None else wl.top_k.to(dev),
+                            None if wl.top_p is None else wl.top_p.to(dev), seed=seed)
+    torch.cuda.synchronize()
+    tok, acc, st = oracle.kseq_verify(ni["target"], ni["draft"], ni["candidates"], ni["temperature"],
+                                      ni["num_candidates"], ni["top_k"], ni["top_p"], seed=seed)
+    gt, ga, gs = to_np(g["out_token"]), to_np(g["accepted"]), to_np(g["row_status"]).astype(np.uint32)
+    for b in range(wl.B):
+        if gs[b] != st[b]:
+            rep.hard.append(("status", b, int(gs[b]), int(st[b])))
+            continue
+        if st[b]:
+            if gt[b] != -1 or ga[b] != -1:
+                rep.hard.append(("invalid-row-outputs", b))
+            continue
+        k = wl.K if ni["num_candidates"] is None else int(ni["num_candidates"][b])
+        margins = _row_margins(ni, b, seed, k)
+        rep.decisions += len(margins)
+        low = min(margins) < MARGIN
+        rep.low_margin += sum(m < MARGIN for m in margins)
+        if gt[b] != tok[b] or ga[b] != acc[b]:
+            if low:
+                rep.excused += 1
+            else:
+                rep.hard.append(("kseq", b, int(gt[b]), int(tok[b]), int(ga[b]), int(acc[b]), min(margins)))
+    return rep, g
+
+
+def _batch(B, K, V, dtype, seed, T=1.0, k=None, p=None, sigma=1.0):
+    gen = torch.Generator().manual_seed(seed)
+    t = torch.randn(B, V, generator=gen) * 2
+    d = t + torch.randn(B, V, generator=gen) * sigma
+    if dtype == "bf16":
+        t, d = t.bfloat16(), d.bfloat16()
+    Tt = torch.full((B,), T) if np.isscalar(T) else torch.as_tensor(T, dtype=torch.float32)
+    kk = None if k is None else torch.full((B,), k, dtype=torch.int32)
+    pp = None if p is None else torch.full((B,), p, dtype=torch.float32)
+    cand = workloads._propose(d.unsqueeze(1).expand(B, K, V), Tt.float(), kk, pp, gen)
+    return workloads.KseqWorkload("kseq-edge", B, K, V, dtype, t.contiguous(), d.contiguous(), cand.contiguous(),
+                                  None, Tt.float(), kk, pp, seed)
+
+
+@pytest.mark.parametrize("K", [1, 2, 4, 8, 13])
+@pytest.mark.parametrize("V,dtype", [(37, "f32"), (1000, "f32"), (4096, "bf16")])
+def test_kseq_parity_small(K, V, dtype):
+    wl = _batch(48, K, V, dtype, seed=V + K, T=np.linspace(0.4, 1.6, 48))
+    rep = ParityReport()
+    for seed in (1, 2):
+        run_kseq(wl, seed, rep)
+    assert_ok(rep)
+
+
+def test_kseq_parity_filters_and_greedy():
+    wl = _batch(40, 5, 3000, "f32", seed=7, T=[0.0, 0.5, 1.0, 1.3] * 10, k=None, p=None)
+    wl.top_k = torch.tensor([0, 3, 50, 0, 300] * 8, dtype=torch.int32)
+    wl.top_p = torch.tensor([1.0, 0.9, 0.95, 0.5] * 10, dtype=torch.float32)
+    wl.num_candidates = torch.tensor([1, 2, 3, 4, 5] * 8, dtype=torch.int32)
+    # candidates from the filtered drafter of each row
+    gen = torch.Generator().manual_seed(3)
+    wl.candidates = workloads._propose(wl.draft.unsqueeze(1).expand(40, 5, 3000), wl.temperature, wl.top_k,
+                                       wl.top_p, gen)
+    rep, _ = run_kseq(wl, 9)
+    assert_ok(rep)
+
+
+@pytest.mark.parametrize("name,kw", [("kseq32k", dict(B=64)), ("kseq128k", dict(B=12))])
+def test_kseq_parity_recipes(name, kw):
+    wl = workloads.make_kseq(name, seed=2, **kw)
+    rep, g = run_kseq(wl, 5)
+    assert_ok(rep)
+    assert (to_np(g["accepted"]) >= 0).mean() > 0.3  # drafts are close: candidates are often accepted
+
+
+def test_invalid_rows():
+    wl = _batch(8, 3, 500, "f32", seed=4)
+    wl.num_candidates = torch.tensor([3, 0, 4, 3, 3, 3, 3, 3], dtype=torch.int32)
+    wl.candidates[3, 1] = 500
+    wl.temperature[4] = -1.0
+    wl.target[5, 7] = float("nan")
+    wl.draft[6, :] = float("-inf")
+    rep, g = run_kseq(wl, 3)
+    assert_ok(rep)
+    st = to_np(g["row_status"])
+    assert (st[1:7] != 0).all() and st[0] == 0 and st[7] == 0
+
+
+def test_page_counterexample_half_not_three_quarters():
+    """Draft always proposes A, the target is uniform on {A, B}, k = 2: K-SEQ emits A with
+    probability exactly 1/2 (the naive per-candidate rule would give 3/4)."""
+    B, V = 200_000, 2
+    dev = torch.device("cuda")
+    tgt = torch.zeros(B, V, device=dev)
+    drf = torch.tensor([0.0, float("-inf")], device=dev).expand(B, V).contiguous()
+    cand = torch.zeros(B, 2, dtype=torch.int32, device=dev)
+    g = sv.spec_verify_kseq(tgt, drf, cand, 1.0, seed=17)
+    torch.cuda.synchronize()
+    assert (to_np(g["row_status"]) == 0).all()
+    freq_a = float((g["out_token"] == 0).float().mean())
+    se = np.sqrt(0.25 / B)
+    assert abs(freq_a - 0.5) < 4 * se, freq_a
+    assert abs(freq_a - 0.75) > 100 * se
+
+
+@pytest.mark.parametrize("k", [2, 4])
+def test_output_law_is_the_target(k):
+    stats = pytest.importorskip("scipy.stats")
+    rng = np.random.default_rng(11 + k)
+    V, B = 6, 100_000
+    p = rng.dirichlet(np.ones(V))
+    q = rng.dirichlet(np.ones(V))
+    lp, lq = np.log(p).astype(np.float32), np.log(q).astype(np.float32)
+    pe = oracle.normalise(lp, 1.0)
+    qe = oracle.normalise(lq, 1.0)
+    dev = torch.device("cuda")
+    cand = torch.as_tensor(rng.choice(V, size=(B, k), p=qe / qe.sum()).astype(np.int32), device=dev)
+    g = sv.spec_verify_kseq(torch.as_tensor(np.broadcast_to(lp, (B, V)).copy(), device=dev),
+                            torch.as_tensor(np.broadcast_to(lq, (B, V)).copy(), device=dev), cand, 1.0, seed=99)
+    torch.cuda.synchronize()
+    counts = np.bincount(to_np(g["out_token"]), minlength=V)
+    _, pval = stats.chisquare(counts, pe * B)
+    assert pval > 1e-3, (counts / B, pe, pval)
