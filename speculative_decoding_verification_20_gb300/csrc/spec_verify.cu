@@ -298,6 +298,7 @@ int verify_call(const void* target_logits, const void* draft_logits, int dtype, 
     a.free_units = (uint32_t*)(ws + L.free_units);
     a.counts = (uint32_t*)(ws + L.counts);
     a.cand = (unsigned long long*)(ws + L.cand);
+    a.cand_rowcap = L.cand_rowcap;
     a.cand_cnt = (uint32_t*)(ws + L.cand_cnt);
     a.free_rec = (FreeRec*)(ws + L.free_rec);
     a.free_blk = (float*)(ws + L.free_blk);

@@ -125,7 +125,7 @@ __device__ int row_topk(const Args& a, uint32_t row_slot, int k, unsigned long l
     for (int j = 0; j < ppr; ++j) {
         const size_t piece = (size_t)row_slot * ppr + j;
         const int c = (int)__ldcg(&a.cand_cnt[piece]);
-        const unsigned long long* src = a.cand + piece * kListCap;
+        const unsigned long long* src = a.cand + (size_t)row_slot * a.cand_rowcap + (size_t)j * kListCap;
         for (int i0 = 0; i0 < c;) {
             if (kept + 32 > kSelBuf) kept = warp_keep_topk<KB>(buf, kept, k, lane);
             const int take = min(c - i0, kSelBuf - kept);

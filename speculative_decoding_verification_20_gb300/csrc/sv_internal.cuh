@@ -134,8 +134,10 @@ struct Args {
     uint32_t* stream_units;
     uint32_t* free_units;
     uint32_t* counts;         // kCnt* above
-    unsigned long long* cand; // [stream rows * ppr * kListCap] (key << 32 | ~id), unsorted
+    unsigned long long* cand; // per stream row, cand_rowcap entries: piece j's list at j * kListCap
+                              // (key << 32 | ~id, unsorted), each at most min(kListCap, piece length)
     uint32_t* cand_cnt;       // [stream rows * ppr]
+    int cand_rowcap;          // candidate entries reserved per stream row
     FreeRec* free_rec;        // [units] by free list index
     float* free_blk;          // [units][2][free_nblk]: per block sums of r (residual weights) and p
     int free_nblk;            // blocks per row of the free kernel's variant (set by its launcher)
@@ -146,6 +148,7 @@ struct WsLayout {
     size_t seq, seq_done, seq_status, unit_acc, unit_tok, stream_rows, dense_units, stream_units, free_units,
         counts, cand, cand_cnt, free_rec, free_blk, total;
     int ppr, free_nblk;
+    int cand_rowcap;  // candidate entries per stream row: kListCap per piece, the last piece min(kListCap, its length)
 };
 
 __host__ __device__ inline int tile_elems(int dtype) { return kTileBytes / (dtype == SV_BF16 ? 2 : 4); }
@@ -181,7 +184,11 @@ __host__ __device__ inline WsLayout ws_layout(int B, int G, int V, int dtype) {
     L.free_units = o;  o = align_up(o + 4 * units, 256);
     L.counts = o;      o = align_up(o + 64, 256);
     L.cand_cnt = o;    o = align_up(o + 4 * rows * L.ppr, 256);
-    L.cand = o;        o = align_up(o + 8 * rows * L.ppr * kListCap, 256);
+    {  // a piece's list never holds more entries than the piece has logits
+        const int last_len = V - (L.ppr - 1) * stream_piece_elems(dtype);
+        L.cand_rowcap = (L.ppr - 1) * kListCap + (last_len < kListCap ? last_len : kListCap);
+    }
+    L.cand = o;        o = align_up(o + 8 * rows * (size_t)L.cand_rowcap, 256);
     L.free_nblk = free_blocks(V, dtype, kFreeWarpsNarrow) > free_blocks(V, dtype, kFreeWarpsWide)
                       ? free_blocks(V, dtype, kFreeWarpsNarrow)
                       : free_blocks(V, dtype, kFreeWarpsWide);  // room for either variant

@@ -727,7 +727,8 @@ __device__ __forceinline__ int finish_piece(SelSmem& sm, GSync& g, const Args& a
     }
     if (lane == 0) sm.pub[warp] = 0u;  // every warp has read the floor: reset for the next piece
     if (cs.spec && !any_overflow && appended < k) return 0;
-    unsigned long long* out = a.cand + (size_t)w * kListCap;
+    const uint32_t row_slot = (uint32_t)w / (uint32_t)a.ppr;
+    unsigned long long* out = a.cand + (size_t)row_slot * a.cand_rowcap + (size_t)(w - row_slot * a.ppr) * kListCap;
     int written = total;
     if (total <= kListCap) {
         for (int i = lane; i < cs.st.cnt; i += 32) out[off + i] = L[i];

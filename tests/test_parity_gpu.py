@@ -310,16 +310,15 @@ def test_streaming_threshold_redo_and_overflow(dtype):
 
 @pytest.mark.parametrize("k,p_top", [(None, None), (3, None), (None, 0.9)])
 def test_chisquare_first_token_law_million_sequences(k, p_top):
-    """10^6 sequences (5 calls of 2 * 10^5 with different seeds; one call of 10^6
-    would need a 12 GB workspace for the select kernel's candidate lists, sized
-    for 512 per row whatever V), V = 8, gamma = 1, one (p, q) pair for all, x drawn
-    from the filtered q: the first emitted token (the accepted draft or the
-    residual draw) must follow the filtered p.  No filter runs the whole-row
+    """10^6 sequences in one call (the select kernel's candidate lists are sized by
+    the rows' length: 8 entries per row here), V = 8, gamma = 1, one (p, q) pair for
+    all, x drawn from the filtered q: the first emitted token (the accepted draft or
+    the residual draw) must follow the filtered p.  No filter runs the whole-row
     kernel, top-k 3 the select and combine kernels, top-p 0.9 the nucleus cut.
     The filtered laws come from the oracle (one row, probability outputs)."""
     stats = pytest.importorskip("scipy.stats")
     rng = np.random.default_rng(2024 + (k or 0) + int(100 * (p_top or 0)))
-    V, B, calls = 8, 200_000, 5
+    V, B, calls = 8, 1_000_000, 1
     lp = np.log(rng.dirichlet(np.ones(V))).astype(np.float32)
     lq = np.log(rng.dirichlet(np.ones(V))).astype(np.float32)
     kk = None if k is None else np.array([k], dtype=np.int32)
