@@ -93,6 +93,26 @@ __device__ __forceinline__ void block_sum_vec(const double (&v)[N], DenseSmem& s
     __syncthreads();
 }
 
+// The same for N floats per thread: warp sums in fp32 (32 terms), the warps'
+// partials added in fp64 by N threads.
+template <int N>
+__device__ __forceinline__ void block_sum_vec_f(const float (&v)[N], DenseSmem& sm, double* out) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float s = warp_sum(v[i]);
+        if (lane == 0) sm.red[wid][i] = (double)s;
+    }
+    __syncthreads();
+    if (threadIdx.x < N) {
+        double s = 0.0;
+#pragma unroll
+        for (int w = 0; w < kDenseThreads / 32; ++w) s += sm.red[w][threadIdx.x];
+        out[threadIdx.x] = s;
+    }
+    __syncthreads();
+}
+
 template <int N>
 __device__ __forceinline__ void block_max_vec(const double (&v)[N], DenseSmem& sm, double* out) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -124,13 +144,18 @@ __device__ __forceinline__ double block_excl_scan_dbl(double v, DenseSmem& sm, d
     }
     if (lane == 31) sm.red[wid][0] = x;
     __syncthreads();
-    double before = 0.0, tot = 0.0;
+    // lane w < 8 holds warp w's total: an inclusive scan over the 8 lanes gives
+    // every thread the totals before its warp and of the block
+    constexpr int NW = kDenseThreads / 32;
+    double wsum = lane < NW ? sm.red[lane][0] : 0.0;
 #pragma unroll
-    for (int w = 0; w < kDenseThreads / 32; ++w) {
-        const double s = sm.red[w][0];
-        if (w < wid) before += s;
-        tot += s;
+    for (int o = 1; o < NW; o <<= 1) {
+        const double y = __shfl_up_sync(0xFFFFFFFFu, wsum, o);
+        if (lane >= o) wsum += y;
     }
+    const double incl_prev = __shfl_sync(0xFFFFFFFFu, wsum, (wid + 31) & 31);
+    const double tot = __shfl_sync(0xFFFFFFFFu, wsum, NW - 1);
+    const double before = wid > 0 ? incl_prev : 0.0;
     __syncthreads();
     *total = tot;
     return before + (x - v);
@@ -151,16 +176,16 @@ __device__ int ordered_search(Ctx& c, DenseSmem& sm, WF wgt, double target, bool
                               double* cum_incl) {
     using C = DenseCfg<TIn, R>;
     // per-thread sums of each load group (R groups of VEC consecutive columns)
-    double gs[R];
+    float gs[R];
 #pragma unroll
     for (int l = 0; l < R; ++l) {
         float s = 0.0f;
 #pragma unroll
         for (int j = 0; j < C::VEC; ++j) s += wgt(l, j);
-        gs[l] = (double)s;
+        gs[l] = s;
     }
     double* G = sm.res + 2 * kXch - R;  // scratch tail of res, outside the exchange results
-    block_sum_vec<R>(gs, sm, G);
+    block_sum_vec_f<R>(gs, sm, G);
     double gtot[R];
     double cta_total = 0.0;
 #pragma unroll
@@ -207,7 +232,7 @@ __device__ int ordered_search(Ctx& c, DenseSmem& sm, WF wgt, double target, bool
         double mine = 0.0;
 #pragma unroll
         for (int l = 0; l < R; ++l)
-            if (l == lsel) mine = gs[l];
+            if (l == lsel) mine = (double)gs[l];
         double tot_g;
         const double before = block_excl_scan_dbl(mine, sm, &tot_g);
         __shared__ int s_thr;
@@ -332,38 +357,45 @@ __device__ void select_keep(Ctx& c, DenseSmem& sm, float (&e)[DenseCfg<TIn, R>::
             float s = 0.0f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) s += sm.hist[bin][part * 16 + i];
-            double ds = (double)s;
-            ds += __shfl_xor_sync(0xFFFFFFFFu, ds, 16);
+            s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
             const int wid = t >> 5, lane = t & 31;
-            if (lane < 16) sm.red[wid][lane] = ds;
+            if (lane < 16) sm.red[wid][lane] = (double)s;
         }
         __syncthreads();
         __shared__ double s_bins[16];
-        if (t < 16) {
+        if (t < 16) {  // read back by this same thread in the exchange below
             double s = 0.0;
 #pragma unroll
             for (int w = 0; w < kDenseThreads / 32; ++w) s += sm.red[w][t];
             s_bins[t] = s;
         }
-        __syncthreads();
         cluster_combine(c, sm, s_bins, 16, false);
-        double acc = above;
-        int dsel = -1, lowest = -1;
-        for (int bin = 15; bin >= 0; --bin) {
-            const double g = sm.res[bin];
-            if (g > 0.0) lowest = bin;
-            if (dsel < 0 && g > 0.0 && acc + g >= target) dsel = bin;
-            if (dsel < 0) acc += g;
-        }
-        if (dsel < 0) {  // the weight never reaches the target (rounding): keep everything
-            keep_all = true;
-            dsel = (lowest < 0) ? 0 : lowest;
-            acc = above;
-            for (int bin = 15; bin > dsel; --bin) acc += sm.res[bin];
+        // the digit: one thread walks the 16 bins (an fp64 chain), the block reads it
+        __shared__ double s_above;
+        __shared__ int s_dsel, s_keep_all;
+        if (t == 0) {
+            double acc = above;
+            int dsel = -1, lowest = -1, all = 0;
+            for (int bin = 15; bin >= 0; --bin) {
+                const double g = sm.res[bin];
+                if (g > 0.0) lowest = bin;
+                if (dsel < 0 && g > 0.0 && acc + g >= target) dsel = bin;
+                if (dsel < 0) acc += g;
+            }
+            if (dsel < 0) {  // the weight never reaches the target (rounding): keep everything
+                all = 1;
+                dsel = (lowest < 0) ? 0 : lowest;
+                acc = above;
+                for (int bin = 15; bin > dsel; --bin) acc += sm.res[bin];
+            }
+            s_above = acc;
+            s_dsel = dsel;
+            s_keep_all = all;
         }
         __syncthreads();
-        above = acc;
-        prefix |= (uint32_t)dsel << sh;
+        above = s_above;
+        keep_all = s_keep_all != 0;
+        prefix |= (uint32_t)s_dsel << sh;
         if (keep_all) break;
     }
     if (keep_all) return;
@@ -445,24 +477,37 @@ __device__ __forceinline__ void load_row(const TIn* row, const Ctx& c, int V, fl
 // largest float rho_lo with f(rho_lo) > 0, four bits per round, f being evaluated
 // in fp64 at the 16 digit boundaries from a cluster histogram of the q and p mass
 // of the ratio keys in the current range; inside (rho_lo, next float) no ratio
-// lies, so Q and P are constants there and f = 0 is solved by fp64 bisection.
+// lies, so Q and P are constants there and f, affine there to within rounding,
+// is zero at the interpolation of its values at the two ends.
 template <typename TIn, int R>
 __device__ void kseq_unit(const Args& a, Ctx& c, DenseSmem& sm, double* s_vals, const float (&p)[DenseCfg<TIn, R>::EPR],
                           const float (&q)[DenseCfg<TIn, R>::EPR], int b, int k, int V) {
     using C = DenseCfg<TIn, R>;
     const int t = threadIdx.x;
     const double kd = (double)k;
-    auto fval = [&](double rho, double Q, double P) -> double {  // f at rho for fixed Q, P
-        const double beta = Q + (P > 0.0 ? P / rho : 0.0);
-        double pw = 1.0;  // (1 - beta)^k, k <= 13: repeated products
-        for (int i = 0; i < k; ++i) pw *= (1.0 - beta);
-        return 1.0 - pw - rho * beta;
+    // rho^k f(rho) = rho^k (1 - rho Q - P) - (rho (1 - Q) - P)^k for fixed Q, P (rho beta =
+    // rho Q + P and 1 - beta = (rho (1 - Q) - P) / rho): the sign of f without a
+    // division; k <= 13 products on each side
+    auto fk = [&](double rho, double Q, double P) -> double {
+        const double lhs = 1.0 - rho * Q - P, base = rho * (1.0 - Q) - P;
+        double rk = 1.0, bk = 1.0;
+        for (int i = 0; i < k; ++i) {
+            rk *= rho;
+            bk *= base;
+        }
+        return rk * lhs - bk;
     };
-    // ---- the radix descent
+    // ---- the radix descent.  Per round: each thread bins its own elements into
+    // its column of the (q, p) histograms; 8 threads per column sum them
+    // (compensated fp32); 32 threads add the 8 partials in fp64; the cluster sums
+    // them; warp 0 evaluates f at the 16 digit boundaries (16-lane scans) and
+    // carries Q (q mass above the range) and P (p mass below it) in registers.
+    // The ratio key is the float bits of p / q by the fast reciprocal: the same
+    // key in every round, so the histograms stay consistent; a ratio within two
+    // ulps of rho* changes beta by that fraction of the token's own mass.
     uint32_t prefix = 0u;
-    double Qhi = 0.0, Plo = 0.0;  // q mass of ratio keys above the current range, p mass below it
+    double Qhi = 0.0, Plo = 0.0, Pfin = 0.0;  // meaningful in warp 0
     __shared__ int s_sel;
-    __shared__ double s_q[16], s_p[16];
     for (int d = 7; d >= 0; --d) {
         const int sh = 4 * d;
 #pragma unroll
@@ -476,7 +521,7 @@ __device__ void kseq_unit(const Args& a, Ctx& c, DenseSmem& sm, double* s_vals, 
             for (int j = 0; j < C::VEC; ++j) {
                 const int i = l * C::VEC + j;
                 if (col_of<TIn, R>(c, l, j) < V && p[i] > 0.0f && q[i] > 0.0f) {
-                    const uint32_t key = __float_as_uint(p[i] / q[i]);
+                    const uint32_t key = __float_as_uint(__fdividef(p[i], q[i]));
                     if (d == 7 || (key >> (sh + 4)) == (prefix >> (sh + 4))) {
                         sm.hist[(key >> sh) & 15u][t] += q[i];
                         sm.hist2[(key >> sh) & 15u][t] += p[i];
@@ -484,31 +529,44 @@ __device__ void kseq_unit(const Args& a, Ctx& c, DenseSmem& sm, double* s_vals, 
                 }
             }
         __syncthreads();
-        {  // block sums of the 32 (bin, mass) columns: 8 threads per column
+        {  // partial sums of the 32 (bin, mass) columns: 8 threads per column, Kahan in fp32
             const int col = t & 31, part = t >> 5;
             const float* h = (col < 16) ? &sm.hist[col][0] : &sm.hist2[col - 16][0];
-            double sum = 0.0;
-#pragma unroll 4
-            for (int i = 0; i < kDenseThreads / 8; ++i) sum += (double)h[part * (kDenseThreads / 8) + i];
-            sm.red[part][col] = sum;
+            float sum = 0.0f, comp = 0.0f;
+#pragma unroll 8
+            for (int i = 0; i < kDenseThreads / 8; ++i) {
+                const float y = h[part * (kDenseThreads / 8) + i] - comp;
+                const float tt = sum + y;
+                comp = (tt - sum) - y;
+                sum = tt;
+            }
+            sm.red[part][col] = (double)sum - (double)comp;
         }
         __syncthreads();
         if (t < 32) {
             double sum = 0.0;
 #pragma unroll
             for (int w = 0; w < 8; ++w) sum += sm.red[w][t];
-            s_vals[t] = sum;
+            s_vals[t] = sum;  // read back by this same thread in the exchange below
         }
-        __syncthreads();
         cluster_combine(c, sm, s_vals, 32, false);
-        if (t < 16) {
-            s_q[t] = sm.res[t];
-            s_p[t] = sm.res[16 + t];
-        }
-        __syncthreads();
         if (t < 32) {
             // digit t of this round: is f > 0 at the start of its range?  (rho < 1: yes,
             // f(1) >= 0 and rho* >= 1; rho > k: no; sign-bit keys are not ratios)
+            // Q_t = Qhi + sum_{j >= t} q_j and P_t = Plo + sum_{j < t} p_j by 16-lane scans
+            double qs = t < 16 ? sm.res[15 - t] : 0.0, ps = t < 16 ? sm.res[16 + t] : 0.0;
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                const double qy = __shfl_up_sync(0xFFFFFFFFu, qs, o), py = __shfl_up_sync(0xFFFFFFFFu, ps, o);
+                if ((t & 15) >= o) {
+                    qs += qy;
+                    ps += py;
+                }
+            }
+            // lane t: qs = sum_{j >= 15 - t} q_j, ps = sum_{j <= t} p_j (lanes 16..31: 0)
+            const double q_ge = __shfl_sync(0xFFFFFFFFu, qs, (15 - t) & 31);  // sum_{j >= t} q_j
+            const double p_prev = __shfl_sync(0xFFFFFFFFu, ps, (t + 31) & 31);
+            const double p_lt = t > 0 ? p_prev : 0.0;  // sum_{j < t} p_j
             bool pos = false;
             if (t < 16 && !(d == 7 && t >= 8)) {
                 const float rho_f = __uint_as_float(prefix | ((uint32_t)t << sh));
@@ -516,44 +574,47 @@ __device__ void kseq_unit(const Args& a, Ctx& c, DenseSmem& sm, double* s_vals, 
                 if (rho < 1.0) {
                     pos = true;
                 } else if (rho <= kd) {
-                    double Q = Qhi, P = Plo;
-                    for (int j = 0; j < 16; ++j) {
-                        if (j >= t) Q += s_q[j];
-                        else P += s_p[j];
-                    }
-                    pos = fval(rho, Q, P) > 0.0;
+                    pos = fk(rho, Qhi + q_ge, Plo + p_lt) > 0.0;
                 }
             }
             const unsigned m = __ballot_sync(0xFFFFFFFFu, pos);
-            if (t == 0) s_sel = m ? 31 - __clz(m) : 0;  // f does not increase: the largest such digit
+            const int sel = m ? 31 - __clz(m) : 0;  // f does not increase: the largest such digit
+            // carry: the q mass of the digits above sel, the p mass of those below it; the
+            // keys equal to the final prefix (the last round's digit) lie below every rho
+            // inside (rho_lo, next float): their p mass joins P
+            const double q_above = __shfl_sync(0xFFFFFFFFu, q_ge, (sel + 1) & 31);  // lane 16: 0
+            const double p_below = __shfl_sync(0xFFFFFFFFu, p_lt, sel);
+            const double p_upto = __shfl_sync(0xFFFFFFFFu, ps, sel);
+            Pfin = Plo + p_upto;
+            Qhi += q_above;
+            Plo += p_below;
+            if (t == 0) s_sel = sel;
         }
         __syncthreads();
-        const int sel = s_sel;
-#pragma unroll 1
-        for (int j = 0; j < 16; ++j) {
-            if (j > sel) Qhi += s_q[j];
-            if (j < sel) Plo += s_p[j];
-        }
-        prefix |= (uint32_t)sel << sh;
-        __syncthreads();
+        prefix |= (uint32_t)s_sel << sh;
     }
-    // the ratios equal to rho_lo are below every rho in (rho_lo, next float)
-    const double Q = Qhi, P = Plo + s_p[prefix & 15u];
+    const double Q = Qhi, P = Pfin;  // thread 0's values are the ones used below
     __shared__ double s_rho, s_beta;
     __shared__ int s_tok, s_idx;
     if (t == 0) {
+        // inside [lo, hi] (at most one float step wide, relative 1.2e-7) f is affine to
+        // within rounding: the root is the interpolation of its two ends
         double lo = fmax(1.0, (double)__uint_as_float(prefix));
         double hi = fmin(kd, (double)__uint_as_float(prefix + 1u));
-        if (!(lo < hi)) lo = hi;
-        for (int it = 0; it < 200 && hi - lo > 1e-15 * hi; ++it) {
-            const double mid = 0.5 * (lo + hi);
-            if (fval(mid, Q, P) > 0.0)
-                lo = mid;
-            else
-                hi = mid;
+        double rho = hi;
+        if (lo < hi) {
+            auto f = [&](double r) {
+                const double beta = Q + (P > 0.0 ? P / r : 0.0);
+                double pw = 1.0;
+                for (int i = 0; i < k; ++i) pw *= (1.0 - beta);
+                return 1.0 - pw - r * beta;
+            };
+            const double flo = f(lo), fhi = f(hi);
+            if (flo > 0.0 && fhi < 0.0) rho = lo + (hi - lo) * (flo / (flo - fhi));
+            else rho = flo > 0.0 ? hi : lo;
         }
-        s_rho = hi;
-        s_beta = Q + (P > 0.0 ? P / hi : 0.0);
+        s_rho = rho;
+        s_beta = Q + (P > 0.0 ? P / rho : 0.0);
     }
     __syncthreads();
     const double rho = s_rho, beta = s_beta;
