@@ -34,8 +34,13 @@ UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
 # kernels one spec_verify call launches: plan, select (streaming top-k), combine,
 # the whole-row kernel of rows without top-k and its per-unit tail, and the
-# dense cluster kernel (a kernel whose path no row takes exits at once)
+# dense cluster kernel (a kernel whose path no row takes exits at once);
+# spec_verify_gumbel adds its one-pass kernel of unfiltered rows
 LAUNCHES_PER_STEP = 6
+
+
+def launches_per_step(rule: str = "sampling") -> int:
+    return LAUNCHES_PER_STEP + (1 if rule == "gumbel" else 0)
 # sources of each kernel whose DRAM traffic profiles/traffic.json records: a
 # record counts only while these files are unchanged since its capture
 _CSRC = "speculative_decoding_verification_20_gb300/csrc/"
@@ -43,6 +48,7 @@ KERNEL_SOURCES = {
     "stream": tuple(_CSRC + f for f in ("sv_stream.cu", "sv_keys.cuh", "sv_internal.cuh", "sv_finalize.cuh")),
     "free": tuple(_CSRC + f for f in ("sv_free.cu", "sv_cf.cuh", "sv_warp_sort.cuh", "sv_internal.cuh",
                                       "sv_finalize.cuh")),
+    "gumbel": tuple(_CSRC + f for f in ("sv_gumbel.cu", "sv_internal.cuh", "sv_finalize.cuh")),
 }
 
 
@@ -265,21 +271,28 @@ def rank_seed(rank: int) -> int:
 def bytes_by_path(wl, stream_max_k: int, rule: str = "sampling") -> dict:
     """Algorithmic logit bytes each path of the library reads for this batch:
     greedy or 1 <= top_k <= stream_max_k rows stream (select kernel); rows with
-    no top-k the whole-row kernel (free); larger top-k the cluster kernel.  The
-    sampling rule reads 2 gamma_b + 1 rows per sequence, shared noise the
-    gamma_b + 1 target rows only."""
+    no top-k the whole-row kernel (free), except that shared noise on rows with
+    no filter at all takes its one-pass kernel (gumbel); larger top-k the cluster
+    kernel.  The sampling rule reads 2 gamma_b + 1 rows per sequence, shared
+    noise the gamma_b + 1 target rows only."""
     import numpy as np
 
     gam = wl.gammas()
     T = wl.temperature.detach().cpu().numpy()
     k = np.zeros(wl.B, dtype=np.int64) if wl.top_k is None else wl.top_k.detach().cpu().numpy().astype(np.int64)
     k = np.where((k > 0) & (k < wl.V), k, 0)
+    P = np.ones(wl.B) if wl.top_p is None else wl.top_p.detach().cpu().numpy().astype(np.float64)
     stream = (T == 0) | ((k >= 1) & (k <= stream_max_k))
     free = ~stream & (k == 0)
+    gumbel = free & (P >= 1.0) if rule == "gumbel" else np.zeros(wl.B, dtype=bool)
+    free &= ~gumbel
     es = 2 if wl.dtype == "bf16" else 4
     rowb = ((gam + 1) if rule == "gumbel" else (2 * gam + 1)) * wl.V * es
-    return {"stream": int(rowb[stream].sum()), "free": int(rowb[free].sum()),
-            "dense": int(rowb[~stream & ~free].sum())}
+    out = {"stream": int(rowb[stream].sum()), "free": int(rowb[free].sum()),
+           "dense": int(rowb[~stream & ~free & ~gumbel].sum())}
+    if rule == "gumbel":
+        out["gumbel"] = int(rowb[gumbel].sum())
+    return out
 
 
 def workload_config(name: str, B: int | None = None) -> dict:
@@ -296,8 +309,10 @@ def workload_config(name: str, B: int | None = None) -> dict:
 
 
 def run_kseq(args, sv, workloads, world, rank, dev):
-    """K-SEQ: one position per row with k candidates; the cluster kernel holds each
-    row's target and draft on chip while it finds rho*.  Positions = rows."""
+    """K-SEQ: one position per row with k candidates.  Rows with top-k <= 256 take the
+    streaming select kernel and solve rho* over their kept lists in the combine
+    kernel; the others are held on chip by the cluster kernel while it finds rho*.
+    Positions = rows."""
     import torch
     import torch.distributed as dist
 
@@ -352,8 +367,11 @@ def run_kseq(args, sv, workloads, world, rank, dev):
         a_.record(stream)
         b_.record(stream)
     torch.cuda.synchronize(dev)
+    tk = None if wl.top_k is None else wl.top_k.detach().cpu()
+    listed = tk is not None and bool(((tk >= 1) & (tk <= sv.SV_STREAM_MAX_TOP_K)).all())
+    main = "stream" if listed else "dense"  # the kernel that reads this batch's logits
     for i in range(args.steps):
-        step(3_000_000 + i, events={"dense": kev[i]})
+        step(3_000_000 + i, events={main: kev[i]})
     torch.cuda.synchronize(dev)
     kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
     peak, peak_kind = measured_peak()
@@ -373,7 +391,9 @@ def run_kseq(args, sv, workloads, world, rank, dev):
         "hbm_gbs_step": nbytes / (ms_step * 1e-3) / 1e9, "hbm_frac_step": nbytes / (ms_step * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     "kernel": "dense_kernel (cluster path, K-SEQ)", "kernel_ms": kernel_ms,
+                     "kernel": ("select_kernel (streaming top-k path; K-SEQ on the kept lists in combine)"
+                                if main == "stream" else "dense_kernel (cluster path, K-SEQ)"),
+                     "kernel_ms": kernel_ms,
                      "algorithmic_bytes_per_launch": nbytes, "traffic": None},
         "e2e": None, "gpu_launches": LAUNCHES_PER_STEP * args.steps, "clocks": clk.summary(wall0, wall1),
     }
@@ -589,14 +609,15 @@ def main():
                 else "fallback 6.8 TB/s",
                 "kernel": {"stream": "select_kernel (streaming top-k path)",
                            "free": "free_kernel (whole-row path: rows without top-k)",
-                           "dense": "dense_kernel (cluster path)"}[main],
+                           "dense": "dense_kernel (cluster path)",
+                           "gumbel": "gumbel_kernel (one pass of shared noise: rows without filters)"}[main],
                 "kernel_ms": kernel_ms_avg, "algorithmic_bytes_per_launch": main_bytes,
                 "traffic": traffic,
                 "timing": "kernel events in a separate run of K steps "
                           f"({ms_step_with_events:.4f} ms per step with the events recorded)"}
-    if args.rule == "gumbel" and main == "free":
-        # shared noise on rows without top-k: a Philox block per 4 tokens and two logarithms
-        # per token make the whole-row kernel issue-bound, not HBM-bound
+    if args.rule == "gumbel" and main in ("free", "gumbel"):
+        # shared noise on rows without top-k: a quarter Philox block and the noise test
+        # per token make the kernel issue-bound, not HBM-bound
         inst = recorded_instructions(args.rule, args.workload, main, args.batch is None)
         hbm = dict(roofline)
         roofline = {"bound": "alu", "unit": "T thread-inst/s", "peak": ALU_PEAK_TINST,
@@ -621,7 +642,7 @@ def main():
         "hbm_frac_step": bytes_per_launch / (ms_step * 1e-3) / 1e9 / peak,
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": launches_per_step(args.rule) * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:

@@ -139,6 +139,8 @@ typedef enum {
  *   ev_dense   the same around the dense cluster kernel (top-k > 256)
  *   ev_free    the same around the whole-row kernel of rows with no top-k
  *              (its per-unit tail kernel follows, outside the events)
+ *   ev_gumbel  the same around the one-pass kernel of spec_verify_gumbel's rows
+ *              with no filter (temperature only); not recorded by other calls
  *   lenience   [B] float or NULL (1 everywhere): the lenient acceptance test of
  *              the review page's section Lenience -- draft token x_i is accepted
  *              iff u_i * l_b * q_i(x_i) < p_i(x_i), so no token is emitted with
@@ -165,6 +167,7 @@ typedef struct {
     void* ev_free[2];
     const float* lenience;
     uint64_t wait_limit_ns;
+    void* ev_gumbel[2];
 } sv_options;
 
 int spec_verify_ex(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
@@ -253,6 +256,9 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, int 
  * workspace     spec_verify_workspace_size() bytes for the same shape and dtype
  * options       NULL or sv_options: path, pos_accept (draft k equals t_k), wait_limit_ns
  *               and the events are honoured; lenience is ignored
+ * Rows with neither top-k nor top-p (temperature > 0) take one pass: log p differs
+ * from l / T by a constant of the row, so t_k = argmax_i(l_i / T + g_k,i) needs no
+ * maximum or sum; the batch's rows are cut into equal parts, one per CTA.
  * Errors and asynchrony as spec_verify.
  */
 int spec_verify_gumbel(const void* target_logits, int dtype, const int32_t* draft_tokens, const int32_t* num_draft,
@@ -284,10 +290,14 @@ int spec_verify_gumbel(const void* target_logits, int dtype, const int32_t* draf
  * row_status     [B] uint32 out or NULL: SV_ROW_* bits (SV_ROW_BAD_NUM_DRAFT for k_b,
  *                SV_ROW_BAD_DRAFT_TOKEN for a candidate outside [0, V))
  * workspace      spec_verify_kseq_workspace_size() bytes
- * options        NULL or sv_options: ev_dense (the events around the cluster kernel) and
- *                wait_limit_ns are honoured; the rest is ignored
- * Each row is one unit of the cluster kernel (the rows are held on chip while
- * rho* is found).  Errors and asynchrony as spec_verify.
+ * options        NULL or sv_options: path (SV_PATH_DENSE sends every row to the cluster
+ *                kernel), ev_stream and ev_dense (the events around the streaming and
+ *                cluster kernels) and wait_limit_ns are honoured; the rest is ignored
+ * Rows with 1 <= top_k <= SV_STREAM_MAX_TOP_K, or temperature 0, are supported on
+ * their kept lists: the streaming top-k kernel selects both rows' candidates and
+ * one warp solves rho* and draws over those lists.  Other rows are each one unit
+ * of the cluster kernel (the rows are held on chip while rho* is found).  Errors
+ * and asynchrony as spec_verify.
  */
 size_t spec_verify_kseq_workspace_size(int B, int K, int V, int dtype);
 int spec_verify_kseq(const void* target_logits, const void* draft_logits, int dtype, const int32_t* candidates,

@@ -50,7 +50,8 @@ class SpecVerifyError(RuntimeError):
 class _Options(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32), ("pos_accept", ctypes.c_void_p), ("pos_token", ctypes.c_void_p),
                 ("path", ctypes.c_int32), ("ev_stream", ctypes.c_void_p * 2), ("ev_dense", ctypes.c_void_p * 2),
-                ("ev_free", ctypes.c_void_p * 2), ("lenience", ctypes.c_void_p), ("wait_limit_ns", ctypes.c_uint64)]
+                ("ev_free", ctypes.c_void_p * 2), ("lenience", ctypes.c_void_p), ("wait_limit_ns", ctypes.c_uint64),
+                ("ev_gumbel", ctypes.c_void_p * 2)]
 
 
 _lib = None
@@ -234,7 +235,8 @@ def spec_verify_gumbel(target: torch.Tensor, draft_tokens: torch.Tensor, tempera
     (float32 or bfloat16, CUDA), the drafter's tokens [B, G].  Returns accepted_len [B],
     out_tokens [B, G+1], target_tokens [B, G+1] (the target's noisy argmax at every
     position, -1 beyond gamma_b + 1), row_status [B] and, with positions=True,
-    pos_accept [B, G] (draft k equals the target's token k)."""
+    pos_accept [B, G] (draft k equals the target's token k).  events: as spec_verify,
+    plus "gumbel": (begin, end) around the one-pass kernel of the unfiltered rows."""
     lib = load_library()
     if not target.is_cuda or target.dim() != 3:
         raise ValueError("target must be a CUDA tensor [B, G+1, V]")
@@ -260,7 +262,7 @@ def spec_verify_gumbel(target: torch.Tensor, draft_tokens: torch.Tensor, tempera
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     opts = _Options(ctypes.sizeof(_Options), _ptr(pa), None, SV_PATH_DENSE if path == "dense" else SV_PATH_AUTO)
     opts.wait_limit_ns = int(wait_limit_ns)
-    for key in ("stream", "dense", "free"):
+    for key in ("stream", "dense", "free", "gumbel"):
         if events and events.get(key):
             getattr(opts, "ev_" + key)[0] = events[key][0].cuda_event
             getattr(opts, "ev_" + key)[1] = events[key][1].cuda_event
@@ -278,11 +280,13 @@ def spec_verify_gumbel(target: torch.Tensor, draft_tokens: torch.Tensor, tempera
 
 def spec_verify_kseq(target: torch.Tensor, draft: torch.Tensor, candidates: torch.Tensor, temperature,
                      num_candidates=None, top_k=None, top_p=None, *, seed: int, stream=None,
-                     workspace: Optional[torch.Tensor] = None, events: Optional[dict] = None) -> dict:
+                     workspace: Optional[torch.Tensor] = None, events: Optional[dict] = None,
+                     path: str = "auto") -> dict:
     """K-SEQ verification of one position per row on the GPU: target and draft logits
     [B, V] (float32 or bfloat16, CUDA), k candidates per row [B, K] (K <= 13).  Returns
     out_token [B], accepted [B] (the accepted candidate's index, -1: the residual draw)
-    and row_status [B]."""
+    and row_status [B].  path="dense" sends every row to the cluster kernel; events:
+    {"stream": (begin, end), "dense": (begin, end)} around those kernels."""
     lib = load_library()
     if not (target.is_cuda and draft.is_cuda) or target.dim() != 2 or tuple(draft.shape) != tuple(target.shape):
         raise ValueError("target and draft must be CUDA tensors [B, V] of one shape")
@@ -306,10 +310,11 @@ def spec_verify_kseq(target: torch.Tensor, draft: torch.Tensor, candidates: torc
     need = int(lib.spec_verify_kseq_workspace_size(B, K, V, dt))
     ws = workspace if workspace is not None else _workspace(max(need, 256), dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    opts = _Options(ctypes.sizeof(_Options), None, None, SV_PATH_DENSE)
-    if events and events.get("dense"):  # (begin, end) torch.cuda.Event around the cluster kernel
-        opts.ev_dense[0] = events["dense"][0].cuda_event
-        opts.ev_dense[1] = events["dense"][1].cuda_event
+    opts = _Options(ctypes.sizeof(_Options), None, None, SV_PATH_DENSE if path == "dense" else SV_PATH_AUTO)
+    for key in ("stream", "dense"):
+        if events and events.get(key):
+            getattr(opts, "ev_" + key)[0] = events[key][0].cuda_event
+            getattr(opts, "ev_" + key)[1] = events[key][1].cuda_event
     with torch.cuda.device(dev):
         rc = lib.spec_verify_kseq(_ptr(target), _ptr(draft), dt, _ptr(cand), _ptr(nc), _ptr(T), _ptr(tk), _ptr(tp),
                                   ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF), B, K, V, _ptr(tok), _ptr(acc),

@@ -48,7 +48,7 @@ __device__ __forceinline__ uint32_t block_excl_scan_1024(uint32_t v, uint32_t* s
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
     __shared__ uint32_t s_warp[32];
     grid_dependents_go();
-    uint32_t base_rows = 0, base_units = 0, base_sunits = 0, base_funits = 0;
+    uint32_t base_rows = 0, base_units = 0, base_sunits = 0, base_funits = 0, base_gunits = 0;
     const int G = a.G, V = a.V;
     for (int b0 = 0; b0 < a.B; b0 += blockDim.x) {
         const int b = b0 + threadIdx.x;
@@ -88,20 +88,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
                 const bool stream = (k >= 1 && k <= kStreamMaxK);
                 // no top-k: the whole-row kernel (with the nucleus cut when top-p < 1)
                 mode = a.force_dense ? kModeDense : stream ? kModeStream : k == 0 ? kModeFree : kModeDense;
-                if (a.kseq) mode = kModeDense;  // K-SEQ: one unit per row, held by a cluster
+                // K-SEQ: one unit per row; top-k rows from their kept lists (select +
+                // combine), the others held by a cluster
+                if (a.kseq && mode != kModeStream) mode = kModeDense;
+                // shared noise on a row with no filter: one pass of noise and argmax
+                if (a.gumbel && mode == kModeFree && !(P < 1.0f)) mode = kModeGumbel;
                 if (mode == kModeStream)
-                    nrows = a.gumbel ? gamma + 1 : 2 * gamma + 1;  // shared noise: target rows only
+                    nrows = a.kseq ? 2 : a.gumbel ? gamma + 1 : 2 * gamma + 1;  // shared noise: target rows only
                 else if (mode == kModeDense)
                     nunits = a.kseq ? 1 : gamma + 1;
             }
         }
-        const uint32_t nsunits = (mode == kModeStream) ? (uint32_t)(gamma + 1) : 0u;
+        const uint32_t nsunits = (mode == kModeStream) ? (a.kseq ? 1u : (uint32_t)(gamma + 1)) : 0u;
         const uint32_t nfunits = (mode == kModeFree) ? (uint32_t)(gamma + 1) : 0u;
-        uint32_t tot_r, tot_u, tot_s, tot_f;
+        const uint32_t ngunits = (mode == kModeGumbel) ? (uint32_t)(gamma + 1) : 0u;
+        uint32_t tot_r, tot_u, tot_s, tot_f, tot_g;
         const uint32_t off_r = block_excl_scan_1024(nrows, s_warp, &tot_r);
         const uint32_t off_u = block_excl_scan_1024(nunits, s_warp, &tot_u);
         const uint32_t off_s = block_excl_scan_1024(nsunits, s_warp, &tot_s);
         const uint32_t off_f = block_excl_scan_1024(nfunits, s_warp, &tot_f);
+        const uint32_t off_g = block_excl_scan_1024(ngunits, s_warp, &tot_g);
         if (b < a.B) {
             SeqInfo si;
             si.mode = mode;
@@ -119,6 +125,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
             for (uint32_t u = 0; u < nunits; ++u) a.dense_units[base_units + off_u + u] = ((uint32_t)b << 8) | u;
             for (uint32_t u = 0; u < nsunits; ++u) a.stream_units[base_sunits + off_s + u] = ((uint32_t)b << 8) | u;
             for (uint32_t u = 0; u < nfunits; ++u) a.free_units[base_funits + off_f + u] = ((uint32_t)b << 8) | u;
+            for (uint32_t u = 0; u < ngunits; ++u) {
+                const uint32_t w = base_gunits + off_g + u;
+                a.gum_units[w] = ((uint32_t)b << 8) | u;
+                a.gum_key[w] = 0ull;
+                a.gum_cnt[w] = 0u;
+            }
             if (a.kseq) {  // outputs [B]: the token and the accepted candidate's index
                 if (st) {
                     a.accepted_len[b] = -1;
@@ -144,12 +156,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
         base_units += tot_u;
         base_sunits += tot_s;
         base_funits += tot_f;
+        base_gunits += tot_g;
     }
     if (threadIdx.x == 0) {
         a.counts[kCntStreamRows] = base_rows;
         a.counts[kCntDenseUnits] = base_units;
         a.counts[kCntStreamUnits] = base_sunits;
         a.counts[kCntFreeUnits] = base_funits;
+        a.counts[kCntGumUnits] = base_gunits;
         a.counts[kCntFreeNext] = 0u;
         a.counts[kCntPieceNext] = 0u;
         a.counts[kCntError] = 0u;
@@ -186,6 +200,7 @@ DeviceInfo device_info(int dev) {
 
 cudaError_t launch_all(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, const sv_options& o) {
     cudaError_t e;
+    if (a.gumbel && (e = launch_gumbel_kernel(dtype, vector, a, sms, s, o.ev_gumbel)) != cudaSuccess) return e;
     if ((e = launch_stream_kernel(dtype, vector, a, sms, s, o.ev_stream)) != cudaSuccess) return e;
     if ((e = launch_free_kernel(dtype, vector, a, sms, s, o.ev_free)) != cudaSuccess) return e;
     if (o.ev_dense[0]) cudaEventRecord((cudaEvent_t)o.ev_dense[0], s);
@@ -303,6 +318,9 @@ int verify_call(const void* target_logits, const void* draft_logits, int dtype, 
     a.free_rec = (FreeRec*)(ws + L.free_rec);
     a.free_blk = (float*)(ws + L.free_blk);
     a.free_nblk = L.free_nblk;
+    a.gum_units = (uint32_t*)(ws + L.gum_units);
+    a.gum_key = (unsigned long long*)(ws + L.gum_key);
+    a.gum_cnt = (uint32_t*)(ws + L.gum_cnt);
 
     const size_t es = dtype == SV_BF16 ? 2 : 4;
     if (a.p_out && cudaMemsetAsync(a.p_out, 0, sizeof(float) * (size_t)B * (gamma_max + 1) * V, s) != cudaSuccess)
@@ -351,8 +369,7 @@ extern "C" int spec_verify_kseq(const void* target_logits, const void* draft_log
         if (options->struct_size < sizeof(uint32_t)) return SV_EINVAL;
         memcpy(&opt, options, options->struct_size < sizeof opt ? options->struct_size : sizeof opt);
     }
-    opt.struct_size = sizeof opt;
-    opt.path = SV_PATH_DENSE;
+    opt.struct_size = sizeof opt;  // path is the caller's: SV_PATH_DENSE sends every row to the cluster kernel
     opt.pos_accept = nullptr;
     opt.pos_token = nullptr;
     opt.lenience = nullptr;

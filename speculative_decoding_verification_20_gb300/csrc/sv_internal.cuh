@@ -66,12 +66,14 @@ enum : int {
     kCntPieceNext = 3,
     kCntError = 4,
     kCntFreeUnits = 5,
-    kCntFreeNext = 6
+    kCntFreeNext = 6,
+    kCntGumUnits = 7
 };
 
 // streaming top-k path; cluster path (top-k > 256, and handed-over units);
-// whole-row path of rows with no top-k (with or without top-p)
-enum : uint32_t { kModeErr = 0, kModeStream = 1, kModeDense = 2, kModeFree = 3 };
+// whole-row path of rows with no top-k (with or without top-p); shared-noise
+// rows with no filter at all (one pass of noise and argmax)
+enum : uint32_t { kModeErr = 0, kModeStream = 1, kModeDense = 2, kModeFree = 3, kModeGumbel = 4 };
 
 // Per-unit record of the free kernel for its tail kernel (one per entry of the
 // free unit list).  flags: kRecDead (a row without a finite logit, or with a
@@ -142,11 +144,14 @@ struct Args {
     float* free_blk;          // [units][2][free_nblk]: per block sums of r (residual weights) and p
     int free_nblk;            // blocks per row of the free kernel's variant (set by its launcher)
     int free_warps;           // consumer warps of that variant (set by its launcher)
+    uint32_t* gum_units;      // shared-noise rows with no filter: (b << 8) | position
+    unsigned long long* gum_key;  // [gum units] best (score, id) key so far (score_key; 0 = none)
+    uint32_t* gum_cnt;        // [gum units] CTAs done with their part of the unit's row
 };
 
 struct WsLayout {
     size_t seq, seq_done, seq_status, unit_acc, unit_tok, stream_rows, dense_units, stream_units, free_units,
-        counts, cand, cand_cnt, free_rec, free_blk, total;
+        counts, cand, cand_cnt, free_rec, free_blk, gum_units, gum_key, gum_cnt, total;
     int ppr, free_nblk;
     int cand_rowcap;  // candidate entries per stream row: kListCap per piece, the last piece min(kListCap, its length)
 };
@@ -194,6 +199,9 @@ __host__ __device__ inline WsLayout ws_layout(int B, int G, int V, int dtype) {
                       : free_blocks(V, dtype, kFreeWarpsWide);  // room for either variant
     L.free_rec = o;    o = align_up(o + sizeof(FreeRec) * units, 256);
     L.free_blk = o;    o = align_up(o + 4 * units * 2 * (size_t)L.free_nblk, 256);
+    L.gum_units = o;   o = align_up(o + 4 * units, 256);
+    L.gum_key = o;     o = align_up(o + 8 * units, 256);
+    L.gum_cnt = o;     o = align_up(o + 4 * units, 256);
     L.total = o;
     return L;
 }
@@ -369,6 +377,7 @@ inline cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
 }
 cudaError_t launch_combine_kernel(int dtype, const Args& a, int sms, cudaStream_t s);
 cudaError_t launch_free_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, void* const ev[2]);
+cudaError_t launch_gumbel_kernel(int dtype, bool vector, const Args& a, int sms, cudaStream_t s, void* const ev[2]);
 cudaError_t launch_dense_f32(bool vector, const Args& a, int sms, cudaStream_t s);
 cudaError_t launch_dense_bf16(bool vector, const Args& a, int sms, cudaStream_t s);
 

@@ -150,3 +150,35 @@ def test_target_token_follows_p_chisquare(k, p_top):
     assert counts[~support].sum() == 0
     _, pval = stats.chisquare(counts[support], p_law[support] / p_law[support].sum() * B)
     assert pval > 1e-3, (counts / B, p_law, pval)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [3, 37, 1001, 4099, 40000])
+def test_one_pass_rows_every_vocab_and_part_boundary(dtype, V):
+    """Rows with no filter take the one-pass kernel, which cuts the batch's rows into
+    equal parts that start and end inside rows: vocabularies that are not a multiple
+    of the 16-byte vector (scalar loads), tiny rows (many rows per part) and wide ones
+    (several parts per row), with ragged gamma."""
+    from tests.test_parity_gpu import _rand_batch
+    B, G = 40, 4
+    nd = torch.tensor([1 + (b % G) for b in range(B)], dtype=torch.int32)
+    wl = _rand_batch(B, G, V, dtype, seed=V + 1, T=np.linspace(0.5, 1.5, B), nd=nd)
+    rep = ParityReport()
+    for seed in (3, 4):
+        run_gumbel(wl, seed, rep=rep)
+    assert_ok(rep)
+
+
+def test_one_pass_rows_mixed_with_every_other_path():
+    """A batch mixing unfiltered rows (one-pass kernel) with greedy and top-k rows
+    (streaming), top-p rows (whole-row kernel) and top-k > 256 rows (cluster kernel)."""
+    from tests.test_parity_gpu import _rand_batch
+    B, G, V = 30, 3, 5000
+    wl = _rand_batch(B, G, V, "bf16", seed=21)
+    wl.temperature = torch.tensor([1.0, 0.0, 0.8, 1.2, 1.0] * 6)
+    wl.top_k = torch.tensor([0, 0, 40, 0, 600] * 6, dtype=torch.int32)
+    wl.top_p = torch.tensor([1.0, 1.0, 1.0, 0.9, 1.0] * 6, dtype=torch.float32)
+    rep = ParityReport()
+    for seed in (8, 9):
+        run_gumbel(wl, seed, rep=rep)
+    assert_ok(rep)
