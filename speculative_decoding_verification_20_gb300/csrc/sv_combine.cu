@@ -244,7 +244,9 @@ __device__ void normalise_kept(const unsigned long long* top, int k, float Tf, f
 // then top-p) and the index by token id.
 template <typename TIn>
 __device__ void combine_row(const Args& a, const SeqInfo& si, int unit, int r, CombPair& sm, int lane) {
-    const uint32_t slot = si.row_off + (r == 0 ? (uint32_t)unit : (uint32_t)si.gamma + 1u + (uint32_t)unit);
+    // K-SEQ rows are one target and one draft row per sequence
+    const uint32_t slot = si.row_off + (a.kseq ? (uint32_t)r
+                                               : r == 0 ? (uint32_t)unit : (uint32_t)si.gamma + 1u + (uint32_t)unit);
     const int kk = row_topk<Elem<TIn>::KB>(a, slot, si.k, sm.buf[r], sm.top[r], lane);  // ties to the lower id
     // a row without a finite logit (non-finite ones are already flagged)
     const uint32_t ninf_key = Elem<TIn>::key(Elem<TIn>::kNegInfBits);
@@ -397,6 +399,124 @@ __device__ void gumbel_unit(const Args& a, int b, int unit, const SeqInfo& si, C
     unit_finished_warp(a, b, lane);
 }
 
+// K-SEQ verification of one position ("SpecTr: Fast Speculative Decoding via
+// Optimal Transport" page, section K-SEQ, eqs. (4)-(7) and the residual
+// distribution; p = target, q = draft here) for rows with top-k <= 256 or
+// greedy: both rows are supported on their kept lists, so everything below
+// runs on one warp over at most 256 tokens.  With m(x) = min(q(x), p(x) / rho)
+// and beta(rho) = sum_x m(x) (only tokens kept by both rows add to it):
+//   rho* is the root on [1, k] of f(rho) = 1 - (1 - beta)^k - rho beta, which
+//     does not increase with rho: bisection, keeping the end where f <= 0;
+//   candidate i (in the given order, uniform U(seed, b, 1, 3 + i)) is accepted
+//     iff u_i rho* q(X_i) < p(X_i); the first accepted one is emitted;
+//   otherwise the token is drawn from p - A, A = (P_A / beta) m at rho*,
+//     P_A = 1 - (1 - beta)^k, by the inverse CDF in ascending token id with
+//     U(seed, b, 1, 1) (p itself when the residual has no mass).
+template <typename TIn>
+__device__ void kseq_list_unit(const Args& a, int b, const SeqInfo& si, CombPair& sm, int lane) {
+    const int kt = sm.kept[0], kd = sm.kept[1], k = si.gamma;
+    uint32_t st = __ldcg(&a.seq_status[b]);  // a NaN or +inf logit seen by the select kernel
+    if (kt < 0 || kd < 0) st |= SV_ROW_NONFINITE;
+    if (st) {
+        if (lane == 0) {
+            a.out_tokens[b] = -1;
+            a.accepted_len[b] = -1;
+            if (a.row_status) a.row_status[b] = st;
+        }
+        return;
+    }
+    // the draft probability of each of the target's kept tokens (in the draft row's
+    // free scratch; 0 where the draft does not keep it)
+    float* qk = reinterpret_cast<float*>(sm.buf[1]);
+    for (int j = lane; j < kt; j += 32)
+        qk[j] = sm.prob[0][j] > 0.0f ? prob_of(sm.byid[1], sm.prob[1], kd, comp_id(sm.top[0][j])) : 0.0f;
+    __syncwarp();
+    auto beta_at = [&](double rho) -> double {  // compensated fp32 sum over the warp
+        const float inv = (float)(1.0 / rho);
+        CF s{0.0f, 0.0f};
+        for (int j = lane; j < kt; j += 32) s = cf_add(s, CF{fminf(qk[j], sm.prob[0][j] * inv), 0.0f});
+        s = warp_cf_sum(s);
+        return (double)s.s - (double)s.c;
+    };
+    auto one_minus_pow = [&](double beta) -> double {  // 1 - (1 - beta)^k, k <= 13 products
+        double pw = 1.0;
+        for (int i = 0; i < k; ++i) pw *= (1.0 - beta);
+        return 1.0 - pw;
+    };
+    double lo = 1.0, hi = (double)k;
+    for (int it = 0; it < 48 && hi - lo > 1e-13 * hi; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        const double be = beta_at(mid);
+        if (one_minus_pow(be) - mid * be > 0.0)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const double rho = hi, beta = beta_at(hi);
+
+    // the candidates, one per lane: the lowest index that passes wins
+    int idx = -1, token = -1;
+    {
+        bool pass = false;
+        int x = 0;
+        if (lane < k) {
+            x = a.draft_tokens[(size_t)b * a.G + lane];
+            const double px = (double)prob_of(sm.byid[0], sm.prob[0], kt, x);
+            const double qx = (double)prob_of(sm.byid[1], sm.prob[1], kd, x);
+            const double u = uniform01(a.seed, (uint32_t)b, 1u, 3u + (uint32_t)lane);
+            pass = u * rho * qx < px;
+        }
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
+        if (m) {
+            idx = __ffs(m) - 1;
+            token = __shfl_sync(0xFFFFFFFFu, x, idx);
+        }
+    }
+    if (idx < 0) {
+        // the residual p - A at rho*, in ascending token id over the target's kept set
+        const double PA = beta > 0.0 ? one_minus_pow(beta) : 0.0;
+        const float As = beta > 0.0 ? (float)(PA / beta) : 0.0f;
+        const float inv_rho = (float)(1.0 / rho);
+        float* rr = reinterpret_cast<float*>(sm.buf[0]);
+        CF Z{0.0f, 0.0f}, Zp{0.0f, 0.0f};
+        for (int j = lane; j < kt; j += 32) {
+            const unsigned long long e = sm.byid[0][j];
+            const float p = sm.prob[0][(uint32_t)e];
+            const float q = prob_of(sm.byid[1], sm.prob[1], kd, (int)(e >> 32));
+            const float r = fmaxf(p - As * fminf(q, p * inv_rho), 0.0f);
+            rr[j] = r;
+            Z = cf_add(Z, CF{r, 0.0f});
+            Zp = cf_add(Zp, CF{p, 0.0f});
+        }
+        float Zt = cf_val(warp_cf_sum(Z));
+        if (!(Zt > 0.0f)) {  // no residual mass (P_A = 1 up to rounding): draw from p
+            Zt = cf_val(warp_cf_sum(Zp));
+            for (int j = lane; j < kt; j += 32) rr[j] = sm.prob[0][(uint32_t)sm.byid[0][j]];
+        }
+        __syncwarp();
+        const double v = uniform01(a.seed, (uint32_t)b, 1u, 1u) * (double)Zt;
+        int last_pos = -1;
+        CF carry{0.0f, 0.0f};
+        for (int c0 = 0; c0 < kt && token < 0; c0 += 32) {
+            const int j = c0 + lane;
+            const float r = j < kt ? rr[j] : 0.0f;
+            const CF xs = cf_add(carry, warp_cf_scan(CF{r, 0.0f}, lane));
+            const unsigned pos = __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0f);
+            if (pos) last_pos = c0 + 31 - __clz(pos);
+            const unsigned hit =
+                __ballot_sync(0xFFFFFFFFu, j < kt && r > 0.0f && (double)xs.s - (double)xs.c > v);
+            if (hit) token = (int)(sm.byid[0][c0 + __ffs(hit) - 1] >> 32);
+            carry = CF{__shfl_sync(0xFFFFFFFFu, xs.s, 31), __shfl_sync(0xFFFFFFFFu, xs.c, 31)};
+        }
+        if (token < 0 && last_pos >= 0) token = (int)(sm.byid[0][last_pos] >> 32);
+    }
+    if (lane == 0) {
+        a.out_tokens[b] = token;
+        a.accepted_len[b] = idx;
+        if (a.row_status) a.row_status[b] = 0u;
+    }
+}
+
 // named barrier of warp pair pr (ids 1 and 2; the ids are constants so the
 // kernel holds only the barriers it uses)
 __device__ __forceinline__ void pair_sync(int pr) {
@@ -410,7 +530,9 @@ __device__ __forceinline__ void pair_sync(int pr) {
 // the two rows are selected and normalised at the same time
 // 7 CTAs (14 units) per SM: the whole unit list of a 256-sequence, 8-unit batch
 // in one wave on 152 SMs (shared memory 7 x 29 KB, at most 73 registers)
-template <typename TIn>
+// KSEQ: the K-SEQ instantiation (a.kseq), kept apart so the sampling path's
+// register allocation does not carry it
+template <typename TIn, bool KSEQ>
 __global__ void __launch_bounds__(kCombineThreads, 7) combine_kernel(Args a) {
     extern __shared__ __align__(16) uint8_t comb_raw[];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -428,9 +550,24 @@ __global__ void __launch_bounds__(kCombineThreads, 7) combine_kernel(Args a) {
         const SeqInfo si = a.seq[b];
         if (failed) {  // a select CTA gave up waiting: no result of this call can be trusted
             if (r == 0) {
-                if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_INTERNAL);
-                unit_finished_warp(a, b, lane);
+                if (KSEQ) {  // K-SEQ outputs are per row, written here
+                    if (lane == 0) {
+                        a.out_tokens[b] = -1;
+                        a.accepted_len[b] = -1;
+                        if (a.row_status) a.row_status[b] = __ldcg(&a.seq_status[b]) | SV_ROW_INTERNAL;
+                    }
+                } else {
+                    if (lane == 0) atomicOr(&a.seq_status[b], SV_ROW_INTERNAL);
+                    unit_finished_warp(a, b, lane);
+                }
             }
+            continue;
+        }
+        if constexpr (KSEQ) {  // both rows of the position, then the K-SEQ step on the first warp
+            combine_row<TIn>(a, si, 0, r, sm, lane);
+            pair_sync(pr);
+            if (r == 0) kseq_list_unit<TIn>(a, b, si, sm, lane);
+            pair_sync(pr);
             continue;
         }
         // the draft token, loaded early: its latency hides behind the row work
@@ -449,9 +586,9 @@ __global__ void __launch_bounds__(kCombineThreads, 7) combine_kernel(Args a) {
 }
 
 namespace {
-template <typename TIn>
+template <typename TIn, bool KSEQ>
 cudaError_t launch_comb_t(const Args& a, int sms, cudaStream_t s) {
-    auto comb = combine_kernel<TIn>;
+    auto comb = combine_kernel<TIn, KSEQ>;
     const int csmem = (int)((kCombineWarps / 2) * sizeof(CombPair));
     static const bool cattr_ok = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem) ==
                                  cudaSuccess;
@@ -469,7 +606,9 @@ cudaError_t launch_comb_t(const Args& a, int sms, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_combine_kernel(int dtype, const Args& a, int sms, cudaStream_t s) {
-    return dtype == SV_BF16 ? launch_comb_t<__nv_bfloat16>(a, sms, s) : launch_comb_t<float>(a, sms, s);
+    if (a.kseq)
+        return dtype == SV_BF16 ? launch_comb_t<__nv_bfloat16, true>(a, sms, s) : launch_comb_t<float, true>(a, sms, s);
+    return dtype == SV_BF16 ? launch_comb_t<__nv_bfloat16, false>(a, sms, s) : launch_comb_t<float, false>(a, sms, s);
 }
 
 }  // namespace sv

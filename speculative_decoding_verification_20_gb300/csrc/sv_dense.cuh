@@ -959,21 +959,33 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
     c.cl.sync();
 }
 
-// vocabulary split: load groups per thread R and cluster size, smallest R first
+// Vocabulary split: load groups per thread R and cluster size cs (R * cs is
+// about V / 2048 for bf16, V / 1024 for fp32).  A unit's time is mostly its
+// rounds of cluster-wide exchanges, so the smallest R (the shortest per-thread
+// loops) serves a batch whose units fit the GPU's clusters at once; a batch with
+// more units than that takes the largest R, whose smaller clusters run more
+// units side by side (the batch's unit count is an upper bound: the plan picks
+// the units on the device).
 template <typename TIn>
-inline bool dense_shape(int V, int* R, int* cs) {
+inline bool dense_shape(int V, long long units, int sms, int* R, int* cs) {
     const int vec = 16 / (int)sizeof(TIn);
     const int rmax = sizeof(TIn) == 2 ? 8 : 16;
+    int n = 0, rs[8], cl[8];
     for (int r = 1; r <= rmax; r <<= 1) {
         const int w = kDenseThreads * r * vec;
         const int c = (V + w - 1) / w;
         if (c <= 8 || (r == rmax && c <= 16)) {
-            *R = r;
-            *cs = c;
-            return true;
+            rs[n] = r;
+            cl[n] = c;
+            ++n;
         }
     }
-    return false;
+    if (n == 0) return false;
+    int pick = 0;
+    if (units > (long long)(sms / cl[0])) pick = n - 1;
+    *R = rs[pick];
+    *cs = cl[pick];
+    return true;
 }
 
 // Persistent launch: as many clusters as fit on the GPU at once, each walking

@@ -10,7 +10,8 @@ cudaError_t launch_r(const Args& a, int cs, int sms, cudaStream_t s) { return la
 template <bool VECTOR>
 cudaError_t launch_v(const Args& a, int sms, cudaStream_t s) {
     int R = 0, cs = 0;
-    if (!dense_shape<__nv_bfloat16>(a.V, &R, &cs)) return cudaErrorInvalidValue;
+    const long long units = a.kseq ? (long long)a.B : (long long)a.B * (a.G + 1);
+    if (!dense_shape<__nv_bfloat16>(a.V, units, sms, &R, &cs)) return cudaErrorInvalidValue;
     switch (R) {
         case 1: return launch_r<1, VECTOR>(a, cs, sms, s);
         case 2: return launch_r<2, VECTOR>(a, cs, sms, s);

@@ -790,8 +790,9 @@ __device__ __noinline__ bool redo_piece(SelSmem& sm, GSync& g, const Args& a, in
     const uint32_t item = a.stream_rows[(uint32_t)w / (uint32_t)a.ppr];
     const int r = (int)(item & 0xFFu);
     const int gamma = a.seq[b].gamma;
-    const TIn* row = (r <= gamma) ? (const TIn*)a.target + ((size_t)b * (G + 1) + r) * (size_t)V
-                                  : (const TIn*)a.draft + ((size_t)b * G + (r - gamma - 1)) * (size_t)V;
+    const TIn* row = a.kseq ? (const TIn*)(r == 0 ? a.target : a.draft) + (size_t)b * V  // K-SEQ: [B, V] rows
+                     : (r <= gamma) ? (const TIn*)a.target + ((size_t)b * (G + 1) + r) * (size_t)V
+                                    : (const TIn*)a.draft + ((size_t)b * G + (r - gamma - 1)) * (size_t)V;
     CState cs;
     cs.spec = false;
     uint4 v[kTileBytes / 16 / kConsumers];
@@ -869,8 +870,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(Args a) {
                 }
                 const uint32_t row_slot = w / (uint32_t)ppr;
                 const int piece = (int)(w - row_slot * (uint32_t)ppr);
-                const TIn* row = (r <= gamma) ? (const TIn*)a.target + ((size_t)b * (G + 1) + r) * (size_t)V
-                                              : (const TIn*)a.draft + ((size_t)b * G + (r - gamma - 1)) * (size_t)V;
+                const TIn* row =
+                    a.kseq ? (const TIn*)(r == 0 ? a.target : a.draft) + (size_t)b * V  // K-SEQ: [B, V] rows
+                    : (r <= gamma) ? (const TIn*)a.target + ((size_t)b * (G + 1) + r) * (size_t)V
+                                   : (const TIn*)a.draft + ((size_t)b * G + (r - gamma - 1)) * (size_t)V;
                 const int c0 = piece * PE, c1 = min(V, c0 + PE);
                 for (int col = c0, tile = 0; col < c1 && ok; col += TE, ++tile) {
                     const int n = min(TE, c1 - col);

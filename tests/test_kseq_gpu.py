@@ -70,14 +70,14 @@ def _row_margins(ni, b, seed, k):
     return out
 
 
-def run_kseq(wl, seed, rep=None):
+def run_kseq(wl, seed, rep=None, path="auto"):
     rep = rep or ParityReport()
     ni = wl.numpy_inputs()
     dev = torch.device("cuda")
     g = sv.spec_verify_kseq(wl.target.to(dev), wl.draft.to(dev), wl.candidates.to(dev), wl.temperature.to(dev),
                             None if wl.num_candidates is None else wl.num_candidates.to(dev),
                             None if wl.top_k is None else wl.top_k.to(dev),
-                            None if wl.top_p is None else wl.top_p.to(dev), seed=seed)
+                            None if wl.top_p is None else wl.top_p.to(dev), seed=seed, path=path)
     torch.cuda.synchronize()
     tok, acc, st = oracle.kseq_verify(ni["target"], ni["draft"], ni["candidates"], ni["temperature"],
                                       ni["num_candidates"], ni["top_k"], ni["top_p"], seed=seed)
@@ -127,7 +127,8 @@ def test_kseq_parity_small(K, V, dtype):
     assert_ok(rep)
 
 
-def test_kseq_parity_filters_and_greedy():
+@pytest.mark.parametrize("path", ["auto", "dense"])
+def test_kseq_parity_filters_and_greedy(path):
     wl = _batch(40, 5, 3000, "f32", seed=7, T=[0.0, 0.5, 1.0, 1.3] * 10, k=None, p=None)
     wl.top_k = torch.tensor([0, 3, 50, 0, 300] * 8, dtype=torch.int32)
     wl.top_p = torch.tensor([1.0, 0.9, 0.95, 0.5] * 10, dtype=torch.float32)
@@ -136,8 +137,36 @@ def test_kseq_parity_filters_and_greedy():
     gen = torch.Generator().manual_seed(3)
     wl.candidates = workloads._propose(wl.draft.unsqueeze(1).expand(40, 5, 3000), wl.temperature, wl.top_k,
                                        wl.top_p, gen)
-    rep, _ = run_kseq(wl, 9)
+    rep, _ = run_kseq(wl, 9, path=path)
     assert_ok(rep)
+
+
+@pytest.mark.parametrize("K", [1, 4, 13])
+@pytest.mark.parametrize("V,dtype,k", [(37, "f32", 5), (1000, "f32", 256), (4096, "bf16", 40), (50000, "bf16", 64)])
+def test_kseq_parity_kept_lists(K, V, dtype, k):
+    """Top-k rows: rho* and the draws over the two rows' kept lists (streaming path),
+    against the oracle and against the cluster kernel on the same inputs."""
+    wl = _batch(48, K, V, dtype, seed=V + K + k, T=np.linspace(0.4, 1.6, 48), k=k,
+                p=0.9 if V > 100 else None)
+    rep = ParityReport()
+    for seed in (1, 2):
+        _, g = run_kseq(wl, seed, rep)
+        _, gd = run_kseq(wl, seed, ParityReport(), path="dense")
+        # the two paths agree wherever neither is a margin case (checked against the oracle above)
+        same = (to_np(g["out_token"]) == to_np(gd["out_token"])).mean()
+        assert same > 0.9, same
+    assert_ok(rep)
+
+
+def test_kseq_invalid_rows_on_the_list_path():
+    wl = _batch(6, 3, 500, "f32", seed=5, k=20)
+    wl.target[1, 7] = float("nan")
+    wl.draft[2, :] = float("-inf")
+    wl.target[3, 11] = float("inf")
+    rep, g = run_kseq(wl, 3)
+    assert_ok(rep)
+    st = to_np(g["row_status"])
+    assert (st[1:4] != 0).all() and st[0] == 0 and (st[4:] == 0).all()
 
 
 @pytest.mark.parametrize("name,kw", [("kseq32k", dict(B=64)), ("kseq128k", dict(B=12))])
