@@ -425,34 +425,62 @@ __device__ void kseq_list_unit(const Args& a, int b, const SeqInfo& si, CombPair
         }
         return;
     }
-    // the draft probability of each of the target's kept tokens (in the draft row's
-    // free scratch; 0 where the draft does not keep it)
+    // the draft probability of each of the target's kept tokens, and the target
+    // probability of each of the draft's (in the draft row's free scratch; 0 where
+    // the other row does not keep the token)
     float* qk = reinterpret_cast<float*>(sm.buf[1]);
+    float* pk = qk + kStreamMaxK;
     for (int j = lane; j < kt; j += 32)
         qk[j] = sm.prob[0][j] > 0.0f ? prob_of(sm.byid[1], sm.prob[1], kd, comp_id(sm.top[0][j])) : 0.0f;
+    for (int j = lane; j < kd; j += 32)
+        pk[j] = sm.prob[1][j] > 0.0f ? prob_of(sm.byid[0], sm.prob[0], kt, comp_id(sm.top[1][j])) : 0.0f;
     __syncwarp();
-    auto beta_at = [&](double rho) -> double {  // compensated fp32 sum over the warp
-        const float inv = (float)(1.0 / rho);
+    // compensated fp32 sums over the warp of beta = sum min(q, p / rho),
+    // R = sum (p - rho q)+ (= 1 - rho beta) and D = sum (q - p / rho)+ (= 1 - beta)
+    auto wsum = [&](CF s) -> float { return cf_val(warp_cf_sum(s)); };
+    auto beta_f = [&](float inv) {
+        CF s{0.0f, 0.0f};
+        for (int j = lane; j < kt; j += 32) s = cf_add(s, CF{fminf(qk[j], sm.prob[0][j] * inv), 0.0f});
+        return wsum(s);
+    };
+    // rho*: bisection on [1, k] with the sign of f taken in fp32 from a form without
+    // cancellation (dependent fp64 operations are slow on this GPU): for beta <= 1/2,
+    // f = 1 - (1 - beta)^k - rho beta = -expm1(k log1p(-beta)) - rho beta, each term
+    // accurate to its own size; above, f = R - D^k, two sums of nonnegative terms.
+    // Both are accurate relative to f's terms, so a sign is wrong only within about
+    // 1e-7 (relative) of the root; the end where f <= 0 is kept, as the page's
+    // bisection does
+    double lo = 1.0, hi = (double)k;
+    for (int it = 0; it < 40 && k > 1 && hi - lo > 5.9604644775390625e-8 * hi; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        const float r = (float)mid, inv = 1.0f / r;
+        const float be = beta_f(inv);
+        float fv;
+        if (be <= 0.5f) {
+            fv = -expm1f((float)k * log1pf(-be)) - r * be;
+        } else {
+            CF sr{0.0f, 0.0f}, sd{0.0f, 0.0f};
+            for (int j = lane; j < kt; j += 32) sr = cf_add(sr, CF{fmaxf(sm.prob[0][j] - r * qk[j], 0.0f), 0.0f});
+            for (int j = lane; j < kd; j += 32) sd = cf_add(sd, CF{fmaxf(sm.prob[1][j] - pk[j] * inv, 0.0f), 0.0f});
+            const float R = wsum(sr), D = wsum(sd);
+            float pw = 1.0f;
+            for (int i = 0; i < k; ++i) pw *= D;
+            fv = R - pw;
+        }
+        if (fv > 0.0f)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const double rho = k > 1 ? hi : 1.0;
+    auto beta_at = [&](double x) -> double {
+        const float inv = (float)(1.0 / x);
         CF s{0.0f, 0.0f};
         for (int j = lane; j < kt; j += 32) s = cf_add(s, CF{fminf(qk[j], sm.prob[0][j] * inv), 0.0f});
         s = warp_cf_sum(s);
         return (double)s.s - (double)s.c;
     };
-    auto one_minus_pow = [&](double beta) -> double {  // 1 - (1 - beta)^k, k <= 13 products
-        double pw = 1.0;
-        for (int i = 0; i < k; ++i) pw *= (1.0 - beta);
-        return 1.0 - pw;
-    };
-    double lo = 1.0, hi = (double)k;
-    for (int it = 0; it < 48 && hi - lo > 1e-13 * hi; ++it) {
-        const double mid = 0.5 * (lo + hi);
-        const double be = beta_at(mid);
-        if (one_minus_pow(be) - mid * be > 0.0)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    const double rho = hi, beta = beta_at(hi);
+    const double beta = beta_at(rho);
 
     // the candidates, one per lane: the lowest index that passes wins
     int idx = -1, token = -1;
@@ -474,7 +502,9 @@ __device__ void kseq_list_unit(const Args& a, int b, const SeqInfo& si, CombPair
     }
     if (idx < 0) {
         // the residual p - A at rho*, in ascending token id over the target's kept set
-        const double PA = beta > 0.0 ? one_minus_pow(beta) : 0.0;
+        double omb_k = 1.0;  // (1 - beta)^k, k <= 13 products, once
+        for (int i = 0; i < k; ++i) omb_k *= (1.0 - beta);
+        const double PA = beta > 0.0 ? 1.0 - omb_k : 0.0;
         const float As = beta > 0.0 ? (float)(PA / beta) : 0.0f;
         const float inv_rho = (float)(1.0 / rho);
         float* rr = reinterpret_cast<float*>(sm.buf[0]);
