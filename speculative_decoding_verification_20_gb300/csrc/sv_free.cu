@@ -599,6 +599,11 @@ __global__ void __launch_bounds__(FGeo<W>::kThreads, FGeo<W>::kCtasPerSm) free_k
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int V = a.V, G = a.G;
     const int ntiles = (V + TS - 1) / TS;
+    // No unit on this path: leave at once, without waiting for the kernels before
+    // this one.  The count is the plan's, final and visible here: this kernel is
+    // launched only once every CTA of the previous one has passed its own wait,
+    // which the plan's completion precedes.  Nothing here reads their results.
+    if (a.counts[kCntFreeUnits] == 0u) return;
 
     if (t == 0) {
         for (int s = 0; s < kFStages; ++s) {
@@ -1136,6 +1141,7 @@ __global__ void __launch_bounds__(32 * kTailWarps) free_tail_kernel(Args a) {
     constexpr int NCH = BS / CH;
     static_assert(NCH * CH == BS, "block geometry");
     const int lane = threadIdx.x & 31;
+    if (a.counts[kCntFreeUnits] == 0u) return;  // no unit: no wait (the plan's count, as in free_kernel)
     grid_dependency_wait();  // the free kernel's records
     grid_dependents_go();
     const uint32_t n_units = a.counts[kCntFreeUnits];
