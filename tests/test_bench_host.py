@@ -59,3 +59,38 @@ def test_kernel_hash_covers_each_kernels_sources():
         assert all(os.path.exists(os.path.join(ROOT, f)) for f in files)
         assert len(bench.kernel_hash(path)) == 16
     assert bench.kernel_hash("stream") != bench.kernel_hash("free")
+
+
+def test_bytes_by_path_shared_noise_splits_unfiltered_rows():
+    """Under the shared-noise rule only the gamma_b + 1 target rows are read; rows
+    with neither top-k nor top-p (T > 0) take the one-pass kernel, top-p rows the
+    whole-row kernel, greedy and top-k rows the streaming path."""
+    wl = workloads.make("ragged", seed=0)
+    wl.top_p = torch.tensor([1.0 if b % 3 == 0 else 0.9 for b in range(wl.B)], dtype=torch.float32)
+    b = bench.bytes_by_path(wl, 256, "gumbel")
+    T = wl.temperature.numpy()
+    P = wl.top_p.numpy()
+    row = (wl.gammas() + 1) * wl.V * 4
+    assert b["stream"] == int(row[T == 0].sum())
+    assert b["gumbel"] == int(row[(T != 0) & (P >= 1.0)].sum()) > 0
+    assert b["free"] == int(row[(T != 0) & (P < 1.0)].sum()) > 0
+    assert b["dense"] == 0
+    assert "gumbel" not in bench.bytes_by_path(wl, 256)  # the sampling rule has no such path
+
+
+def test_launches_per_step_counts_the_one_pass_kernel():
+    assert bench.launches_per_step("sampling") == 6
+    assert bench.launches_per_step("gumbel") == 7
+    assert bench.launches_per_step("kseq") == 6
+
+
+def test_recorded_instructions_only_for_its_kernel_full_batch_and_sources():
+    with open(os.path.join(ROOT, "profiles", "instructions.json")) as f:
+        rec = json.load(f)
+    for key, r in rec.items():
+        rule, wl = key.split(":")
+        current = r["kernel_hash"] == bench.kernel_hash(r["path"])
+        assert bench.recorded_instructions(rule, wl, r["path"], True) == (
+            r["thread_inst_per_launch"] if current else None)
+        assert bench.recorded_instructions(rule, wl, r["path"], False) is None
+        assert bench.recorded_instructions(rule, wl, "stream", True) is None
