@@ -569,6 +569,11 @@ __global__ void __launch_bounds__(kCombineThreads, 7) combine_kernel(Args a) {
     const int pr = wid >> 1, r = wid & 1;
     CombPair& sm = reinterpret_cast<CombPair*>(comb_raw)[pr];
     constexpr int kPairs = kCombineWarps / 2;
+    // No streaming unit: leave at once, without waiting for the select kernel.  The
+    // count is the plan's, final and visible here: this kernel is launched only
+    // once every select CTA has passed its own wait, which the plan's completion
+    // precedes.
+    if (a.counts[kCntStreamUnits] == 0u) return;
     grid_dependency_wait();  // the select kernel's candidate lists
     grid_dependents_go();
     const uint32_t n_units = a.counts[kCntStreamUnits];
