@@ -48,7 +48,7 @@ __device__ __forceinline__ uint32_t block_excl_scan_1024(uint32_t v, uint32_t* s
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
     __shared__ uint32_t s_warp[32];
     grid_dependents_go();
-    uint32_t base_rows = 0, base_units = 0, base_sunits = 0, base_funits = 0, base_gunits = 0;
+    uint32_t base_rows = 0, base_units = 0, base_sunits = 0, base_funits = 0, base_gunits = 0, n_fnuc = 0;
     const int G = a.G, V = a.V;
     for (int b0 = 0; b0 < a.B; b0 += blockDim.x) {
         const int b = b0 + threadIdx.x;
@@ -102,12 +102,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
         const uint32_t nsunits = (mode == kModeStream) ? (a.kseq ? 1u : (uint32_t)(gamma + 1)) : 0u;
         const uint32_t nfunits = (mode == kModeFree) ? (uint32_t)(gamma + 1) : 0u;
         const uint32_t ngunits = (mode == kModeGumbel) ? (uint32_t)(gamma + 1) : 0u;
-        uint32_t tot_r, tot_u, tot_s, tot_f, tot_g;
+        const uint32_t nfnuc = (mode == kModeFree && P < 1.0f) ? nfunits : 0u;
+        uint32_t tot_r, tot_u, tot_s, tot_f, tot_g, tot_n;
         const uint32_t off_r = block_excl_scan_1024(nrows, s_warp, &tot_r);
         const uint32_t off_u = block_excl_scan_1024(nunits, s_warp, &tot_u);
         const uint32_t off_s = block_excl_scan_1024(nsunits, s_warp, &tot_s);
         const uint32_t off_f = block_excl_scan_1024(nfunits, s_warp, &tot_f);
         const uint32_t off_g = block_excl_scan_1024(ngunits, s_warp, &tot_g);
+        (void)block_excl_scan_1024(nfnuc, s_warp, &tot_n);
         if (b < a.B) {
             SeqInfo si;
             si.mode = mode;
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
         base_sunits += tot_s;
         base_funits += tot_f;
         base_gunits += tot_g;
+        n_fnuc += tot_n;
     }
     if (threadIdx.x == 0) {
         a.counts[kCntStreamRows] = base_rows;
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
         a.counts[kCntStreamUnits] = base_sunits;
         a.counts[kCntFreeUnits] = base_funits;
         a.counts[kCntGumUnits] = base_gunits;
+        a.counts[kCntFreeNucUnits] = n_fnuc;
         a.counts[kCntFreeNext] = 0u;
         a.counts[kCntPieceNext] = 0u;
         a.counts[kCntError] = 0u;

@@ -698,10 +698,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_kernel(Args a) {
     c.crank = (int)c.cl.block_rank();
     const int t = threadIdx.x;
     const int V = a.V, G = a.G;
-    // No unit from the plan and no whole-row unit that could be handed over: leave
-    // at once, without waiting for the kernels before this one (both counts are the
-    // plan's, final and visible here, as in free_kernel)
-    if (a.counts[kCntDenseUnits] == 0u && a.counts[kCntFreeUnits] == 0u) return;
+    // No unit from the plan and no whole-row unit that could be handed over (only
+    // nucleus units can be): leave at once, without waiting for the kernels before
+    // this one (both counts are the plan's, final and visible here, as in free_kernel)
+    if (a.counts[kCntDenseUnits] == 0u && a.counts[kCntFreeNucUnits] == 0u) return;
     grid_dependency_wait();  // the previous kernels of the call (the plan's lists, the handovers)
     const uint32_t n_units = a.counts[kCntDenseUnits];
     if (n_units == 0) return;  // nothing for any cluster: no shared memory is ever shared

@@ -67,7 +67,8 @@ enum : int {
     kCntError = 4,
     kCntFreeUnits = 5,
     kCntFreeNext = 6,
-    kCntGumUnits = 7
+    kCntGumUnits = 7,
+    kCntFreeNucUnits = 8  // whole-row units with top-p < 1: the only ones that can be handed over
 };
 
 // streaming top-k path; cluster path (top-k > 256, and handed-over units);
