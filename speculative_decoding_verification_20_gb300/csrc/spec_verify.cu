@@ -1,10 +1,11 @@
 // spec_verify.cu -- host side of the C ABI declared in include/spec_verify.h.
 //
 // Validates arguments on the host (nothing is enqueued on an error), then
-// enqueues on the caller's stream: plan kernel -> select (streaming top-k) ->
-// combine -> whole-row kernel -> its per-unit tail -> dense cluster kernel,
-// each after the plan as a programmatic dependent launch.  No host
-// synchronisation (spec_verify_host excepted).
+// enqueues on the caller's stream: plan kernel -> (shared-noise calls: the
+// one-pass kernel ->) select (streaming top-k) -> combine -> whole-row kernel ->
+// its per-unit tail -> dense cluster kernel, each after the plan as a
+// programmatic dependent launch.  No host synchronisation (spec_verify_host
+// excepted).
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -19,34 +20,51 @@ namespace sv {
 // ---------------------------------------------------------------------------
 // plan kernel: one CTA walks the batch in chunks of blockDim.x (<= 1024) sequences.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t block_excl_scan_1024(uint32_t v, uint32_t* s_warp, uint32_t* total) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    uint32_t x = v;
+// Exclusive block scans of N per-thread counts at once (thread order), with the
+// block totals; the N shuffle ladders run side by side.
+template <int N>
+__device__ __forceinline__ void block_excl_scan_n(const uint32_t (&v)[N], uint32_t (*s_warp)[N], uint32_t (&before)[N],
+                                                  uint32_t (&total)[N]) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+    uint32_t x[N];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) s_warp[wid] = x;
+    for (int i = 0; i < N; ++i) x[i] = v[i];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x[i], o);
+            if (lane >= o) x[i] += y;
+        }
+    if (lane == 31)
+#pragma unroll
+        for (int i = 0; i < N; ++i) s_warp[wid][i] = x[i];
     __syncthreads();
     if (wid == 0) {
-        uint32_t w = (lane < (int)(blockDim.x >> 5)) ? s_warp[lane] : 0u;
+        uint32_t w[N];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
-            if (lane >= o) w += y;
-        }
-        s_warp[lane] = w;  // inclusive warp-total prefix
+        for (int i = 0; i < N; ++i) w[i] = lane < nw ? s_warp[lane][i] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, w[i], o);
+                if (lane >= o) w[i] += y;
+            }
+#pragma unroll
+        for (int i = 0; i < N; ++i) s_warp[lane][i] = w[i];  // inclusive warp-total prefix
     }
     __syncthreads();
-    const uint32_t before = (wid > 0 ? s_warp[wid - 1] : 0u) + x - v;
-    *total = s_warp[(blockDim.x >> 5) - 1];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        before[i] = (wid > 0 ? s_warp[wid - 1][i] : 0u) + x[i] - v[i];
+        total[i] = s_warp[nw - 1][i];
+    }
     __syncthreads();
-    return before;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
-    __shared__ uint32_t s_warp[32];
+    __shared__ uint32_t s_warp[32][6];
     grid_dependents_go();
     uint32_t base_rows = 0, base_units = 0, base_sunits = 0, base_funits = 0, base_gunits = 0, n_fnuc = 0;
     const int G = a.G, V = a.V;
@@ -103,13 +121,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Args a) {
         const uint32_t nfunits = (mode == kModeFree) ? (uint32_t)(gamma + 1) : 0u;
         const uint32_t ngunits = (mode == kModeGumbel) ? (uint32_t)(gamma + 1) : 0u;
         const uint32_t nfnuc = (mode == kModeFree && P < 1.0f) ? nfunits : 0u;
-        uint32_t tot_r, tot_u, tot_s, tot_f, tot_g, tot_n;
-        const uint32_t off_r = block_excl_scan_1024(nrows, s_warp, &tot_r);
-        const uint32_t off_u = block_excl_scan_1024(nunits, s_warp, &tot_u);
-        const uint32_t off_s = block_excl_scan_1024(nsunits, s_warp, &tot_s);
-        const uint32_t off_f = block_excl_scan_1024(nfunits, s_warp, &tot_f);
-        const uint32_t off_g = block_excl_scan_1024(ngunits, s_warp, &tot_g);
-        (void)block_excl_scan_1024(nfnuc, s_warp, &tot_n);
+        // the six work lists' offsets and totals in one pass
+        const uint32_t cnt[6] = {nrows, nunits, nsunits, nfunits, ngunits, nfnuc};
+        uint32_t off[6], tot[6];
+        block_excl_scan_n<6>(cnt, s_warp, off, tot);
+        const uint32_t off_r = off[0], off_u = off[1], off_s = off[2], off_f = off[3], off_g = off[4];
+        const uint32_t tot_r = tot[0], tot_u = tot[1], tot_s = tot[2], tot_f = tot[3], tot_g = tot[4], tot_n = tot[5];
         if (b < a.B) {
             SeqInfo si;
             si.mode = mode;
